@@ -1,0 +1,303 @@
+"""Plain fp64 CPU oracle for Multi-Head Latent Attention decode with weight absorption.
+
+TEST INFRASTRUCTURE ONLY.  This module is imported by the test suite, by
+``__graft_entry__.smoke()`` and by the CPU-baseline leg of ``bench.py``.  The
+product path (the ``mla_latent_kv_70_b300`` package and its CUDA library) never
+imports, links or calls it, and it imports nothing from the product.
+
+Everything is float64 numpy.  Inputs arrive as float arrays whose values are the
+exact bf16 inputs of the GPU path (bf16 -> float64 is exact); nothing here rounds
+to a narrower type.  Dimensions are read from the array shapes, so the same code
+runs the pages' toy examples (d_c=3, d_k=d_r=2) and the DeepSeek-V3 shapes
+(d_c=512, d_r=64, d_nope=d_v=128).
+
+Pages cited (by title):
+  [MLA]     "Multi-Head Latent Attention (MLA)" (molayo1419.me)
+  [CALC]    "MLA의 계산: KV를 펼치지 않고 Attention하기" (ai-systems-engineering.com)
+  [ANATOMY] "DeepSeek Multi-Head Latent Attention(MLA) 아키텍처 해부" (blog.huny.dev)
+
+Readings taken where the pages are silent or disagree (each is also listed in the
+design notes): one score scale 1/sqrt(d_nope + d_r) ([CALC], "RoPE 경로를 분리한
+이유"); one decoupled RoPE key k^R shared by all heads, cached beside c^KV
+([CALC], Fig. 2; [ANATOMY] section 2); W_UK[h] and W_UV[h] stored as
+[d_c x d_k] matrices with K_h = C W_UK[h] ([MLA], "공식 정의"); RoPE on
+interleaved pairs with inverse frequency theta^(-2i/d_r) ([MLA], "구현",
+_apply_rope); natural-log LSE; an empty sequence gives o = 0 and lse = -inf.
+
+Parity pins for every function live in tests/test_oracle_pins.py; none of them is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "score_scale",
+    "rope_interleaved",
+    "absorb_q",
+    "visible_length",
+    "decode_expanded_seq",
+    "decode_absorbed_seq",
+    "decode_absorbed_partial_seq",
+    "combine_partials",
+    "out_proj_uv",
+    "gather_paged_rows",
+    "cache_values_per_token",
+    "cache_bytes_per_token",
+    "compression_ratio",
+    "full_cache_gib",
+]
+
+
+# ----------------------------------------------------------------------------
+# Scale and positions
+# ----------------------------------------------------------------------------
+
+def score_scale(d_nope: int, d_r: int) -> float:
+    """1 / sqrt(d_content + d_rope).
+
+    [CALC] "Content 점수와 위치 점수 합치기": the toy query/key have a 2-wide content
+    part and a 2-wide position part, so the scores are divided by sqrt(2+2) = 2.
+    [CALC] "RoPE 경로를 분리한 이유": after absorption the content dot runs in the
+    d_c-wide latent space, but the scale stays sqrt(d_content + d_rope), not
+    sqrt(d_c + d_rope), because the score itself is unchanged.
+    """
+    return 1.0 / math.sqrt(d_nope + d_r)
+
+
+def visible_length(T: int, S: int, s: int, causal: bool) -> int:
+    """Number of cached positions query token s (of S) may read.
+
+    The sequence holds T cached rows at positions 0..T-1 and the S query tokens
+    are its last S rows ([CALC] "계산 재배치의 효과와 한계": the current token's latent
+    is appended before attention and the token reads itself).  Without a mask
+    every query reads all T rows; with the causal mask of [CALC] "Content 점수와
+    위치 점수 합치기" (several tokens computed together must not read future
+    positions) query s sits at position T-S+s and reads rows 0..T-S+s.
+    """
+    if T <= 0:
+        return 0
+    if not causal:
+        return T
+    return max(0, min(T, T - S + s + 1))
+
+
+def rope_interleaved(x: np.ndarray, pos, theta: float = 10000.0) -> np.ndarray:
+    """Rotate interleaved pairs (x[2i], x[2i+1]) by angle pos * theta^(-2i/d).
+
+    [MLA] "구현" (_apply_rope): the inverse frequencies are theta^(-(0,2,4,..)/d_r),
+    the angle is position x inverse frequency, and the even/odd elements of the
+    last axis form the rotated pairs (x1 cos - x2 sin, x1 sin + x2 cos).
+    ``pos`` broadcasts against x[..., 0].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    if d % 2:
+        raise ValueError("rope width must be even")
+    inv_freq = np.power(float(theta), -np.arange(0, d, 2, dtype=np.float64) / d)
+    angle = np.asarray(pos, dtype=np.float64)[..., None] * inv_freq
+    cos, sin = np.cos(angle), np.sin(angle)
+    even, odd = x[..., 0::2], x[..., 1::2]
+    out = np.empty(np.broadcast_shapes(x.shape, angle.shape[:-1] + (d,)), dtype=np.float64)
+    out[..., 0::2] = even * cos - odd * sin
+    out[..., 1::2] = even * sin + odd * cos
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Key absorption (step a1)
+# ----------------------------------------------------------------------------
+
+def absorb_q(q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
+    """q_lat[..., h, :] = q_nope[..., h, :] . W_UK[h]^T.
+
+    [CALC] "Key 투영을 Query 쪽으로 옮기기" (Fig. 3): q (c_j U^K)^T = (q U^K^T) c_j^T,
+    so the per-head content query is mapped once into the latent space
+    (q~ = q U^K^T, 1 x d_c) instead of expanding every cached latent.
+    q_nope: [..., H, d_nope]; w_uk: [H, d_c, d_nope]  ->  [..., H, d_c].
+    """
+    q = np.asarray(q_nope, dtype=np.float64)
+    w = np.asarray(w_uk, dtype=np.float64)
+    return np.einsum("...hk,hck->...hc", q, w)
+
+
+# ----------------------------------------------------------------------------
+# The definition: textbook attention over expanded per-head K/V
+# ----------------------------------------------------------------------------
+
+def decode_expanded_seq(q_nope, q_rope, c_kv, k_rope, w_uk, w_uv, scale, causal=False):
+    """One sequence, expanded form (the definition the absorbed method must equal).
+
+    [MLA] "공식 정의": K_h = c^KV W_UK^(h), V_h = c^KV W_UV^(h).
+    [CALC] "Content 점수와 위치 점수 합치기" (Fig. 2): s_j = q^C_h . k^C_{j,h} + q^R_h . k^R_j
+    (no cross terms; k^R is shared by the heads), divided by the scale, softmax
+    over all readable positions (one softmax over the positions, not one per
+    position), then the attention weights mix the per-head values v_{j,h}; the
+    position key is never appended to the value.
+
+    q_nope [S,H,d_nope]; q_rope [S,H,d_r] (already rotated); c_kv [T,d_c];
+    k_rope [T,d_r] (already rotated); w_uk, w_uv [H,d_c,d_k].
+    Returns o [S,H,d_v] and lse [S,H] (natural log of sum_j exp(scale*s_j)).
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    KR = np.asarray(k_rope, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    S, H, _ = q_nope.shape
+    T = C.shape[0]
+    d_v = w_uv.shape[2]
+    o = np.zeros((S, H, d_v))
+    lse = np.full((S, H), -np.inf)
+    for h in range(H):
+        K_h = C @ w_uk[h]          # [T, d_k] content keys of head h
+        V_h = C @ w_uv[h]          # [T, d_v] values of head h
+        for s in range(S):
+            n = visible_length(T, S, s, causal)
+            if n == 0:
+                continue
+            x = (K_h[:n] @ q_nope[s, h] + KR[:n] @ q_rope[s, h]) * scale
+            m = x.max()
+            e = np.exp(x - m)
+            l = e.sum()
+            a = e / l
+            o[s, h] = a @ V_h[:n]
+            lse[s, h] = m + math.log(l)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------
+# The absorbed form (steps a2-a4): scores and aggregation in latent space
+# ----------------------------------------------------------------------------
+
+def decode_absorbed_partial_seq(q_lat, q_rope, c_kv, k_rope, scale, t0, t1, n_visible):
+    """Attention of every (s, h) over cached rows [t0, min(t1, n_visible[s])).
+
+    [CALC] "Key 투영을 Query 쪽으로 옮기기": content score = q~ . c_j read straight
+    from the latent cache; plus the position score q^R . k^R_j ("RoPE 경로를
+    분리한 이유": the position part is computed separately and added).
+    [CALC] "Value 투영을 가중합 뒤로 옮기기" (Fig. 4): z = a C, the latents mixed
+    with the attention weights, is returned as o_lat (U^V is applied later).
+
+    Returns (o_lat [S,H,d_c] normalised over the rows it saw, lse [S,H]); rows it
+    never saw give o_lat = 0, lse = -inf.
+    """
+    q_lat = np.asarray(q_lat, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    C = np.asarray(c_kv, np.float64)
+    KR = np.asarray(k_rope, np.float64)
+    S, H, d_c = q_lat.shape
+    o_lat = np.zeros((S, H, d_c))
+    lse = np.full((S, H), -np.inf)
+    for s in range(S):
+        hi = min(t1, n_visible[s])
+        if hi <= t0:
+            continue
+        Cs, KRs = C[t0:hi], KR[t0:hi]
+        x = (q_lat[s] @ Cs.T + q_rope[s] @ KRs.T) * scale    # [H, n]
+        m = x.max(axis=1, keepdims=True)
+        e = np.exp(x - m)
+        l = e.sum(axis=1, keepdims=True)
+        o_lat[s] = (e / l) @ Cs
+        lse[s] = (m + np.log(l))[:, 0]
+    return o_lat, lse
+
+
+def decode_absorbed_seq(q_lat, q_rope, c_kv, k_rope, scale, causal=False):
+    """One sequence, absorbed form over all readable rows: (o_lat [S,H,d_c], lse [S,H])."""
+    q_lat = np.asarray(q_lat, np.float64)
+    S = q_lat.shape[0]
+    T = np.asarray(c_kv).shape[0]
+    n_vis = [visible_length(T, S, s, causal) for s in range(S)]
+    return decode_absorbed_partial_seq(q_lat, q_rope, c_kv, k_rope, scale, 0, T, n_vis)
+
+
+def combine_partials(o_parts, lse_parts):
+    """Merge attention over disjoint row ranges by their log-sum-exp.
+
+    Not on the pages (split-KV serves long contexts at small batch).  It follows
+    from the softmax definition: if part k has lse_k and normalised output o_k,
+    the whole has lse = log sum_k exp(lse_k) and o = sum_k exp(lse_k - lse) o_k.
+    o_parts [K,...,d]; lse_parts [K,...].  All parts empty -> o = 0, lse = -inf.
+    """
+    o_parts = np.asarray(o_parts, np.float64)
+    lse_parts = np.asarray(lse_parts, np.float64)
+    m = lse_parts.max(axis=0)
+    finite = np.isfinite(m)
+    m_safe = np.where(finite, m, 0.0)
+    w = np.where(np.isfinite(lse_parts), np.exp(lse_parts - m_safe), 0.0)
+    tot = w.sum(axis=0)
+    lse = np.where(finite, m_safe + np.log(np.where(finite, tot, 1.0)), -np.inf)
+    coef = np.where(finite, 1.0 / np.where(finite, tot, 1.0), 0.0)
+    o = np.einsum("k...,k...d->...d", w * coef, o_parts)
+    return o, lse
+
+
+# ----------------------------------------------------------------------------
+# Value up-projection (step a6)
+# ----------------------------------------------------------------------------
+
+def out_proj_uv(o_lat: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
+    """o[..., h, :] = o_lat[..., h, :] . W_UV[h].
+
+    [CALC] "Value 투영을 가중합 뒤로 옮기기": a (C U^V) = (a C) U^V = z U^V, so U^V is
+    applied once, per head, after the latents are mixed.
+    o_lat [..., H, d_c]; w_uv [H, d_c, d_v] -> [..., H, d_v].
+    """
+    return np.einsum("...hc,hcv->...hv", np.asarray(o_lat, np.float64),
+                     np.asarray(w_uv, np.float64))
+
+
+# ----------------------------------------------------------------------------
+# Paged cache addressing
+# ----------------------------------------------------------------------------
+
+def gather_paged_rows(pool: np.ndarray, block_row: np.ndarray, T: int) -> np.ndarray:
+    """Rows 0..T-1 of one sequence stored in pages of a shared pool.
+
+    [MLA] "MLA + 투기적 디코딩", "vLLM 구현 과제": paged serving of MLA needs a page
+    table whose entries hold latent vectors instead of K/V pairs.  Row t lives in page block_row[t // P] at
+    offset t % P, with P = pool.shape[1].
+    """
+    pool = np.asarray(pool)
+    P = pool.shape[1]
+    t = np.arange(T)
+    return pool[np.asarray(block_row)[t // P], t % P]
+
+
+# ----------------------------------------------------------------------------
+# Cache-size identities
+# ----------------------------------------------------------------------------
+
+def cache_values_per_token(kind: str, n_h=128, d_k=128, d_c=512, d_r=64, n_kv_heads=8) -> int:
+    """Cached values per token per layer.
+
+    [MLA] "공식 정의": MHA caches 2 n_h d_k values per token.
+    [ANATOMY] section 1 table: GQA caches K and V for its KV heads only; MLA caches
+    the 512-wide c^KV plus the 64-wide shared k^R (576 values).
+    """
+    if kind == "mha":
+        return 2 * n_h * d_k
+    if kind == "gqa":
+        return 2 * n_kv_heads * d_k
+    if kind == "mla":
+        return d_c + d_r
+    raise ValueError(kind)
+
+
+def cache_bytes_per_token(kind: str, bytes_per_value: int = 2, **dims) -> int:
+    """FP16/bf16 bytes cached per token per layer ([ANATOMY] section 1 table)."""
+    return cache_values_per_token(kind, **dims) * bytes_per_value
+
+
+def compression_ratio(n_h=128, d_k=128, d_c=512) -> float:
+    """2 n_h d_k / d_c ([MLA] "공식 정의", compression ratio)."""
+    return 2 * n_h * d_k / d_c
+
+
+def full_cache_gib(kind: str, tokens: int = 131072, layers: int = 61, **dims) -> float:
+    """Whole-model cache size in GiB ([ANATOMY] section 1 table, 128k context, 61 layers)."""
+    return cache_bytes_per_token(kind, **dims) * tokens * layers / 2.0 ** 30
