@@ -1,0 +1,369 @@
+"""Benchmark of the MLA decode hot path (absorb -> latent attention -> W_UV up-projection).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dsv3_decode|tiny|ragged_paged|long_splitkv|mtp_causal]
+
+Prints ONE JSON line (rank 0).  A step is one pass of the whole path over one batch
+of the workload; the workload is DeepSeek-V3-shaped decode (B=64, H=128, T=4096,
+d_c=512, d_r=64) unless --workload says otherwise.  With N>1 (torchrun) every rank
+runs the same batch on its own GPU (independent sequences: weak scaling, no
+collective on the data path); `value` is the whole-job tokens/s over the slowest rank.
+
+--impl reference times the fp64 CPU oracle on this host's cores on a bounded sample
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_latent_kv_70_b300 import inputs as I  # noqa: E402
+
+METRIC = "MLA decode tokens/s (one attention layer: absorb + latent attention + W_UV)"
+UNIT = "tokens/s"
+ROW_BYTES = 1152
+DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_simt.cu",
+                  "mla_latent_kv_70_b300/csrc/decode_sm103.cu",
+                  "mla_latent_kv_70_b300/csrc/common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3_decode", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic(case):
+    """Bytes and FLOPs of one latent-attention launch, by definition (no overheads)."""
+    pairs = 0
+    for T in case.seqlens:
+        for s in range(case.S):
+            pairs += T if not case.causal else max(0, min(T, T - case.S + s + 1))
+    cache_bytes = ROW_BYTES * case.total_tokens
+    io_bytes = case.B * case.S * case.H * (576 * 2 + 512 * 4 + 4)
+    flops = 2.0 * case.H * (576 + 512) * pairs
+    return cache_bytes, cache_bytes + io_bytes, flops
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get(
+            "bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def source_sha():
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """NVML samples of SM clock and clock-event reasons while `active` is set."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, index):
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self.active = False
+        self._stop = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # noqa: BLE001  (no NVML: report no clocks)
+            self.nv = None
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+
+    def _run(self):
+        while not self._stop and self.nv is not None:
+            if self.active:
+                try:
+                    mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                    r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                    self.samples.append(mhz)
+                    for bit, name in self.REASONS.items():
+                        if r & bit and name != "gpu_idle":
+                            self.reasons.add(name)
+                except Exception:  # noqa: BLE001
+                    pass
+            time.sleep(0.002)
+
+    def stop(self):
+        self._stop = True
+        self.t.join(timeout=1)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+def cpu_baseline(case, min_seconds=5.0, max_seqs=None):
+    """Time the fp64 oracle (as it stands) over whole sequences of the workload."""
+    import numpy as np  # noqa: F401
+    import oracle as O
+    from threadpoolctl import threadpool_info
+    w_uk, w_uv = (w.double().numpy() for w in I.weights(case))
+    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    tokens = 0
+    seqs = 0
+    t0 = time.perf_counter()
+    b = 0
+    max_seqs = max_seqs or 4 * case.B
+    while seqs == 0 or (time.perf_counter() - t0 < min_seconds and seqs < max_seqs):
+        T = case.seqlens[b]
+        rows = I.seq_rows(case, b)[:T].double().numpy()
+        qn, qr = I.seq_queries(case, b)
+        qn, qr = qn.double().numpy(), qr.double().numpy()
+        if case.rope:
+            import numpy as np
+            rows[:, 512:] = O.rope_interleaved(rows[:, 512:], np.arange(T), case.theta)
+            pos = np.array([T - case.S + s for s in range(case.S)], dtype=np.float64)
+            qr = O.rope_interleaved(qr, pos[:, None], case.theta)
+        q_lat = O.absorb_q(qn, w_uk)
+        o_lat, _ = O.decode_absorbed_seq(q_lat, qr, rows[:, :512], rows[:, 512:], case.scale,
+                                         case.causal)
+        O.out_proj_uv(o_lat, w_uv)
+        tokens += case.S
+        seqs += 1
+        b = (b + 1) % case.B
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{seqs} whole sequences of {case.name} (T={case.seqlens[0] if len(set(case.seqlens)) == 1 else 'ragged'}, "
+                      f"H={case.H}) through absorb + fp64 absorbed attention + W_UV, {dt:.1f} s"}
+
+
+def run_reference(args, case):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(case, min_seconds=0.0, max_seqs=1)  # one sequence per step
+        if i >= args.warmup:
+            times.append(case.S / r["value"])
+    step_s = sum(times) / len(times)
+    value = case.S / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "B": case.B, "S": case.S, "H": case.H,
+                       "T": case.seqlens[0], "step": "one sequence of the batch per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                             "cores": r["cores"],
+                             "sample": "one whole sequence per step (absorb + fp64 absorbed attention + W_UV)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    case = I.WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, case)
+        return
+
+    import mla_latent_kv_70_b300 as mla
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    # Inputs resident in HBM before timing.
+    kv = I.cache(case, device=dev)
+    qn, qr = I.queries(case)
+    w_uk, w_uv = (w.to(dev) for w in I.weights(case))
+    q_nope, q_rope = qn.to(dev), qr.to(dev)
+    seqlens = torch.tensor(case.seqlens, dtype=torch.int32, device=dev)
+    block_table = case.block_table.to(dev) if case.paged else None
+    q_pos = case.q_positions().to(dev) if case.rope else None
+    if case.rope:
+        pos = torch.arange(case.t_cap, dtype=torch.int32, device=dev).repeat(case.B)
+        mla.mla_rope_inplace(kv, 576, case.B * case.t_cap, 512, pos, case.theta)
+    step = mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
+                          num_splits=case.num_splits, causal=case.causal, rope_theta=case.theta)
+    stream = torch.cuda.current_stream()
+
+    def run_step(ev=None):
+        mla.mla_absorb_q(q_nope, q_rope, w_uk, q_pos, case.theta, step.q_cat, stream)
+        if ev:
+            ev[0].record(stream)
+        mla.mla_decode_latent(step.q_cat, kv, seqlens, step.o_lat, step.lse, scale=case.scale,
+                              max_seqlen=step.max_seqlen, block_table=block_table,
+                              causal=case.causal, num_splits=step.num_splits,
+                              workspace=step.workspace, status=step.status, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        mla.mla_out_proj_uv(step.o_lat, w_uv, step.o, stream)
+
+    clocks = ClockSampler(dev.index)
+    for _ in range(args.warmup):
+        run_step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # Timed region: K steps, CUDA events on the launching stream.
+    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.active = True
+    start.record(stream)
+    for i in range(args.steps):
+        run_step(dec_events[i])
+    end.record(stream)
+    barrier()
+    clocks.active = False
+    total_ms = start.elapsed_time(end)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_events]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    status = int(step.status.item())
+    clock_info = clocks.stop()
+
+    # End to end through the public API: queries copied in from pinned host memory,
+    # the output read back, every step.
+    qn_h = qn.pin_memory()
+    qr_h = qr.pin_memory()
+    o_h = torch.empty(step.o.shape, dtype=torch.float32).pin_memory()
+    h2d = qn_h.numel() * 2 + qr_h.numel() * 2
+    d2h = o_h.numel() * 4
+
+    def e2e_step():
+        q_nope.copy_(qn_h, non_blocking=True)
+        q_rope.copy_(qr_h, non_blocking=True)
+        step(q_nope, q_rope, kv, seqlens, block_table=block_table, q_pos=q_pos, stream=stream)
+        o_h.copy_(step.o, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = case.B * case.S
+    value = world * tokens_per_step / (ms_per_step / 1e3)
+    e2e_value = world * tokens_per_step / (e2e_ms / args.steps / 1e3)
+
+    cache_b, alg_b, flops = algorithmic(case)
+    hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    achieved_gbs = alg_b / dec_avg_s / 1e9
+    achieved_tf = flops / dec_avg_s / 1e12
+    t_hbm = alg_b / (hbm * 1e9)
+    t_tc = flops / (tf_burst * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = recorded_traffic(case.name)
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": achieved_gbs / hbm}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": achieved_tf / tf_burst}
+    roof.update({"traffic": traffic, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)",
+                 "kernel": "mla_decode_latent", "decode_us": dec_avg_s * 1e6,
+                 "algorithmic_bytes": alg_b, "cache_bytes": cache_b, "flops": flops,
+                 "tflops": achieved_tf, "tensor_frac": achieved_tf / tf_burst,
+                 "roofline_us": max(t_hbm, t_tc) * 1e6,
+                 "frac_of_min_roofline": max(t_hbm, t_tc) / dec_avg_s})
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": case.name, "B": case.B, "S": case.S, "H": case.H,
+                       "T": case.seqlens[0] if len(set(case.seqlens)) == 1 else "ragged",
+                       "total_cached_rows": case.total_tokens, "d_c": 512, "d_r": 64,
+                       "num_splits": step.num_splits, "paged": case.paged,
+                       "causal": case.causal, "rope": case.rope,
+                       "l2": f"inputs larger than L2: {cache_b / 1e6:.0f} MB cache read per step"
+                             if cache_b > 126e6 else "inputs fit in L2 (no flush)",
+                       "parallelism": f"dp{world} (independent replicas, no collective)"},
+            "clocks": {k: clock_info[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * step.kernels_per_step,
+            "device_status": status,
+            "roofline": roof}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

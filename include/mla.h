@@ -1,0 +1,186 @@
+/*
+ * mla.h -- C ABI of libmla.so: Multi-Head Latent Attention decode with weight absorption
+ * on one B300 (sm_103a).
+ *
+ * The calls follow the steps of the decode computation described on the page
+ * "MLA의 계산: KV를 펼치지 않고 Attention하기" (ai-systems-engineering.com), cited below as
+ * [CALC], with dimensions from "Multi-Head Latent Attention (MLA)" (molayo1419.me), [MLA],
+ * and the cache row of "DeepSeek Multi-Head Latent Attention(MLA) 아키텍처 해부"
+ * (blog.huny.dev), [ANATOMY]:
+ *
+ *   mla_absorb_q       key absorption: q~ = q_nope W_UK^T per head, q_rope appended
+ *   mla_decode_latent  scores against the latent cache, softmax, latent aggregation
+ *                      (optionally split along the cache and merged by log-sum-exp)
+ *   mla_out_proj_uv    value up-projection of the aggregated latent, once per head
+ *   mla_rope_inplace   RoPE on the 64-wide rope slice of cache rows or queries
+ *
+ * Conventions shared by every call
+ *   - Dimensions are fixed: d_c = 512 (latent), d_r = 64 (decoupled RoPE key),
+ *     d_nope = d_v = 128.  A cache row is 576 bf16 = [c^KV (512) | k^R (64)], 1152 bytes.
+ *   - H (heads) must be a multiple of 16 and at most 128; S (query tokens per
+ *     sequence) is 1..4; B >= 1.
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned.
+ *     The caller owns every buffer; the library allocates no device memory and
+ *     keeps no state between calls apart from per-device constants (SM count,
+ *     driver entry points) it looks up once.
+ *   - bf16 values are passed as raw 16-bit patterns (mla_bf16).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  The return value reports host-side argument checks and launch
+ *     errors only.  Errors found on the device (a block-table entry outside the
+ *     pool, a pipeline wait that timed out) are OR-ed as bit flags
+ *     (1 << MLA_ERR_BLOCK_TABLE, 1 << MLA_ERR_TIMEOUT) into *status_dev when the
+ *     caller passes one; the affected rows are skipped, never read out of bounds.
+ *   - Argument checks run before any CUDA call, so a rejected call never touches
+ *     the GPU.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_D_C 512
+#define MLA_D_R 64
+#define MLA_D_NOPE 128
+#define MLA_D_V 128
+#define MLA_ROW 576
+#define MLA_MAX_SPLITS 128
+
+typedef uint16_t mla_bf16;   /* raw bfloat16 bits */
+typedef void* mla_stream;    /* cudaStream_t */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID = 1,      /* null pointer, bad size, misaligned pointer */
+  MLA_ERR_UNSUPPORTED = 2,  /* a shape outside the supported set (H, S, page size) */
+  MLA_ERR_CUDA = 3,         /* a CUDA runtime/driver error at launch */
+  MLA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than mla_decode_workspace_bytes */
+  MLA_ERR_BLOCK_TABLE = 5,  /* device flag: a block-table entry outside [0, num_pages) */
+  MLA_ERR_TIMEOUT = 6       /* device flag: a bounded pipeline wait expired */
+} mla_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* mla_status_string(int status);
+
+/* Number of SMs of the current device (0 when no device is usable). */
+int mla_device_sm_count(void);
+
+/*
+ * mla_absorb_q -- key absorption, [CALC] "Key 투영을 Query 쪽으로 옮기기" (Fig. 3):
+ * q (c_j U^K)^T = (q U^K^T) c_j^T, so each head's content query is mapped once into
+ * the latent space instead of expanding every cached latent.
+ *
+ *   q_cat[b,s,h, 0:512]   = bf16( sum_k q_nope[b,s,h,k] * W_UK[h, :, k] )   (fp32 accumulate)
+ *   q_cat[b,s,h, 512:576] = bf16( RoPE(q_rope[b,s,h,:], q_pos[b,s]) )  if q_pos != NULL
+ *                         = q_rope[b,s,h,:]                            otherwise
+ *
+ *   q_nope  bf16 [B,S,H,128]     q_rope bf16 [B,S,H,64]
+ *   w_uk    bf16 [H,512,128]     (W_UK[h] is d_c x d_nope; K_h = C W_UK[h], [MLA] "공식 정의")
+ *   q_pos   int32 [B,S] or NULL  (position of each query token)
+ *   rope_theta                   RoPE base (10000 for DeepSeek-V3); ignored without q_pos
+ *   q_cat   bf16 [B,S,H,576]     output, the query row matched to a 576-wide cache row
+ *
+ * RoPE pairs interleaved elements (2i, 2i+1) and turns them by pos * theta^(-2i/64)
+ * ([MLA] "구현", _apply_rope).
+ */
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* w_uk,
+                        const int32_t* q_pos, float rope_theta, int B, int S, int H,
+                        mla_bf16* q_cat, mla_stream stream);
+
+/*
+ * Workspace needed by mla_decode_latent for `num_splits` splits (0 = the automatic
+ * choice for this shape, see mla_decode_num_splits).  0 when one split is used.
+ * Layout: fp32 partial o_lat [splits,B,S,H,512] then fp32 partial lse [splits,B,S,H].
+ */
+size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen);
+
+/*
+ * The split count mla_decode_latent uses when passed num_splits = 0: enough
+ * (sequence, split) work units to fill the device's SMs, never more splits than
+ * 64-row tiles in the longest sequence, at most MLA_MAX_SPLITS.  max_seqlen is the
+ * caller's bound on seqlens[] (a host value).
+ */
+int mla_decode_num_splits(int B, int S, int H, int max_seqlen);
+
+/*
+ * mla_decode_latent -- attention of the absorbed queries straight over the latent
+ * cache, [CALC] "Content 점수와 위치 점수 합치기" (eq. s_j, Fig. 2) and
+ * "Value 투영을 가중합 뒤로 옮기기" (Fig. 4):
+ *
+ *   x_j   = scale * ( q_cat[b,s,h,:] . row_j[:] )          (= q~.c_j + q^R.k^R_j, scaled)
+ *   a_j   = softmax_j(x_j) over the rows query s may read  (all j < seqlens[b]; with
+ *           causal != 0 query s is the row at position T-S+s and reads j <= T-S+s)
+ *   o_lat[b,s,h,:] = sum_j a_j row_j[0:512]                (the k^R tail is not aggregated)
+ *   lse[b,s,h]     = ln sum_j exp(x_j)
+ *
+ * A sequence with no readable row gives o_lat = 0 and lse = -inf.
+ *
+ *   q_cat        bf16 [B,S,H,576] from mla_absorb_q
+ *   kv           bf16 cache rows of 576:
+ *                  block_table == NULL: contiguous, row t of sequence b at
+ *                                       kv + (b*kv_seq_stride + t)*576
+ *                  block_table != NULL: a pool [num_pages, page_size, 576]; row t of
+ *                                       sequence b is row t % page_size of page
+ *                                       block_table[b*max_pages + t/page_size]
+ *                Rows at or past seqlens[b] are never used, whatever they hold.
+ *   kv_seq_stride rows between sequences (contiguous layout only), >= max seqlen
+ *   seqlens      int32 [B] device, cached rows per sequence (>= 0)
+ *   block_table  int32 [B, max_pages] device or NULL; page_size must be 64
+ *   scale        softmax scale, 1/sqrt(d_nope + d_r) = 1/sqrt(192) for DeepSeek-V3
+ *                ([CALC] "RoPE 경로를 분리한 이유": not 1/sqrt(d_c + d_r))
+ *   num_splits   0 = automatic; 1..MLA_MAX_SPLITS splits the cache axis of every
+ *                sequence into equal ranges merged by log-sum-exp
+ *   max_seqlen   host-side bound on seqlens[] (used to plan splits; rows past it
+ *                are never read)
+ *   o_lat        fp32 [B,S,H,512] output;   lse fp32 [B,S,H] output
+ *   workspace    device scratch of mla_decode_workspace_bytes(...) bytes (may be
+ *                NULL when that is 0)
+ *   status_dev   int32 device word for device-side error flags, or NULL
+ */
+mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t kv_seq_stride,
+                             const int32_t* seqlens, const int32_t* block_table, int max_pages,
+                             int page_size, int num_pages, int B, int S, int H, int causal,
+                             float scale, int num_splits, int max_seqlen, float* o_lat,
+                             float* lse, void* workspace, size_t workspace_bytes,
+                             int32_t* status_dev, mla_stream stream);
+
+/*
+ * mla_combine_partials -- merge attention computed over disjoint row ranges:
+ *   lse = ln sum_k exp(lse_part[k]),  o = sum_k exp(lse_part[k] - lse) * o_part[k]
+ * (the log-sum-exp merge that split-KV and a cross-GPU gather of partials both use;
+ * not on the pages).
+ *   o_part fp32 [num_splits, rows, 512], lse_part fp32 [num_splits, rows];
+ *   o_lat fp32 [rows, 512], lse fp32 [rows].  Parts with lse = -inf count as empty.
+ */
+mla_status mla_combine_partials(const float* o_part, const float* lse_part, int num_splits,
+                                int64_t rows, float* o_lat, float* lse, mla_stream stream);
+
+/*
+ * mla_out_proj_uv -- value up-projection, [CALC] "Value 투영을 가중합 뒤로 옮기기":
+ * a (C U^V) = (a C) U^V, applied once per head after the latents are mixed.
+ *   o[b,s,h,:] = sum_i o_lat[b,s,h,i] * W_UV[h,i,:]       (fp32 accumulate)
+ *   o_lat fp32 [B,S,H,512]; w_uv bf16 [H,512,128]; o fp32 [B,S,H,128]
+ */
+mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int S, int H,
+                           float* o, mla_stream stream);
+
+/*
+ * mla_rope_inplace -- rotate the 64 values x[r, col_offset : col_offset+64] of each of
+ * `rows` rows (row r starts at x + r*row_stride elements) by position pos[r]:
+ * interleaved pairs (2i, 2i+1) turn by pos * theta^(-2i/64) ([MLA] "구현").  Used to
+ * put k^R of cache rows at their positions when they are written
+ * ([ANATOMY] section 2: the cached k^R carries RoPE).  The angle is reduced in
+ * double precision; the rotation runs in fp32 and is stored as bf16.
+ */
+mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
+                            const int32_t* pos, float theta, mla_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

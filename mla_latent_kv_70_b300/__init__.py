@@ -1,0 +1,150 @@
+"""MLA decode with weight absorption on B300: Python binding of libmla.so.
+
+The functions below carry the names of the C ABI in include/mla.h and only marshal
+arguments (torch CUDA tensors -> device pointers, shapes -> ints, the current CUDA
+stream).  Every step of the computation runs in the library's CUDA kernels; there is
+no CPU or PyTorch fallback: a missing or unloadable libmla.so raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import inputs  # noqa: F401  (seeded synthetic inputs; no attention math)
+
+D_C, D_R, D_NOPE, D_V, ROW = 512, 64, 128, 128, 576
+MAX_SPLITS = 128
+
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
+          4: "MLA_ERR_WORKSPACE", 5: "MLA_ERR_BLOCK_TABLE", 6: "MLA_ERR_TIMEOUT"}
+FLAG_BLOCK_TABLE = 1 << 5
+FLAG_TIMEOUT = 1 << 6
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla.so")
+
+# (name, restype, argtypes) of every exported symbol.
+_P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "mla_status_string": (ctypes.c_char_p, [_I]),
+    "mla_device_sm_count": (_I, []),
+    "mla_absorb_q": (_I, [_P, _P, _P, _P, _F, _I, _I, _I, _P, _P]),
+    "mla_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "mla_decode_num_splits": (_I, [_I, _I, _I, _I]),
+    "mla_decode_latent": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                               _P, _P, _P, _SZ, _P, _P]),
+    "mla_combine_partials": (_I, [_P, _P, _I, _I64, _P, _P, _P]),
+    "mla_out_proj_uv": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "mla_rope_inplace": (_I, [_P, _I64, _I64, _I, _P, _F, _P]),
+}
+
+_LIB = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmla.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mla_latent_kv_70_b300.build` (nvcc, sm_103a)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = handle
+    return _LIB
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("libmla takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmla takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(name, code):
+    if code != 0:
+        raise MLAError(name, code)
+
+
+def mla_status_string(code: int) -> str:
+    return lib().mla_status_string(code).decode()
+
+
+def mla_device_sm_count() -> int:
+    return lib().mla_device_sm_count()
+
+
+def mla_absorb_q(q_nope, q_rope, w_uk, q_pos, rope_theta, q_cat, stream=None):
+    """q_cat[b,s,h] = [q_nope[b,s,h] . W_UK[h]^T | RoPE(q_rope[b,s,h], q_pos[b,s])]."""
+    B, S, H, _ = q_nope.shape
+    _check("mla_absorb_q", lib().mla_absorb_q(
+        _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(q_pos), float(rope_theta), B, S, H,
+        _ptr(q_cat), _stream(stream)))
+
+
+def mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen) -> int:
+    return int(lib().mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen))
+
+
+def mla_decode_num_splits(B, S, H, max_seqlen) -> int:
+    return int(lib().mla_decode_num_splits(B, S, H, max_seqlen))
+
+
+def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, block_table=None,
+                      kv_seq_stride=0, page_size=64, causal=False, num_splits=0,
+                      workspace=None, status=None, stream=None):
+    """Absorbed attention over the latent cache; writes o_lat [B,S,H,512] and lse [B,S,H]."""
+    B, S, H, _ = q_cat.shape
+    if block_table is not None:
+        num_pages, max_pages = kv.shape[0], block_table.shape[1]
+    else:
+        num_pages, max_pages = 0, 0
+        kv_seq_stride = kv_seq_stride or kv.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_decode_latent", lib().mla_decode_latent(
+        _ptr(q_cat), _ptr(kv), int(kv_seq_stride), _ptr(seqlens), _ptr(block_table), max_pages,
+        page_size, num_pages, B, S, H, int(bool(causal)), float(scale), int(num_splits),
+        int(max_seqlen), _ptr(o_lat), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
+        _stream(stream)))
+
+
+def mla_combine_partials(o_part, lse_part, o_lat, lse, stream=None):
+    splits = o_part.shape[0]
+    rows = lse_part.numel() // splits
+    _check("mla_combine_partials", lib().mla_combine_partials(
+        _ptr(o_part), _ptr(lse_part), splits, rows, _ptr(o_lat), _ptr(lse), _stream(stream)))
+
+
+def mla_out_proj_uv(o_lat, w_uv, o, stream=None):
+    B, S, H, _ = o_lat.shape
+    _check("mla_out_proj_uv", lib().mla_out_proj_uv(_ptr(o_lat), _ptr(w_uv), B, S, H, _ptr(o),
+                                                    _stream(stream)))
+
+
+def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):
+    _check("mla_rope_inplace", lib().mla_rope_inplace(_ptr(x), int(row_stride), int(rows),
+                                                      int(col_offset), _ptr(pos), float(theta),
+                                                      _stream(stream)))
+
+
+from .pipeline import DecodeStep  # noqa: E402,F401

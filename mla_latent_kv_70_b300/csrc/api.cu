@@ -1,0 +1,180 @@
+// The C ABI of include/mla.h: argument checks, split planning, launches.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+
+using mla::kDc;
+using mla::kPage;
+using mla::kRow;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool heads_ok(int H) { return H >= 16 && H <= 128 && H % 16 == 0; }
+
+int sm_count_cached() {
+  static int count = -1;
+  if (count < 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    count = n;
+  }
+  return count;
+}
+
+int auto_splits(int B, int S, int H, int max_seqlen, int sms) {
+  (void)H;
+  if (sms <= 0) sms = 148;
+  const int units = B * S;                  // (sequence, query token) work units
+  const int target = sms / 2;               // one unit per SM pair
+  int splits = (target + units - 1) / units;
+  const int tiles = (max_seqlen + 63) / 64;
+  if (splits > tiles) splits = tiles;
+  if (splits > MLA_MAX_SPLITS) splits = MLA_MAX_SPLITS;
+  if (splits < 1) splits = 1;
+  return splits;
+}
+
+mla_status launch_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  cudaGetLastError();
+  return MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID: return "MLA_ERR_INVALID";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_BLOCK_TABLE: return "MLA_ERR_BLOCK_TABLE";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+int mla_device_sm_count(void) { return sm_count_cached(); }
+
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* w_uk,
+                        const int32_t* q_pos, float rope_theta, int B, int S, int H,
+                        mla_bf16* q_cat, mla_stream stream) {
+  if (!q_nope || !q_rope || !w_uk || !q_cat) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_cat))
+    return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4) return MLA_ERR_UNSUPPORTED;
+  if (q_pos && !(rope_theta > 0.f)) return MLA_ERR_INVALID;
+  const mla::RopeFreqs f = mla::make_rope_freqs(q_pos ? rope_theta : 10000.f);
+  return launch_status(mla::launch_absorb_q(
+      reinterpret_cast<const __nv_bfloat16*>(q_nope), reinterpret_cast<const __nv_bfloat16*>(q_rope),
+      reinterpret_cast<const __nv_bfloat16*>(w_uk), q_pos, f, B * S, H,
+      reinterpret_cast<__nv_bfloat16*>(q_cat), static_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_num_splits(int B, int S, int H, int max_seqlen) {
+  if (B < 1 || S < 1 || max_seqlen < 0) return 1;
+  return auto_splits(B, S, H, max_seqlen, sm_count_cached());
+}
+
+size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen) {
+  if (B < 1 || S < 1 || H < 1 || num_splits < 0 || num_splits > MLA_MAX_SPLITS) return 0;
+  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen);
+  if (splits <= 1) return 0;
+  const size_t rows = (size_t)B * S * H;
+  return (size_t)splits * rows * (kDc + 1) * sizeof(float);
+}
+
+mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t kv_seq_stride,
+                             const int32_t* seqlens, const int32_t* block_table, int max_pages,
+                             int page_size, int num_pages, int B, int S, int H, int causal,
+                             float scale, int num_splits, int max_seqlen, float* o_lat,
+                             float* lse, void* workspace, size_t workspace_bytes,
+                             int32_t* status_dev, mla_stream stream) {
+  if (!q_cat || !kv || !seqlens || !o_lat || !lse) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1 || max_seqlen < 0) return MLA_ERR_INVALID;
+  if (!aligned16(q_cat) || !aligned16(kv) || !aligned16(o_lat)) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4) return MLA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
+  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID;
+  if (block_table) {
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID;
+    if ((int64_t)max_pages * kPage < max_seqlen) return MLA_ERR_INVALID;
+  } else {
+    if (kv_seq_stride < max_seqlen || kv_seq_stride < 0) return MLA_ERR_INVALID;
+  }
+  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen);
+  const size_t need = mla_decode_workspace_bytes(B, S, H, splits, max_seqlen);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return MLA_ERR_WORKSPACE;
+
+  const int64_t rows = (int64_t)B * S * H;
+  mla::DecodeParams p{};
+  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
+  p.kv = reinterpret_cast<const __nv_bfloat16*>(kv);
+  p.kv_seq_stride = kv_seq_stride;
+  p.seqlens = seqlens;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.max_seqlen = max_seqlen;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * mla::kLog2e;
+  p.num_splits = splits;
+  p.status = status_dev;
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = part_o ? part_o + (size_t)splits * rows * kDc : nullptr;
+  p.o_out = splits > 1 ? part_o : o_lat;
+  p.lse_out = splits > 1 ? part_lse : lse;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mla_status r = launch_status(mla::launch_decode(p, st));
+  if (r != MLA_OK || splits <= 1) return r;
+  return launch_status(mla::launch_combine(part_o, part_lse, splits, rows, o_lat, lse, st));
+}
+
+mla_status mla_combine_partials(const float* o_part, const float* lse_part, int num_splits,
+                                int64_t rows, float* o_lat, float* lse, mla_stream stream) {
+  if (!o_part || !lse_part || !o_lat || !lse) return MLA_ERR_INVALID;
+  if (num_splits < 1 || num_splits > MLA_MAX_SPLITS || rows < 0) return MLA_ERR_INVALID;
+  if (!aligned16(o_part) || !aligned16(o_lat)) return MLA_ERR_INVALID;
+  return launch_status(mla::launch_combine(o_part, lse_part, num_splits, rows, o_lat, lse,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int S, int H,
+                           float* o, mla_stream stream) {
+  if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1) return MLA_ERR_INVALID;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4) return MLA_ERR_UNSUPPORTED;
+  return launch_status(mla::launch_out_proj_uv(o_lat, reinterpret_cast<const __nv_bfloat16*>(w_uv),
+                                               B * S, H, o, static_cast<cudaStream_t>(stream)));
+}
+
+mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
+                            const int32_t* pos, float theta, mla_stream stream) {
+  if (!x || !pos || rows < 0 || col_offset < 0 || row_stride < col_offset + mla::kDr)
+    return MLA_ERR_INVALID;
+  if ((col_offset & 1) || (row_stride & 1) || !(theta > 0.f)) return MLA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(x) & 3u) return MLA_ERR_INVALID;
+  const mla::RopeFreqs f = mla::make_rope_freqs(theta);
+  return launch_status(mla::launch_rope_inplace(reinterpret_cast<__nv_bfloat16*>(x), row_stride,
+                                                rows, col_offset, pos, f,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

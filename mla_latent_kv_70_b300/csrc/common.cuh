@@ -1,0 +1,102 @@
+// Shared definitions of libmla's kernels (internal; the public ABI is include/mla.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+namespace mla {
+
+constexpr int kDc = MLA_D_C;      // latent width d_c
+constexpr int kDr = MLA_D_R;      // decoupled RoPE width d_r
+constexpr int kDn = MLA_D_NOPE;   // per-head content query/key width
+constexpr int kDv = MLA_D_V;      // per-head value width
+constexpr int kRow = MLA_ROW;     // cached row: c^KV | k^R
+constexpr int kPage = 64;         // rows per page of a paged cache
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device-side error flags OR-ed into the caller's status word.
+constexpr int32_t kFlagBlockTable = 1 << MLA_ERR_BLOCK_TABLE;
+constexpr int32_t kFlagTimeout = 1 << MLA_ERR_TIMEOUT;
+
+__device__ __forceinline__ void raise_flag(int32_t* status, int32_t flag) {
+  if (status) atomicOr(status, flag);
+}
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
+  return __bfloat1622float2(v);
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Inverse RoPE frequencies theta^(-2i/64), i = 0..31, computed on the host in double.
+struct RopeFreqs {
+  double inv_freq[kDr / 2];
+};
+RopeFreqs make_rope_freqs(float theta);
+
+// Rotate one interleaved pair by pos * inv_freq: the angle is formed and reduced to
+// [-pi, pi] in double, the rotation itself runs in fp32.
+__device__ __forceinline__ float2 rope_pair(float x0, float x1, int pos, double inv_freq) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double a = (double)pos * inv_freq;
+  a -= two_pi * rint(a / two_pi);
+  float s, c;
+  sincosf((float)a, &s, &c);
+  return make_float2(x0 * c - x1 * s, x0 * s + x1 * c);
+}
+
+// ---------------------------------------------------------------------------
+// Decode: per-launch parameters shared by the host planner and the kernel.
+// ---------------------------------------------------------------------------
+struct DecodeParams {
+  const __nv_bfloat16* q_cat;  // [B,S,H,576]
+  const __nv_bfloat16* kv;     // contiguous rows or page pool
+  int64_t kv_seq_stride;       // rows between sequences (contiguous layout)
+  const int32_t* seqlens;      // [B]
+  const int32_t* block_table;  // [B,max_pages] or null
+  int max_pages;
+  int num_pages;
+  int max_seqlen;              // rows past this bound are never read (seqlens are clamped)
+  int B, S, H;
+  int causal;
+  float scale_log2;            // softmax scale * log2(e)
+  int num_splits;
+  float* o_out;                // o_lat [B,S,H,512] (1 split) or partials [splits,B,S,H,512]
+  float* lse_out;              // lse [B,S,H] or partials [splits,B,S,H]
+  int32_t* status;
+};
+
+// Rows [t0, t1) of sequence b that split `split` covers for query token s.
+__device__ __forceinline__ void split_range(const DecodeParams& p, int T, int s, int split,
+                                            int& t0, int& t1) {
+  int n_vis = T;
+  if (p.causal) n_vis = min(T, max(0, T - p.S + s + 1));
+  int chunk = (T + p.num_splits - 1) / p.num_splits;
+  chunk = (chunk + 63) & ~63;
+  t0 = split * chunk;
+  t1 = min(t0 + chunk, n_vis);
+}
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_rope,
+                            const __nv_bfloat16* w_uk, const int32_t* q_pos, const RopeFreqs& f,
+                            int M, int H, __nv_bfloat16* q_cat, cudaStream_t st);
+cudaError_t launch_out_proj_uv(const float* o_lat, const __nv_bfloat16* w_uv, int M, int H,
+                               float* o, cudaStream_t st);
+cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t rows,
+                                int col_offset, const int32_t* pos, const RopeFreqs& f,
+                                cudaStream_t st);
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
+                           float* o, float* lse, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+
+}  // namespace mla

@@ -1,0 +1,90 @@
+// RoPE of the 64-wide rope slice of rows, and the log-sum-exp merge of split partials.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace mla {
+
+RopeFreqs make_rope_freqs(float theta) {
+  // Page "Multi-Head Latent Attention (MLA)", section "구현" (_apply_rope): inverse
+  // frequencies theta^(-(0, 2, 4, ..)/d_r) for the interleaved pairs.
+  RopeFreqs f;
+  for (int i = 0; i < kDr / 2; ++i) f.inv_freq[i] = std::pow((double)theta, -2.0 * i / kDr);
+  return f;
+}
+
+namespace {
+
+__global__ void k_rope_inplace(__nv_bfloat16* __restrict__ x, int64_t row_stride, int64_t rows,
+                               int col_offset, const int32_t* __restrict__ pos, RopeFreqs f) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * (kDr / 2)) return;
+  const int64_t r = idx / (kDr / 2);
+  const int i = (int)(idx % (kDr / 2));
+  uint32_t* p = reinterpret_cast<uint32_t*>(x + r * row_stride + col_offset) + i;
+  const float2 v = bf2_to_f2(*p);
+  const float2 y = rope_pair(v.x, v.y, pos[r], f.inv_freq[i]);
+  *p = f2_to_bf2(y.x, y.y);
+}
+
+// One CTA of 128 threads per output row: weights exp(lse_k - max) are formed once in
+// shared memory, then each thread merges one float4 of the 512-wide latent row.
+__global__ void __launch_bounds__(128)
+k_combine(const float* __restrict__ o_part, const float* __restrict__ lse_part, int splits,
+          int64_t rows, float* __restrict__ o, float* __restrict__ lse) {
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  __shared__ float w_s[MLA_MAX_SPLITS];
+  __shared__ float red[4];
+  const float l = tid < splits ? lse_part[(int64_t)tid * rows + row] : -INFINITY;
+  float m = l;
+  for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((tid & 31) == 0) red[tid >> 5] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  const float w = (l == -INFINITY) ? 0.f : expf(l - m);
+  float sum = w;
+  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if ((tid & 31) == 0) red[tid >> 5] = sum;
+  __syncthreads();
+  sum = red[0] + red[1] + red[2] + red[3];
+  const bool empty = (m == -INFINITY);
+  const float inv = empty ? 0.f : 1.f / sum;
+  if (tid < splits) w_s[tid] = w * inv;
+  __syncthreads();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < splits; ++k) {
+    const float wk = w_s[k];
+    if (wk == 0.f) continue;
+    const float4 v = reinterpret_cast<const float4*>(o_part + ((int64_t)k * rows + row) * kDc)[tid];
+    acc.x = fmaf(wk, v.x, acc.x);
+    acc.y = fmaf(wk, v.y, acc.y);
+    acc.z = fmaf(wk, v.z, acc.z);
+    acc.w = fmaf(wk, v.w, acc.w);
+  }
+  reinterpret_cast<float4*>(o + row * kDc)[tid] = acc;
+  if (tid == 0) lse[row] = empty ? -INFINITY : m + logf(sum);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t rows,
+                                int col_offset, const int32_t* pos, const RopeFreqs& f,
+                                cudaStream_t st) {
+  const int64_t n = rows * (kDr / 2);
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  k_rope_inplace<<<(unsigned)((n + threads - 1) / threads), threads, 0, st>>>(
+      x, row_stride, rows, col_offset, pos, f);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
+                           float* o, float* lse, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  k_combine<<<(unsigned)rows, 128, 0, st>>>(o_part, lse_part, splits, rows, o, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

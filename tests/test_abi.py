@@ -1,0 +1,88 @@
+"""The C ABI library loads, exports every symbol include/mla.h declares, and rejects bad
+arguments on the host before touching the GPU (these tests need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_latent_kv_70_b300 as mla
+from mla_latent_kv_70_b300 import build as mla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mla_absorb_q", "mla_decode_latent", "mla_out_proj_uv",
+                     "mla_decode_workspace_bytes", "mla_combine_partials", "mla_rope_inplace"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in mla.SIGNATURES, f"{name} has no binding"
+
+
+def test_status_strings(lib):
+    for code, name in mla.STATUS.items():
+        assert mla.mla_status_string(code) == name
+    assert mla.mla_status_string(99) == "MLA_ERR_UNKNOWN"
+
+
+P = 4096  # a fake, 16-byte aligned "device" address: never dereferenced by a rejected call
+
+
+def decode_args(**over):
+    a = dict(q_cat=P, kv=P, kv_seq_stride=256, seqlens=P, block_table=None, max_pages=0,
+             page_size=64, num_pages=0, B=4, S=1, H=16, causal=0, scale=0.07, num_splits=1,
+             max_seqlen=256, o_lat=P, lse=P, workspace=None, workspace_bytes=0, status=None,
+             stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q_cat=None), 1), (dict(kv=None), 1), (dict(seqlens=None), 1), (dict(o_lat=None), 1),
+    (dict(B=0), 1), (dict(H=12), 2), (dict(H=256), 2), (dict(S=5), 2), (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1), (dict(num_splits=129), 1), (dict(num_splits=-1), 1),
+    (dict(kv_seq_stride=100), 1), (dict(q_cat=P + 2), 1),
+    (dict(block_table=P, max_pages=4, page_size=32, num_pages=8), 2),
+    (dict(block_table=P, max_pages=2, num_pages=8), 1),
+    (dict(num_splits=4, max_seqlen=256), 4),
+])
+def test_decode_rejects_bad_arguments(lib, over, code):
+    assert lib.mla_decode_latent(*decode_args(**over)) == code
+
+
+def test_workspace_bytes(lib):
+    assert lib.mla_decode_workspace_bytes(4, 1, 16, 1, 256) == 0
+    assert lib.mla_decode_workspace_bytes(4, 1, 16, 3, 256) == 3 * 4 * 16 * 513 * 4
+    assert lib.mla_decode_workspace_bytes(4, 1, 16, 129, 256) == 0
+
+
+def test_other_calls_reject_bad_arguments(lib):
+    assert lib.mla_absorb_q(None, P, P, None, 1e4, 4, 1, 16, P, None) == 1
+    assert lib.mla_absorb_q(P, P, P, None, 1e4, 4, 1, 20, P, None) == 2
+    assert lib.mla_absorb_q(P, P, P, P, 0.0, 4, 1, 16, P, None) == 1
+    assert lib.mla_out_proj_uv(P, P, 4, 1, 0, P, None) == 1
+    assert lib.mla_out_proj_uv(P, None, 4, 1, 16, P, None) == 1
+    assert lib.mla_combine_partials(P, P, 0, 10, P, P, None) == 1
+    assert lib.mla_combine_partials(P, P, 200, 10, P, P, None) == 1
+    assert lib.mla_rope_inplace(P, 576, 10, 512, None, 1e4, None) == 1
+    assert lib.mla_rope_inplace(P, 576, 10, 520, P, 1e4, None) == 1
+    assert lib.mla_rope_inplace(P, 576, 10, 511, P, 1e4, None) == 1

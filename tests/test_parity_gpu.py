@@ -1,0 +1,207 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases are compared in full; the five named workloads run at their full sizes in
+the launch configuration the bench uses, and are compared on seeded samples of
+sequences (every head and every output of each sampled sequence).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mla_latent_kv_70_b300 import inputs as I
+from tests.mla_cases import (LSE_ABS_TOL, ROW_REL_TOL, DeviceCase, lse_err, oracle_seq,
+                             row_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_70_b300 import build
+    build.build()
+
+
+def check_case(dc: DeviceCase, st, seqs, expanded_heads=None):
+    case = dc.case
+    w_uk, w_uv = (w.double().numpy() for w in I.weights(case))
+    o_lat = st.o_lat.cpu().numpy()
+    lse = st.lse.cpu().numpy()
+    o = st.o.cpu().numpy()
+    assert int(st.status.item()) == 0
+    for b in seqs:
+        r_lat, r_lse, r_o = oracle_seq(case, b, w_uk, w_uv)
+        assert row_rel_err(o_lat[b], r_lat) <= ROW_REL_TOL, (case.name, b)
+        assert lse_err(lse[b], r_lse) <= LSE_ABS_TOL, (case.name, b)
+        assert row_rel_err(o[b], r_o) <= ROW_REL_TOL, (case.name, b)
+    if expanded_heads is not None:
+        b = seqs[0]
+        _, e_lse, e_o = oracle_seq(case, b, w_uk, w_uv, heads=expanded_heads, expanded=True)
+        assert row_rel_err(o[b][:, expanded_heads], e_o) <= ROW_REL_TOL
+        assert lse_err(lse[b][:, expanded_heads], e_lse) <= LSE_ABS_TOL
+
+
+# ----------------------------------------------------------------------------
+# Small cases, compared in full
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("splits", [1, 2, 0])
+def test_tiny_workload(splits):
+    case = I.tiny()
+    dc = DeviceCase(case)
+    st = dc.step(num_splits=splits)
+    check_case(dc, st, range(case.B), expanded_heads=list(range(case.H)))
+
+
+@pytest.mark.parametrize("H", [16, 128])
+@pytest.mark.parametrize("splits", [1, 3, 64])
+def test_ragged_contiguous_edges(H, splits):
+    lens = [1, 5, 63, 64, 65, 200, 0, 129]
+    case = I.make_case("edges", len(lens), 1, H, lens, t_cap=256, seed=3)
+    dc = DeviceCase(case)
+    for b, T in enumerate(lens):
+        dc.kv[b, T:] = float("nan")       # rows past the sequence must never be used
+    st = dc.step(num_splits=splits, max_seqlen=256)
+    check_case(dc, st, range(case.B))
+    assert np.all(st.o_lat[6].cpu().numpy() == 0)
+    assert np.all(np.isneginf(st.lse[6].cpu().numpy()))
+
+
+@pytest.mark.parametrize("splits", [1, 4])
+def test_paged_small(splits):
+    lens = [70, 1, 300, 64]
+    case = I.make_case("paged_small", 4, 1, 128, lens, paged=True, seed=5)
+    dc = DeviceCase(case)
+    for b, T in enumerate(lens):
+        last = int(case.block_table[b, case.pages_per_seq[b] - 1])
+        off = T - (case.pages_per_seq[b] - 1) * 64
+        dc.kv[last, off:] = float("nan")
+    st = dc.step(num_splits=splits)
+    check_case(dc, st, range(case.B))
+
+
+def test_paged_equals_contiguous_bitwise():
+    lens = [300, 77]
+    paged = I.make_case("p", 2, 1, 128, lens, paged=True, seed=9)
+    cont = I.make_case("c", 2, 1, 128, lens, seed=9, t_cap=320)
+    dp, dcn = DeviceCase(paged), DeviceCase(cont)
+    for b, T in enumerate(lens):
+        rows = I.seq_rows(paged, b)[:T].cuda()
+        dcn.kv[b, :T] = rows
+    sp = dp.step(num_splits=2)
+    sc = dcn.step(num_splits=2)
+    assert torch.equal(sp.o_lat, sc.o_lat) and torch.equal(sp.lse, sc.lse)
+
+
+@pytest.mark.parametrize("lens", [[100, 7, 2, 1], [129, 64]])
+def test_causal_two_tokens_with_rope(lens):
+    case = I.make_case("mtp_small", len(lens), 2, 128, lens, causal=True, rope=True, seed=11)
+    dc = DeviceCase(case)
+    st = dc.step(num_splits=1)
+    check_case(dc, st, range(case.B), expanded_heads=[0, 77])
+    st2 = dc.step(num_splits=3)
+    check_case(dc, st2, range(case.B))
+
+
+def test_block_table_out_of_range_is_flagged():
+    lens = [130]
+    case = I.make_case("badpage", 1, 1, 16, lens, paged=True, seed=13)
+    dc = DeviceCase(case)
+    dc.block_table[0, 1] = 10_000          # a page id outside the pool
+    st = dc.step(num_splits=1)
+    import mla_latent_kv_70_b300 as mla
+    assert int(st.status.item()) & mla.FLAG_BLOCK_TABLE
+    assert np.all(np.isfinite(st.o_lat.cpu().numpy()))
+
+
+# ----------------------------------------------------------------------------
+# The stand-alone calls
+# ----------------------------------------------------------------------------
+
+def test_rope_inplace_matches_oracle():
+    import mla_latent_kv_70_b300 as mla
+    rows = 1000
+    x = I.randn_bf16((rows, 576), 0, "ropetest")
+    pos = torch.randint(0, 131072, (rows,), generator=torch.Generator().manual_seed(1),
+                        dtype=torch.int32)
+    xd = x.cuda()
+    mla.mla_rope_inplace(xd, 576, rows, 512, pos.cuda(), 10000.0)
+    got = xd.cpu().double().numpy()
+    ref = O.rope_interleaved(x[:, 512:].double().numpy(), pos.double().numpy(), 10000.0)
+    np.testing.assert_array_equal(got[:, :512], x[:, :512].double().numpy())
+    # fp32 rotation stored as bf16: within two bf16 ulps of the exact value
+    np.testing.assert_allclose(got[:, 512:], ref, rtol=2 ** -7, atol=2 ** -7)
+
+
+def test_combine_matches_oracle():
+    import mla_latent_kv_70_b300 as mla
+    g = torch.Generator().manual_seed(2)
+    K, rows = 7, 300
+    o_part = torch.randn(K, rows, 512, generator=g)
+    lse_part = torch.randn(K, rows, generator=g) * 3
+    lse_part[2, :50] = -math.inf
+    lse_part[:, 299] = -math.inf
+    o = torch.empty(rows, 512, device="cuda")
+    lse = torch.empty(rows, device="cuda")
+    mla.mla_combine_partials(o_part.cuda(), lse_part.cuda(), o, lse)
+    r_o, r_lse = O.combine_partials(o_part.double().numpy(), lse_part.double().numpy())
+    np.testing.assert_allclose(o.cpu().numpy(), r_o, rtol=1e-5, atol=1e-5)
+    assert lse_err(lse.cpu().numpy(), r_lse) < 1e-5
+
+
+def test_absorb_and_out_proj_match_oracle():
+    import mla_latent_kv_70_b300 as mla
+    case = I.make_case("proj", 3, 2, 128, [10, 10, 10], seed=17)
+    qn, qr = I.queries(case)
+    w_uk, w_uv = I.weights(case)
+    q_cat = torch.empty(3, 2, 128, 576, dtype=torch.bfloat16, device="cuda")
+    mla.mla_absorb_q(qn.cuda(), qr.cuda(), w_uk.cuda(), None, 1e4, q_cat)
+    ref = O.absorb_q(qn.double().numpy(), w_uk.double().numpy())
+    got = q_cat.cpu().double().numpy()
+    assert row_rel_err(got[..., :512], ref) < 1e-2
+    np.testing.assert_array_equal(got[..., 512:], qr.double().numpy())
+    o_lat = torch.randn(3, 2, 128, 512, generator=torch.Generator().manual_seed(3))
+    o = torch.empty(3, 2, 128, 128, device="cuda")
+    mla.mla_out_proj_uv(o_lat.cuda(), w_uv.cuda(), o)
+    r = O.out_proj_uv(o_lat.double().numpy(), w_uv.double().numpy())
+    assert row_rel_err(o.cpu().numpy(), r) < 1e-5
+
+
+# ----------------------------------------------------------------------------
+# The named workloads at full size (sampled sequences)
+# ----------------------------------------------------------------------------
+
+def test_dsv3_decode_full_size():
+    case = I.dsv3()
+    dc = DeviceCase(case)
+    st = dc.step()
+    check_case(dc, st, [0, 31, 63], expanded_heads=[0, 64, 127])
+
+
+def test_ragged_paged_full_size():
+    case = I.ragged_paged()
+    dc = DeviceCase(case)
+    st = dc.step()
+    lens = case.seqlens
+    seqs = [int(np.argmin(lens)), int(np.argmax(lens)), 7]
+    check_case(dc, st, seqs, expanded_heads=[5])
+
+
+def test_long_context_splitkv_full_size():
+    case = I.long_splitkv(num_splits=64)
+    dc = DeviceCase(case)
+    st = dc.step()
+    check_case(dc, st, [0, 1], expanded_heads=[1])
+    st_auto = dc.step(num_splits=0)
+    check_case(dc, st_auto, [0, 1])
+
+
+def test_mtp_causal_full_size():
+    case = I.mtp()
+    dc = DeviceCase(case)
+    st = dc.step()
+    check_case(dc, st, [0, 64, 127], expanded_heads=[3])
