@@ -150,13 +150,27 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
+def blas_threads():
+    """Threads the oracle's BLAS uses (numpy's OpenBLAS/MKL), else the usable cores."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
 def cpu_baseline(case, min_seconds=5.0, max_seqs=None):
     """Time the fp64 oracle (as it stands) over whole sequences of the workload."""
     import numpy as np  # noqa: F401
     import oracle as O
-    from threadpoolctl import threadpool_info
     w_uk, w_uv = (w.double().numpy() for w in I.weights(case))
-    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    cores = blas_threads()
     tokens = 0
     seqs = 0
     t0 = time.perf_counter()

@@ -71,6 +71,30 @@ def oracle_seq(case: I.DecodeCase, b: int, w_uk=None, w_uv=None, heads=None, exp
     return o_lat, lse, O.out_proj_uv(o_lat, w_uv)
 
 
+def lse_rounding_bound(case: I.DecodeCase, b: int, w_uk=None) -> np.ndarray:
+    """Bound on |lse_gpu - lse_exact| from storing q~ in bf16, per (s, h).
+
+    The CUDA path rounds q~ = q_nope W_UK^T to bf16 (relative error <= 2^-9 per element)
+    before scoring.  Each scaled score then moves by at most
+    scale * 2^-9 * sum_i |q~_i c_ji|, and log-sum-exp moves by at most the largest score
+    change.  The bound below doubles that to cover the fp32 accumulations.  At small T
+    this exceeds 1e-3; for the named workloads (T >= 256) the tests use 1e-3.
+    """
+    T = case.seqlens[b]
+    if T == 0:
+        return np.zeros((case.S, case.H))
+    rows = I.seq_rows(case, b)[:T].double().numpy()
+    qn, qr = I.seq_queries(case, b)
+    if w_uk is None:
+        w_uk = I.weights(case)[0].double().numpy()
+    q_lat = np.abs(O.absorb_q(qn.double().numpy(), w_uk))       # [S,H,512]
+    terms = q_lat @ np.abs(rows[:, :I.D_C]).T                    # [S,H,T]
+    if case.rope:
+        # q^R and k^R are both rotated and stored as bf16 on the GPU: 2 roundings.
+        terms = terms + 2.0 * np.abs(qr.double().numpy()) @ np.abs(rows[:, I.D_C:]).T
+    return case.scale * 2.0 ** -8 * terms.max(axis=-1)
+
+
 def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     """max over rows of max|g - r| / max|r| along the last axis (rows with ref == 0 use abs)."""
     num = np.abs(gpu - ref).max(axis=-1)
@@ -81,5 +105,6 @@ def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
 
 def lse_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     both_inf = np.isneginf(gpu) & np.isneginf(ref)
-    d = np.where(both_inf, 0.0, np.abs(gpu - ref))
+    with np.errstate(invalid="ignore"):
+        d = np.where(both_inf, 0.0, np.abs(gpu - ref))
     return float(d.max()) if d.size else 0.0
