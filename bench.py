@@ -42,7 +42,7 @@ DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_simt.cu",
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3_decode", choices=sorted(I.WORKLOADS))
@@ -105,26 +105,43 @@ def recorded_traffic(workload):
 
 
 class ClockSampler:
-    """NVML samples of SM clock and clock-event reasons while `active` is set."""
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-               0x100: "display_clock_setting"}
+    """SM clock and clock-event reasons sampled while `active` is set.
 
-    def __init__(self, index):
+    NVML (handle found by the device's UUID, so CUDA_VISIBLE_DEVICES remapping is
+    harmless); if NVML is unusable, `nvidia-smi -lms` on the device's PCI bus id."""
+    REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, dev):
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
         self.active = False
+        self.error = None
         self._stop = False
+        self.nv = None
+        self.proc = None
+        props = torch.cuda.get_device_properties(dev)
         try:
             import pynvml
             pynvml.nvmlInit()
+            uuid = str(props.uuid)
+            h = None
+            for cand in (uuid, "GPU-" + uuid):
+                try:
+                    h = pynvml.nvmlDeviceGetHandleByUUID(cand)
+                    break
+                except Exception:  # noqa: BLE001
+                    continue
+            if h is None:
+                h = pynvml.nvmlDeviceGetHandleByIndex(dev.index)
+            self.h = h
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # noqa: BLE001  (no NVML: report no clocks)
-            self.nv = None
+        except Exception as e:  # noqa: BLE001
+            self.error = f"nvml: {e!r}"
+        self.bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
         self.t = threading.Thread(target=self._run, daemon=True)
         self.t.start()
 
@@ -132,22 +149,52 @@ class ClockSampler:
         while not self._stop and self.nv is not None:
             if self.active:
                 try:
-                    mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                    self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
                     r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                    self.samples.append(mhz)
                     for bit, name in self.REASONS.items():
-                        if r & bit and name != "gpu_idle":
+                        if r & bit:
                             self.reasons.add(name)
-                except Exception:  # noqa: BLE001
-                    pass
-            time.sleep(0.002)
+                except Exception as e:  # noqa: BLE001
+                    self.error = f"nvml sample: {e!r}"
+            time.sleep(0.001)
+
+    def start_smi(self):
+        """Fallback sampler: nvidia-smi on this device, 20 ms period."""
+        if self.nv is not None:
+            return
+        import shutil
+        import subprocess
+        if not shutil.which("nvidia-smi"):
+            return
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.bus}", f"--query-gpu={q}",
+                                      "--format=csv,noheader,nounits", "-lms", "20"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
 
     def stop(self):
         self._stop = True
         self.t.join(timeout=1)
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        if self.proc is not None:
+            self.proc.terminate()
+            out = self.proc.communicate(timeout=5)[0]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6 or not f[0].isdigit():
+                    continue
+                self.samples.append(int(f[0]))
+                self.max_mhz = int(f[1]) if f[1].isdigit() else self.max_mhz
+                for name, v in zip(names, f[2:]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
+        d = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+             "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+             "samples": len(self.samples)}
+        if self.error and not self.samples:
+            d["error"] = self.error
+        return d
 
 
 def blas_threads():
@@ -266,7 +313,7 @@ def main():
             ev[1].record(stream)
         mla.mla_out_proj_uv(step.o_lat, w_uv, step.o, stream)
 
-    clocks = ClockSampler(dev.index)
+    clocks = ClockSampler(dev)
     for _ in range(args.warmup):
         run_step()
     torch.cuda.synchronize()
@@ -280,6 +327,7 @@ def main():
     dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.start_smi()
     barrier()
     clocks.active = True
     start.record(stream)
@@ -365,7 +413,7 @@ def main():
                        "l2": f"inputs larger than L2: {cache_b / 1e6:.0f} MB cache read per step"
                              if cache_b > 126e6 else "inputs fit in L2 (no flush)",
                        "parallelism": f"dp{world} (independent replicas, no collective)"},
-            "clocks": {k: clock_info[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "clocks": clock_info,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * step.kernels_per_step,
