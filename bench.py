@@ -34,8 +34,8 @@ from mla_latent_kv_70_b300 import inputs as I  # noqa: E402
 METRIC = "MLA decode tokens/s (one attention layer: absorb + latent attention + W_UV)"
 UNIT = "tokens/s"
 ROW_BYTES = 1152
-DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_simt.cu",
-                  "mla_latent_kv_70_b300/csrc/decode_sm103.cu",
+DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_sm103.cu",
+                  "mla_latent_kv_70_b300/csrc/ptx_sm103.cuh",
                   "mla_latent_kv_70_b300/csrc/common.cuh"]
 
 

@@ -28,17 +28,28 @@ int sm_count_cached() {
   return count;
 }
 
+// Split count for the CTA-pair decode: each (query token, split) unit occupies two SMs.
+// Pick the count that minimises (cache bytes + partial round trip) / wave efficiency.
 int auto_splits(int B, int S, int H, int max_seqlen, int sms) {
-  (void)H;
   if (sms <= 0) sms = 148;
-  const int units = B * S;                  // (sequence, query token) work units
-  const int target = sms / 2;               // one unit per SM pair
-  int splits = (target + units - 1) / units;
+  const int slots = sms / 2;
+  const int units = B * S;
   const int tiles = (max_seqlen + 63) / 64;
-  if (splits > tiles) splits = tiles;
-  if (splits > MLA_MAX_SPLITS) splits = MLA_MAX_SPLITS;
-  if (splits < 1) splits = 1;
-  return splits;
+  const double cache = (double)units * (double)max_seqlen * 1152.0;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int s = 1; s <= MLA_MAX_SPLITS && s <= (tiles > 0 ? tiles : 1); ++s) {
+    const int n = units * s;
+    const int waves = (n + slots - 1) / slots;
+    const double eff = (double)n / ((double)slots * waves);
+    const double partial = s > 1 ? (double)n * H * (kDc + 1) * 4.0 * 2.0 : 0.0;
+    const double cost = (cache + partial) / eff;
+    if (s == 1 || cost < best_cost * 0.98) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 mla_status launch_status(cudaError_t e) {

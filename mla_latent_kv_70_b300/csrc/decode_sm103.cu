@@ -1,0 +1,475 @@
+// Absorbed MLA decode on the sm_103a tensor cores (tcgen05 + TMEM + TMA), one CTA pair
+// per (query token, split).
+//
+// What it computes -- page "MLA의 계산: KV를 펼치지 않고 Attention하기":
+//   section "Content 점수와 위치 점수 합치기" (eq. s_j): s_j = q~ . c_j + q^R . k^R_j, one
+//     scale, one softmax over every readable position, causal mask between query tokens;
+//   section "Key 투영을 Query 쪽으로 옮기기" (Fig. 3): q~ = q U^K^T is read straight
+//     against the latent rows, no per-head key is built;
+//   section "Value 투영을 가중합 뒤로 옮기기" (Fig. 4): z = sum_j a_j c_j is accumulated in
+//     the latent space; U^V is applied afterwards (mla_out_proj_uv).
+//
+// How (B300 design).  All 128 heads read the same latent row, so per tile of 64 cache
+// rows the work is two dense products: S[128 x 64] = Q[128 x 576] . K^T and
+// O[128 x 512] += P[128 x 64] . V[64 x 512].  O alone fills the 512 TMEM columns of one
+// SM, so a cluster of two CTAs shares a query token:
+//   * CTA r owns latent columns [256r, 256r+256) and rope columns [512+32r, 512+32r+32)
+//     of every cache row; its TMA loads only those (each cache byte is read once);
+//   * each CTA computes the partial score over its 288 columns into TMEM (A operand =
+//     its half of q~, held in TMEM; the rope half of q from shared memory);
+//   * the two fp32 partials are exchanged through distributed shared memory and
+//     summed (a+b == b+a, so both CTAs hold bit-identical scores, maxima and P);
+//   * each CTA accumulates its 256 columns of O in TMEM from P (bf16, written back to
+//     TMEM) and its own V columns (the same shared-memory tile read MN-major).
+// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-5 (one per
+// TMEM lane quarter) run the online softmax, the exchange and the epilogue.
+// Softmax runs in the log2 domain with a lazily raised reference maximum (the running
+// output is rescaled only when the maximum grows by more than 2^8).
+// Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
+// status word, drains its own copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kN = 64;                            // cache rows per tile
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
+constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
+constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
+constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
+constexpr uint32_t kRecvBytes = 128 * kN * 4;     // peer's fp32 partial scores
+
+constexpr uint32_t kOffQRope = kStages * kStageBytes;
+constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
+constexpr uint32_t kOffBars = kOffRecv + 2 * kRecvBytes;
+constexpr uint32_t kOffSlot = kOffBars + 256;
+constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
+
+// TMEM columns.
+constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
+constexpr uint32_t kTmemS = 256;    // [256,384) two score buffers of 64 fp32 (P aliases them)
+constexpr uint32_t kTmemQ = 384;    // [384,512) q~ half: 256 bf16 packed in pairs
+
+constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+
+enum Bar {
+  kKvFull = 0,              // [kStages]
+  kKvEmpty = kStages,       // [kStages]
+  kSFull = 2 * kStages,     // [2]
+  kPFull = 2 * kStages + 2, // [2]
+  kPvDone = 2 * kStages + 4,// [2]
+  kRecvFull = 2 * kStages + 6, // [2]
+  kQFull = 2 * kStages + 8,
+  kQReady = 2 * kStages + 9,
+  kDrain = 2 * kStages + 10,
+  kNumBars = 2 * kStages + 11
+};
+
+struct Maps {
+  CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle
+  CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle
+  CUtensorMap q_rope;    // q_cat rows, box 32 cols x 128 rows, 64B swizzle
+};
+
+__device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int t) {
+  return p.block_table[(int64_t)b * p.max_pages + t / kPage];
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s0 = smem_addr(smem);
+  const uint32_t bars = s0 + kOffBars;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+
+  // Work unit of this CTA pair.
+  const int unit = blockIdx.x >> 1;
+  const int m = unit / p.num_splits;          // query token b*S + s
+  const int split = unit % p.num_splits;
+  const int b = m / p.S, s = m % p.S;
+  const int T = min(max(0, p.seqlens[b]), p.max_seqlen);
+  int t0, t1;
+  split_range(p, T, s, split, t0, t1);
+  const int ntiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar(kKvFull + i), 1);
+      mbar_init(bar(kKvEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kSFull + i), 1);
+      mbar_init(bar(kPFull + i), 128);
+      mbar_init(bar(kPvDone + i), 1);
+      mbar_init(bar(kRecvFull + i), 128);
+    }
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQReady), 128);
+    mbar_init(bar(kDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // the peer's barriers exist before any remote arrive
+  const uint32_t tb = *tmem_slot;
+
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&maps.kv_lat);
+      prefetch_tmap(&maps.kv_rope);
+      prefetch_tmap(&maps.q_rope);
+      mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
+      tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+      int issued = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(bar(kKvEmpty + st), ph ^ 1u, kWaitNs)) {
+          aborted = true;
+          break;
+        }
+        const int t = t0 + i * kN;
+        int y;
+        if (p.block_table) {
+          const int page = tile_page(p, b, t);
+          if (page < 0 || page >= p.num_pages) {
+            raise_flag(p.status, kFlagBlockTable);
+            y = p.num_pages * kPage;   // past the pool: the copy fills zeros
+          } else {
+            y = page * kPage;
+          }
+        } else {
+          y = (int)((int64_t)b * p.kv_seq_stride + t);
+        }
+        const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
+        mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(stage + j * kBoxBytes, &maps.kv_lat, bar(kKvFull + st), 256 * (int)rank + 64 * j, y);
+        tma_load_2d(stage + 4 * kBoxBytes, &maps.kv_rope, bar(kKvFull + st), kDc + 32 * (int)rank, y);
+        ++issued;
+      }
+      // No copy may still be landing when the CTA exits.
+      for (int i = max(0, issued - kStages); i < issued; ++i)
+        mbar_wait(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u, kWaitNs);
+      if (!mbar_wait(bar(kQFull), 0, kWaitNs)) aborted = true;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t id_qk = idesc_bf16(128, kN, false, false);
+      const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
+      tc_fence_after();
+      for (int i = 0; i <= ntiles && !aborted; ++i) {
+        if (i < ntiles) {
+          const int st = i % kStages;
+          if (!mbar_wait(bar(kKvFull + st), (uint32_t)(i / kStages) & 1u, kWaitNs)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
+          const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
+          // latent half: A = q~ half from TMEM, B = cache rows (K-major, 128B swizzle)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint32_t box = stage + (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
+            mma_ts(d, tb + kTmemQ + 8u * k, smem_desc(box, 16, 1024, kSwizzle128B), id_qk, k > 0);
+          }
+          // rope half: A = q^R half (smem), B = k^R half (64B swizzle)
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_ss(d, smem_desc(s0 + kOffQRope + 32u * k, 16, 512, kSwizzle64B),
+                   smem_desc(stage + 4 * kBoxBytes + 32u * k, 16, 512, kSwizzle64B), id_qk, 1);
+          mma_commit(bar(kSFull + (i & 1)));
+        }
+        if (i >= 1) {
+          const int j = i - 1;
+          if (!mbar_wait(bar(kPFull + (j & 1)), (uint32_t)(j >> 1) & 1u, kWaitNs)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t stage = s0 + (uint32_t)(j % kStages) * kStageBytes;
+          const uint32_t pa = tb + kTmemS + 64u * (uint32_t)(j & 1);
+          // O half += P . V: B = the same tile read MN-major (N = 256 latent columns over
+          // four 64-column boxes, K = 16 rows per step)
+#pragma unroll
+          for (int k = 0; k < kN / 16; ++k)
+            mma_ts(tb + kTmemO, pa + 8u * k, smem_desc(stage + 2048u * k, 8192, 1024, kSwizzle128B),
+                   id_pv, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(bar(kKvEmpty + j % kStages));
+          mma_commit(bar(kPvDone + (j & 1)));
+        }
+      }
+      mma_commit(bar(kDrain));
+      mbar_wait(bar(kDrain), 0, kWaitNs);
+    }
+  } else {
+    // ---------------- softmax / exchange / epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;
+    const int h = 32 * quarter + lane;               // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const bool head_ok = h < p.H;
+    const int64_t qrow = (int64_t)m * p.H + h;
+    float m_ref = -INFINITY, l = 0.f;
+
+    if (ntiles > 0) {
+      // q~ half of this head into TMEM (A operand of the score MMA).
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 w = head_ok ? src[c * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * v] = w.x;
+          r[4 * v + 1] = w.y;
+          r[4 * v + 2] = w.z;
+          r[4 * v + 3] = w.w;
+        }
+        tmem_st32(tb + lane_off + kTmemQ + 32u * c, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kQReady));
+    }
+
+    const uint32_t recv_local = s0 + kOffRecv;
+    const uint32_t recv_peer = map_to_rank(recv_local, peer);
+    const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
+
+    for (int i = 0; i < ntiles && !aborted; ++i) {
+      const int buf = i & 1;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      if (__any_sync(0xffffffffu, !mbar_wait(bar(kSFull + buf), ph, kWaitNs))) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      float x[kN];
+      {
+        uint32_t r[32];
+        tmem_ld32(tb + lane_off + kTmemS + 64u * buf, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+        tmem_ld32(tb + lane_off + kTmemS + 64u * buf + 32u, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
+      }
+      // Exchange the partial scores with the peer CTA: [j/4][h][4] fp32 layout.
+      const uint32_t rb = recv_peer + (uint32_t)buf * kRecvBytes;
+#pragma unroll
+      for (int q = 0; q < kN / 4; ++q)
+        st_cluster_v4(rb + (uint32_t)(q * 128 + h) * 16u, x[4 * q], x[4 * q + 1], x[4 * q + 2],
+                      x[4 * q + 3]);
+      mbar_arrive_cluster(recv_bar_peer + 8u * (uint32_t)buf);
+      if (__any_sync(0xffffffffu, !mbar_wait<true>(bar(kRecvFull + buf), ph, kWaitNs))) {
+        aborted = true;
+        break;
+      }
+      const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes;
+#pragma unroll
+      for (int q = 0; q < kN / 4; ++q) {
+        const float4 v = ld_shared_v4(rl + (uint32_t)(q * 128 + h) * 16u);
+        x[4 * q] += v.x;
+        x[4 * q + 1] += v.y;
+        x[4 * q + 2] += v.z;
+        x[4 * q + 3] += v.w;
+      }
+
+      // Readable rows of this tile.
+      const int t = t0 + i * kN;
+      int valid = min(kN, t1 - t);
+      if (p.block_table) {
+        const int page = tile_page(p, b, t);
+        if (page < 0 || page >= p.num_pages) valid = 0;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kN; ++j) {
+        x[j] = (j < valid) ? x[j] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, x[j]);
+      }
+      // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
+      const bool grow = mx > m_ref + kRescaleThreshold;
+      const float m_new = grow ? mx : m_ref;
+      const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
+      if (__any_sync(0xffffffffu, grow && i > 0)) {
+        // Rescale this warp's rows of O once PV(i-1) has landed.
+        const int jprev = i - 1;
+        if (__any_sync(0xffffffffu,
+                       !mbar_wait(bar(kPvDone + (jprev & 1)), (uint32_t)(jprev >> 1) & 1u, kWaitNs)))
+          aborted = true;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(tb + lane_off + kTmemO + 32u * c, r);
+        }
+      }
+      l *= alpha;
+      m_ref = m_new;
+      uint32_t pk[32];
+      float ps = 0.f;
+#pragma unroll
+      for (int j = 0; j < kN; j += 2) {
+        const float a = (x[j] == -INFINITY) ? 0.f : exp2f(x[j] - m_ref);
+        const float c = (x[j + 1] == -INFINITY) ? 0.f : exp2f(x[j + 1] - m_ref);
+        ps += a + c;
+        pk[j >> 1] = f2_to_bf2(a, c);
+      }
+      l += ps;
+      tmem_st32(tb + lane_off + kTmemS + 64u * buf, pk);
+
+      // Rows past the readable range may hold anything (even NaN): clear them in the
+      // V columns of the staged tile so that 0-weighted rows add exactly 0.
+      if (valid < kN) {
+        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
+        const int nrow = kN - valid;
+        for (int idx = h; idx < nrow * 32; idx += 128) {      // 4 boxes x 8 chunks per row
+          const int row = valid + idx / 32, c = idx % 32;
+          st_shared_v4_zero(stage + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u +
+                            (uint32_t)(c & 7) * 16u);
+        }
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull + buf));
+    }
+
+    // Epilogue: O half / l -> global.
+    const int64_t rows_all = (int64_t)p.B * p.S * p.H;
+    const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
+    float* out = p.o_out + orow * kDc + 256 * rank;
+    const bool have = ntiles > 0 && l > 0.f;
+    if (ntiles > 0 && !aborted) {
+      const int last = ntiles - 1;
+      if (__any_sync(0xffffffffu,
+                     !mbar_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u, kWaitNs)))
+        aborted = true;
+    }
+    tc_fence_after();
+    const float inv = have ? 1.f / l : 0.f;
+    if (ntiles > 0 && !aborted) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
+        tmem_ld_wait();
+        if (head_ok) {
+          // A row that saw no readable position (l == 0) is written as exact zeros.
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(out + 32 * c)[v] =
+                have ? make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    } else if (head_ok) {
+      for (int v = 0; v < 64; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (head_ok && rank == 0)
+      p.lse_out[orow] = have ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+  }
+
+  if (aborted) raise_flag(p.status, kFlagTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
+  }
+  cluster_sync();  // neither CTA leaves while the other may still touch its shared memory
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_cols,
+                 uint32_t box_rows, CUtensorMapSwizzle sw) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
+  Maps maps;
+  const uint64_t kv_rows = p.block_table ? (uint64_t)p.num_pages * kPage
+                                         : (uint64_t)p.B * (uint64_t)p.kv_seq_stride;
+  const uint64_t q_rows = (uint64_t)p.B * p.S * p.H;
+  if (kv_rows == 0 || kv_rows > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  if (!encode_rows(&maps.kv_lat, p.kv, kv_rows, 64, kN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(k_decode_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int units = p.B * p.S * p.num_splits;
+  k_decode_sm103<<<2 * units, kThreads, kSmemBytes, st>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
