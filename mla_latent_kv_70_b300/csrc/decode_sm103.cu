@@ -17,12 +17,17 @@
 //     of every cache row; its TMA loads only those (each cache byte is read once);
 //   * each CTA computes the partial score over its 288 columns into TMEM (A operand =
 //     its half of q~, held in TMEM; the rope half of q from shared memory);
-//   * the two fp32 partials are exchanged through distributed shared memory and
-//     summed (a+b == b+a, so both CTAs hold bit-identical scores, maxima and P);
-//   * each CTA accumulates its 256 columns of O in TMEM from P (bf16, written back to
-//     TMEM) and its own V columns (the same shared-memory tile read MN-major).
+//   * the partials are swapped through distributed shared memory as bf16 (st.async,
+//     counted on the receiver's mbarrier).  The cross-SM path moves ~16 B/clk per SM,
+//     so fp32 partials would cost more than the HBM stream; bf16 halves that and adds an
+//     error of the same order as storing q~ in bf16 (2^-9 of the partial sum).  Each CTA
+//     adds its own fp32 partial to the peer's bf16 partial and normalises its half of O
+//     with its own softmax sums, so the two halves need not agree bit for bit;
+//   * the exchange runs one tile ahead of the softmax, P (bf16) goes to shared memory
+//     in the 128B-swizzled K-major layout, and each CTA accumulates its 256 columns of
+//     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
 // Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-5 (one per
-// TMEM lane quarter) run the online softmax, the exchange and the epilogue.
+// TMEM lane quarter) run the exchange, the online softmax and the epilogue.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
 // output is rescaled only when the maximum grows by more than 2^8).
 // Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
@@ -45,34 +50,40 @@ constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swi
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
-constexpr uint32_t kRecvBytes = 128 * kN * 4;     // peer's fp32 partial scores
+constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
+constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
 
 constexpr uint32_t kOffQRope = kStages * kStageBytes;
 constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
-constexpr uint32_t kOffBars = kOffRecv + 2 * kRecvBytes;
+constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
+constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
 constexpr uint32_t kOffSlot = kOffBars + 256;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
+static_assert(kOffP % 1024 == 0, "P tiles need 1024-byte alignment (128B swizzle atoms)");
 
 // TMEM columns.
 constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
-constexpr uint32_t kTmemS = 256;    // [256,384) two score buffers of 64 fp32 (P aliases them)
+constexpr uint32_t kTmemS = 256;    // [256,384) two score buffers of 64 fp32
 constexpr uint32_t kTmemQ = 384;    // [384,512) q~ half: 256 bf16 packed in pairs
 
 constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 enum Bar {
-  kKvFull = 0,              // [kStages]
-  kKvEmpty = kStages,       // [kStages]
-  kSFull = 2 * kStages,     // [2]
-  kPFull = 2 * kStages + 2, // [2]
-  kPvDone = 2 * kStages + 4,// [2]
-  kRecvFull = 2 * kStages + 6, // [2]
-  kQFull = 2 * kStages + 8,
-  kQReady = 2 * kStages + 9,
-  kDrain = 2 * kStages + 10,
-  kNumBars = 2 * kStages + 11
+  kKvFull = 0,                   // [kStages] TMA -> MMA
+  kKvEmpty = kStages,            // [kStages] MMA -> TMA
+  kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
+  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: score buffer read (4 warps)
+  kPFull = 2 * kStages + 4,      // [2] softmax -> MMA: P in shared memory (128 threads)
+  kPvDone = 2 * kStages + 6,     // [2] MMA -> softmax: PV finished (P buffer, O stable)
+  kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by thread 0)
+  kSendFree = 2 * kStages + 10,  // [2] peer has read our previous partial (4 remote warps)
+  kQFull = 2 * kStages + 12,
+  kQReady = 2 * kStages + 13,
+  kDrain = 2 * kStages + 14,
+  kNumBars = 2 * kStages + 15
 };
+static_assert(kNumBars * 8 <= 256, "barrier area");
 
 struct Maps {
   CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle
@@ -82,6 +93,14 @@ struct Maps {
 
 __device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int t) {
   return p.block_table[(int64_t)b * p.max_pages + t / kPage];
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, kWaitNs));
+}
+
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity) {
+  return !__any_sync(0xffffffffu, !mbar_wait<true>(bar, parity, kWaitNs));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -117,9 +136,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
+      mbar_init(bar(kSFree + i), 4);
       mbar_init(bar(kPFull + i), 128);
       mbar_init(bar(kPvDone + i), 1);
-      mbar_init(bar(kRecvFull + i), 128);
+      mbar_init(bar(kRecvFull + i), 1);
+      mbar_init(bar(kSendFree + i), 4);
     }
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQReady), 128);
@@ -184,61 +205,99 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     if (lane == 0 && ntiles > 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
       const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      auto issue_qk = [&](int i) -> bool {
+        const int st = i % kStages;
+        if (!mbar_wait(bar(kKvFull + st), (uint32_t)(i / kStages) & 1u, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
+        const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
+        // latent half: A = q~ half from TMEM, B = cache rows (K-major, 128B swizzle)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t box = stage + (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
+          mma_ts(d, tb + kTmemQ + 8u * k, smem_desc(box, 16, 1024, kSwizzle128B), id_qk, k > 0);
+        }
+        // rope half: A = q^R half (smem), B = k^R half (64B swizzle)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          mma_ss(d, smem_desc(s0 + kOffQRope + 32u * k, 16, 512, kSwizzle64B),
+                 smem_desc(stage + 4 * kBoxBytes + 32u * k, 16, 512, kSwizzle64B), id_qk, 1);
+        mma_commit(bar(kSFull + (i & 1)));
+        return true;
+      };
       if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
       tc_fence_after();
-      for (int i = 0; i <= ntiles && !aborted; ++i) {
-        if (i < ntiles) {
-          const int st = i % kStages;
-          if (!mbar_wait(bar(kKvFull + st), (uint32_t)(i / kStages) & 1u, kWaitNs)) {
+      for (int i = 0; i < 2 && i < ntiles && !aborted; ++i)
+        if (!issue_qk(i)) aborted = true;
+      for (int i = 0; i < ntiles && !aborted; ++i) {
+        const int buf = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+        if (i + 2 < ntiles) {
+          // S buffer `buf` is free once the softmax has read tile i from it.
+          if (!mbar_wait(bar(kSFree + buf), ph, kWaitNs) || !issue_qk(i + 2)) {
             aborted = true;
             break;
           }
-          tc_fence_after();
-          const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
-          const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
-          // latent half: A = q~ half from TMEM, B = cache rows (K-major, 128B swizzle)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint32_t box = stage + (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-            mma_ts(d, tb + kTmemQ + 8u * k, smem_desc(box, 16, 1024, kSwizzle128B), id_qk, k > 0);
-          }
-          // rope half: A = q^R half (smem), B = k^R half (64B swizzle)
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            mma_ss(d, smem_desc(s0 + kOffQRope + 32u * k, 16, 512, kSwizzle64B),
-                   smem_desc(stage + 4 * kBoxBytes + 32u * k, 16, 512, kSwizzle64B), id_qk, 1);
-          mma_commit(bar(kSFull + (i & 1)));
         }
-        if (i >= 1) {
-          const int j = i - 1;
-          if (!mbar_wait(bar(kPFull + (j & 1)), (uint32_t)(j >> 1) & 1u, kWaitNs)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t stage = s0 + (uint32_t)(j % kStages) * kStageBytes;
-          const uint32_t pa = tb + kTmemS + 64u * (uint32_t)(j & 1);
-          // O half += P . V: B = the same tile read MN-major (N = 256 latent columns over
-          // four 64-column boxes, K = 16 rows per step)
-#pragma unroll
-          for (int k = 0; k < kN / 16; ++k)
-            mma_ts(tb + kTmemO, pa + 8u * k, smem_desc(stage + 2048u * k, 8192, 1024, kSwizzle128B),
-                   id_pv, (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(bar(kKvEmpty + j % kStages));
-          mma_commit(bar(kPvDone + (j & 1)));
+        if (!mbar_wait(bar(kPFull + buf), ph, kWaitNs)) {
+          aborted = true;
+          break;
         }
+        tc_fence_after();
+        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
+        const uint32_t pbuf = s0 + kOffP + (uint32_t)buf * kPBytes;
+        // O half += P . V: A = P (smem, K-major), B = the staged tile read MN-major
+        // (N = 256 latent columns over four 64-column boxes, K = 16 rows per step).
+#pragma unroll
+        for (int k = 0; k < kN / 16; ++k)
+          mma_ss(tb + kTmemO, smem_desc(pbuf + 32u * k, 16, 1024, kSwizzle128B),
+                 smem_desc(stage + 2048u * k, 8192, 1024, kSwizzle128B), id_pv,
+                 (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar(kKvEmpty + i % kStages));
+        mma_commit(bar(kPvDone + buf));
       }
       mma_commit(bar(kDrain));
       mbar_wait(bar(kDrain), 0, kWaitNs);
     }
   } else {
-    // ---------------- softmax / exchange / epilogue (warps 2..5) ----------------
+    // ---------------- exchange / softmax / epilogue (warps 2..5) ----------------
     const int quarter = warp & 3;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
     const int64_t qrow = (int64_t)m * p.H + h;
     float m_ref = -INFINITY, l = 0.f;
+
+    const uint32_t recv_local = s0 + kOffRecv;
+    const uint32_t recv_peer = map_to_rank(recv_local, peer);
+    const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
+    const uint32_t free_bar_peer = map_to_rank(bar(kSendFree), peer);
+
+    // Partial scores of tile j: TMEM -> bf16 -> the peer's receive buffer.
+    // Layout there: [8 chunks][128 rows][16 B], chunk c holding columns 8c..8c+7.
+    auto send = [&](int j) -> bool {
+      const int buf = j & 1;
+      if (!warp_wait(bar(kSFull + buf), (uint32_t)(j >> 1) & 1u)) return false;
+      if (j >= 2 && !warp_wait_cluster(bar(kSendFree + buf), (uint32_t)((j - 2) >> 1) & 1u))
+        return false;
+      tc_fence_after();
+      uint32_t r[32], pk[32];
+      tmem_ld32(tb + lane_off + kTmemS + 64u * buf, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 16; ++c) pk[c] = f2_to_bf2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+      tmem_ld32(tb + lane_off + kTmemS + 64u * buf + 32u, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        pk[16 + c] = f2_to_bf2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
+      const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + (uint32_t)h * 16u;
+      const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(dst + (uint32_t)c * 2048u, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3], rb);
+      return true;
+    };
 
     if (ntiles > 0) {
       // q~ half of this head into TMEM (A operand of the score MMA).
@@ -259,20 +318,28 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
+      if (h == 0) {
+        mbar_arrive_expect_tx(bar(kRecvFull + 0), kRecvBytes);
+        if (ntiles > 1) mbar_arrive_expect_tx(bar(kRecvFull + 1), kRecvBytes);
+      }
+      if (!send(0)) aborted = true;
     }
-
-    const uint32_t recv_local = s0 + kOffRecv;
-    const uint32_t recv_peer = map_to_rank(recv_local, peer);
-    const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
 
     for (int i = 0; i < ntiles && !aborted; ++i) {
       const int buf = i & 1;
       const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      if (__any_sync(0xffffffffu, !mbar_wait(bar(kSFull + buf), ph, kWaitNs))) {
+      // Keep the exchange one tile ahead of the softmax.
+      if (i + 1 < ntiles && !send(i + 1)) {
         aborted = true;
         break;
       }
-      tc_fence_after();
+      if (!warp_wait(bar(kRecvFull + buf), ph)) {
+        aborted = true;
+        break;
+      }
+      // Re-arm this buffer's barrier for tile i+2 before telling the peer it may send it.
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
+      // Own fp32 partial (still in TMEM) + the peer's bf16 partial.
       float x[kN];
       {
         uint32_t r[32];
@@ -285,26 +352,22 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
       }
-      // Exchange the partial scores with the peer CTA: [j/4][h][4] fp32 layout.
-      const uint32_t rb = recv_peer + (uint32_t)buf * kRecvBytes;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSFree + buf));
+      const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + (uint32_t)h * 16u;
 #pragma unroll
-      for (int q = 0; q < kN / 4; ++q)
-        st_cluster_v4(rb + (uint32_t)(q * 128 + h) * 16u, x[4 * q], x[4 * q + 1], x[4 * q + 2],
-                      x[4 * q + 3]);
-      mbar_arrive_cluster(recv_bar_peer + 8u * (uint32_t)buf);
-      if (__any_sync(0xffffffffu, !mbar_wait<true>(bar(kRecvFull + buf), ph, kWaitNs))) {
-        aborted = true;
-        break;
-      }
-      const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes;
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = ld_shared_u4(rl + (uint32_t)c * 2048u);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int q = 0; q < kN / 4; ++q) {
-        const float4 v = ld_shared_v4(rl + (uint32_t)(q * 128 + h) * 16u);
-        x[4 * q] += v.x;
-        x[4 * q + 1] += v.y;
-        x[4 * q + 2] += v.z;
-        x[4 * q + 3] += v.w;
+        for (int u = 0; u < 4; ++u) {
+          x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
+          x[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(free_bar_peer + 8u * (uint32_t)buf);
 
       // Readable rows of this tile.
       const int t = t0 + i * kN;
@@ -313,22 +376,30 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         const int page = tile_page(p, b, t);
         if (page < 0 || page >= p.num_pages) valid = 0;
       }
-      float mx = -INFINITY;
+      if (valid < kN) {
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        x[j] = (j < valid) ? x[j] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, x[j]);
+        for (int j = 0; j < kN; ++j)
+          if (j >= valid) x[j] = -INFINITY;
+      }
+      float mx;
+      {
+        float t16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t16[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(x[j + 32], x[j + 48]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+        mx = t16[0] * p.scale_log2;
       }
       // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
-      const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
+      const float alpha = grow ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
       if (__any_sync(0xffffffffu, grow && i > 0)) {
         // Rescale this warp's rows of O once PV(i-1) has landed.
-        const int jprev = i - 1;
-        if (__any_sync(0xffffffffu,
-                       !mbar_wait(bar(kPvDone + (jprev & 1)), (uint32_t)(jprev >> 1) & 1u, kWaitNs)))
-          aborted = true;
+        const int jp = i - 1;
+        if (!warp_wait(bar(kPvDone + (jp & 1)), (uint32_t)(jp >> 1) & 1u)) aborted = true;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
@@ -339,20 +410,33 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
           tmem_st32(tb + lane_off + kTmemO + 32u * c, r);
         }
+        tmem_st_wait();
+        tc_fence_before();
       }
       l *= alpha;
       m_ref = m_new;
-      uint32_t pk[32];
+      // P buffer `buf` is free once PV(i-2) is done.
+      if (i >= 2 && !warp_wait(bar(kPvDone + buf), (uint32_t)((i - 2) >> 1) & 1u)) {
+        aborted = true;
+        break;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      const uint32_t prow = s0 + kOffP + (uint32_t)buf * kPBytes + (uint32_t)h * 128u;
       float ps = 0.f;
 #pragma unroll
-      for (int j = 0; j < kN; j += 2) {
-        const float a = (x[j] == -INFINITY) ? 0.f : exp2f(x[j] - m_ref);
-        const float c = (x[j + 1] == -INFINITY) ? 0.f : exp2f(x[j + 1] - m_ref);
-        ps += a + c;
-        pk[j >> 1] = f2_to_bf2(a, c);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = ex2_approx(fmaf(x[8 * c + 2 * u], p.scale_log2, neg));
+          const float d = ex2_approx(fmaf(x[8 * c + 2 * u + 1], p.scale_log2, neg));
+          ps += a + d;
+          w[u] = f2_to_bf2(a, d);
+        }
+        // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7).
+        st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
       }
       l += ps;
-      tmem_st32(tb + lane_off + kTmemS + 64u * buf, pk);
 
       // Rows past the readable range may hold anything (even NaN): clear them in the
       // V columns of the staged tile so that 0-weighted rows add exactly 0.
@@ -364,10 +448,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           st_shared_v4_zero(stage + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u +
                             (uint32_t)(c & 7) * 16u);
         }
-        fence_proxy_async_smem();
       }
-      tmem_st_wait();
-      tc_fence_before();
+      fence_proxy_async_smem();
       mbar_arrive(bar(kPFull + buf));
     }
 
@@ -378,9 +460,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     const bool have = ntiles > 0 && l > 0.f;
     if (ntiles > 0 && !aborted) {
       const int last = ntiles - 1;
-      if (__any_sync(0xffffffffu,
-                     !mbar_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u, kWaitNs)))
-        aborted = true;
+      if (!warp_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u)) aborted = true;
     }
     tc_fence_after();
     const float inv = have ? 1.f / l : 0.f;
