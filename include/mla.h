@@ -149,6 +149,34 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
                              int32_t* status_dev, mla_stream stream);
 
 /*
+ * mla_decode_latent_noalloc -- mla_decode_latent without a caller-provided workspace.
+ * The pages have no counterpart: this is a convenience for callers that cannot allocate
+ * device memory themselves, such as plugins that are handed only their input and output
+ * buffers by a host runtime with no allocator hook, or loops that must not call
+ * cudaMalloc (it can synchronise the device).  The split-KV partials go to a fixed
+ * array of MLA_NOALLOC_SCRATCH_BYTES compiled into libmla.so, which every device that
+ * loads the library keeps until the process exits; this call allocates nothing.
+ *
+ * Arguments and results are those of mla_decode_latent (same layouts, same ownership of
+ * the inputs and outputs), minus `workspace` / `workspace_bytes`.  If the partials of
+ * the chosen split count (mla_decode_workspace_bytes) exceed MLA_NOALLOC_SCRATCH_BYTES
+ * the call returns MLA_ERR_WORKSPACE and launches nothing; pick fewer splits.
+ *
+ * The first call on a device looks up the array's device address on that device
+ * (cudaGetSymbolAddress); make that first call before any stream capture.  All calls
+ * share the one array and each fully rewrites the part it reads, so no clearing is
+ * needed between calls, but calls that overlap on the GPU (other streams, other host
+ * threads) race on it: order them.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+mla_status mla_decode_latent_noalloc(const mla_bf16* q_cat, const mla_bf16* kv,
+                                     int64_t kv_seq_stride, const int32_t* seqlens,
+                                     const int32_t* block_table, int max_pages, int page_size,
+                                     int num_pages, int B, int S, int H, int causal, float scale,
+                                     int num_splits, int max_seqlen, float* o_lat, float* lse,
+                                     int32_t* status_dev, mla_stream stream);
+
+/*
  * mla_combine_partials -- merge attention computed over disjoint row ranges:
  *   lse = ln sum_k exp(lse_part[k]),  o = sum_k exp(lse_part[k] - lse) * o_part[k]
  * (the log-sum-exp merge that split-KV and a cross-GPU gather of partials both use;

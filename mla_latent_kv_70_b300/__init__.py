@@ -34,6 +34,8 @@ SIGNATURES = {
     "mla_decode_num_splits": (_I, [_I, _I, _I, _I]),
     "mla_decode_latent": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _P, _P, _P, _SZ, _P, _P]),
+    "mla_decode_latent_noalloc": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                       _I, _P, _P, _P, _P]),
     "mla_combine_partials": (_I, [_P, _P, _I, _I64, _P, _P, _P]),
     "mla_out_proj_uv": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "mla_rope_inplace": (_I, [_P, _I64, _I64, _I, _P, _F, _P]),
@@ -126,6 +128,23 @@ def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, bloc
         page_size, num_pages, B, S, H, int(bool(causal)), float(scale), int(num_splits),
         int(max_seqlen), _ptr(o_lat), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
         _stream(stream)))
+
+
+def mla_decode_latent_noalloc(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen,
+                              block_table=None, kv_seq_stride=0, page_size=64, causal=False,
+                              num_splits=0, status=None, stream=None):
+    """mla_decode_latent with the split partials in the library's fixed scratch array
+    (for callers that cannot allocate device memory); see include/mla.h."""
+    B, S, H, _ = q_cat.shape
+    if block_table is not None:
+        num_pages, max_pages = kv.shape[0], block_table.shape[1]
+    else:
+        num_pages, max_pages = 0, 0
+        kv_seq_stride = kv_seq_stride or kv.shape[1]
+    _check("mla_decode_latent_noalloc", lib().mla_decode_latent_noalloc(
+        _ptr(q_cat), _ptr(kv), int(kv_seq_stride), _ptr(seqlens), _ptr(block_table), max_pages,
+        page_size, num_pages, B, S, H, int(bool(causal)), float(scale), int(num_splits),
+        int(max_seqlen), _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def mla_combine_partials(o_part, lse_part, o_lat, lse, stream=None):
