@@ -85,7 +85,9 @@ int mla_device_sm_count(void);
  *   q_cat   bf16 [B,S,H,576]     output, the query row matched to a 576-wide cache row
  *
  * RoPE pairs interleaved elements (2i, 2i+1) and turns them by pos * theta^(-2i/64)
- * ([MLA] "구현", _apply_rope).
+ * ([MLA] "구현", _apply_rope).  The product runs on the tensor core (bf16 inputs, fp32
+ * accumulation).  If a pipeline wait inside the kernel expires, the affected q~ values
+ * are NaN.
  */
 mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* w_uk,
                         const int32_t* q_pos, float rope_theta, int B, int S, int H,
@@ -190,8 +192,12 @@ mla_status mla_combine_partials(const float* o_part, const float* lse_part, int 
 /*
  * mla_out_proj_uv -- value up-projection, [CALC] "Value 투영을 가중합 뒤로 옮기기":
  * a (C U^V) = (a C) U^V, applied once per head after the latents are mixed.
- *   o[b,s,h,:] = sum_i o_lat[b,s,h,i] * W_UV[h,i,:]       (fp32 accumulate)
+ *   o[b,s,h,:] = sum_i bf16(o_lat[b,s,h,i]) * W_UV[h,i,:]   (tensor core, fp32 accumulate)
  *   o_lat fp32 [B,S,H,512]; w_uv bf16 [H,512,128]; o fp32 [B,S,H,128]
+ * o_lat is rounded to bf16 on its way to the tensor core (unit roundoff 2^-8), so each
+ * output differs from the exact product by at most 2^-8 * sum_i |o_lat_i W_UV[h,i,n]|
+ * plus fp32 rounding.
+ * If a pipeline wait inside the kernel expires, the affected outputs are NaN.
  */
 mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int S, int H,
                            float* o, mla_stream stream);

@@ -1,6 +1,7 @@
 // Shared definitions of libmla's kernels (internal; the public ABI is include/mla.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -85,6 +86,13 @@ __device__ __forceinline__ void split_range(const DecodeParams& p, int T, int s,
   t0 = split * chunk;
   t1 = min(t0 + chunk, n_vis);
 }
+
+// A 2D TMA tensor map over `rows` rows of `inner` elements (bf16 or fp32), rows
+// `row_stride_bytes` apart, copied in boxes of box_inner x box_rows.  Returns false if
+// the driver rejects it (alignment, sizes) or the entry point is unavailable.
+bool encode_tma_2d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t inner,
+                   uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                   uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // Launchers (defined next to their kernels).
 cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_rope,

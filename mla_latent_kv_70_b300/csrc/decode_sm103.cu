@@ -20,7 +20,7 @@
 //   * the partials are swapped through distributed shared memory as bf16 (st.async,
 //     counted on the receiver's mbarrier).  The cross-SM path moves ~16 B/clk per SM,
 //     so fp32 partials would cost more than the HBM stream; bf16 halves that and adds an
-//     error of the same order as storing q~ in bf16 (2^-9 of the partial sum).  Each CTA
+//     error of the same order as storing q~ in bf16 (2^-8 of the partial sum).  Each CTA
 //     adds its own fp32 partial to the peer's bf16 partial and normalises its half of O
 //     with its own softmax sums, so the two halves need not agree bit for bit;
 //   * the exchange runs one tile ahead of the softmax, P (bf16) goes to shared memory
@@ -497,35 +497,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   cluster_sync();  // neither CTA leaves while the other may still touch its shared memory
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_cols,
                  uint32_t box_rows, CUtensorMapSwizzle sw) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)kRow, rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kRow * 2};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tma_2d(map, true, base, kRow, rows, (uint64_t)kRow * 2, box_cols, box_rows, sw);
 }
 
 }  // namespace
