@@ -17,17 +17,20 @@
 //     of every cache row; its TMA loads only those (each cache byte is read once);
 //   * each CTA computes the partial score over its 288 columns into TMEM (A operand =
 //     its half of q~, held in TMEM; the rope half of q from shared memory);
-//   * the partials are swapped through distributed shared memory as bf16 (st.async,
-//     counted on the receiver's mbarrier).  The cross-SM path moves ~16 B/clk per SM,
-//     so fp32 partials would cost more than the HBM stream; bf16 halves that and adds an
-//     error of the same order as storing q~ in bf16 (2^-8 of the partial sum).  Each CTA
-//     adds its own fp32 partial to the peer's bf16 partial and normalises its half of O
-//     with its own softmax sums, so the two halves need not agree bit for bit;
+//   * the partials are swapped through distributed shared memory as bf16, by 16-byte
+//     st.async into the peer's receive buffer, counted (complete_tx) on its mbarrier.
+//     No "buffer free" signal travels back: under HBM load a remote release-arrive took
+//     ~3900 cycles to land, and the data flow already orders each reuse (a CTA sends
+//     tile i+1 only after reading tile i).  bf16 halves the bytes of fp32 partials and
+//     adds an error of the same order as storing q~ in bf16 (2^-8 of the partial sum).
+//     Each CTA adds its own fp32 partial to the peer's bf16 partial and normalises its
+//     half of O with its own softmax sums, so the two halves need not agree bit for bit;
 //   * the exchange runs one tile ahead of the softmax, P (bf16) goes to shared memory
 //     in the 128B-swizzled K-major layout, and each CTA accumulates its 256 columns of
 //     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
-// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-5 (one per
-// TMEM lane quarter) run the exchange, the online softmax and the epilogue.
+// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-9 run the
+// exchange, the online softmax and the epilogue, two warps per TMEM lane quarter (32
+// heads), each on 32 of the 64 columns of a tile.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
 // output is rescaled only when the maximum grows by more than 2^8).
 // Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
@@ -45,20 +48,25 @@ using namespace ptx;
 
 constexpr int kN = 64;                            // cache rows per tile
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
 constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
 constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
+constexpr uint32_t kWarpXBytes = 32 * 32 * 2;     // one warp's share: 32 rows x 32 columns
 constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
 
 constexpr uint32_t kOffQRope = kStages * kStageBytes;
 constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
 constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffSlot = kOffBars + 256;
+constexpr uint32_t kOffRed = kOffBars + 256;      // row maxima / sums swapped by warp pairs
+constexpr uint32_t kRedBytes = 3 * 2 * 128 * 4;   // [tile parity 0, 1 | sums][half][row]
+constexpr uint32_t kOffSlot = kOffRed + kRedBytes;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kOffP % 1024 == 0, "P tiles need 1024-byte alignment (128B swizzle atoms)");
 
 // TMEM columns.
@@ -73,15 +81,15 @@ enum Bar {
   kKvFull = 0,                   // [kStages] TMA -> MMA
   kKvEmpty = kStages,            // [kStages] MMA -> TMA
   kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
-  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: score buffer read (4 warps)
-  kPFull = 2 * kStages + 4,      // [2] softmax -> MMA: P in shared memory (128 threads)
+  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: score buffer read (8 warps)
+  kPFull = 2 * kStages + 4,      // [2] softmax -> MMA: P in shared memory (256 threads)
   kPvDone = 2 * kStages + 6,     // [2] MMA -> softmax: PV finished (P buffer, O stable)
-  kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by thread 0)
-  kSendFree = 2 * kStages + 10,  // [2] peer has read our previous partial (4 remote warps)
-  kQFull = 2 * kStages + 12,
-  kQReady = 2 * kStages + 13,
-  kDrain = 2 * kStages + 14,
-  kNumBars = 2 * kStages + 15
+  kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by one thread here)
+  kQFull = 2 * kStages + 10,
+  kQReady = 2 * kStages + 11,
+  kDrain = 2 * kStages + 12,
+  kRed = 2 * kStages + 13,       // [4] the two warps of a lane quarter swapped maxima / sums
+  kNumBars = 2 * kStages + 17
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -136,15 +144,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
-      mbar_init(bar(kSFree + i), 4);
-      mbar_init(bar(kPFull + i), 128);
+      mbar_init(bar(kSFree + i), kSoftmaxWarps);
+      mbar_init(bar(kPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(kPvDone + i), 1);
       mbar_init(bar(kRecvFull + i), 1);
-      mbar_init(bar(kSendFree + i), 4);
     }
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQReady), 128);
+    mbar_init(bar(kQReady), 32 * kSoftmaxWarps);
     mbar_init(bar(kDrain), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar(kRed + q), 64);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -205,11 +213,10 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     if (lane == 0 && ntiles > 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
       const uint32_t id_pv = idesc_bf16(128, 256, false, true);
-      auto issue_qk = [&](int i) -> bool {
-        const int st = i % kStages;
-        if (!mbar_wait(bar(kKvFull + st), (uint32_t)(i / kStages) & 1u, kWaitNs)) return false;
+      // QK(i): partial scores of tile i into S buffer i & 1.
+      auto issue_qk = [&](int i) {
         tc_fence_after();
-        const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
+        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
         // latent half: A = q~ half from TMEM, B = cache rows (K-major, 128B swizzle)
 #pragma unroll
@@ -223,31 +230,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           mma_ss(d, smem_desc(s0 + kOffQRope + 32u * k, 16, 512, kSwizzle64B),
                  smem_desc(stage + 4 * kBoxBytes + 32u * k, 16, 512, kSwizzle64B), id_qk, 1);
         mma_commit(bar(kSFull + (i & 1)));
-        return true;
       };
-      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
-      tc_fence_after();
-      for (int i = 0; i < 2 && i < ntiles && !aborted; ++i)
-        if (!issue_qk(i)) aborted = true;
-      for (int i = 0; i < ntiles && !aborted; ++i) {
-        const int buf = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (i + 2 < ntiles) {
-          // S buffer `buf` is free once the softmax has read tile i from it.
-          if (!mbar_wait(bar(kSFree + buf), ph, kWaitNs) || !issue_qk(i + 2)) {
-            aborted = true;
-            break;
-          }
-        }
-        if (!mbar_wait(bar(kPFull + buf), ph, kWaitNs)) {
-          aborted = true;
-          break;
-        }
+      // PV(i): O half += P(i) . V(i), then release the stage and the P buffer.
+      auto issue_pv = [&](int i) {
         tc_fence_after();
+        const int buf = i & 1;
         const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const uint32_t pbuf = s0 + kOffP + (uint32_t)buf * kPBytes;
-        // O half += P . V: A = P (smem, K-major), B = the staged tile read MN-major
-        // (N = 256 latent columns over four 64-column boxes, K = 16 rows per step).
+        // A = P (smem, K-major), B = the staged tile read MN-major (N = 256 latent
+        // columns over four 64-column boxes, K = 16 rows per step).
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k)
           mma_ss(tb + kTmemO, smem_desc(pbuf + 32u * k, 16, 1024, kSwizzle128B),
@@ -255,55 +246,99 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
                  (i > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(kKvEmpty + i % kStages));
         mma_commit(bar(kPvDone + buf));
+      };
+      auto qk_ready = [&](int i) {
+        return (i < 2 || mbar_poll(bar(kSFree + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u)) &&
+               mbar_poll(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u);
+      };
+      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
+      // Issue whichever MMA is ready: QK(j) once its tile has landed and S buffer j & 1
+      // has been read, PV(i) once P(i) is in shared memory.  Neither waits behind the
+      // other, so a PV never waits for the next tile's HBM load.
+      int next_qk = 0, next_pv = 0;
+      uint64_t t_idle = 0;
+      uint32_t polls = 0;
+      while (!aborted && next_pv < ntiles) {
+        bool progressed = false;
+        if (next_qk < ntiles && qk_ready(next_qk)) {
+          issue_qk(next_qk++);
+          progressed = true;
+        }
+        if (next_pv < next_qk && mbar_poll(bar(kPFull + (next_pv & 1)), (uint32_t)(next_pv >> 1) & 1u)) {
+          issue_pv(next_pv++);
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else if ((++polls & 63u) == 0) {
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) t_idle = now;
+          else if (now - t_idle > kWaitNs) aborted = true;
+        }
       }
       mma_commit(bar(kDrain));
       mbar_wait(bar(kDrain), 0, kWaitNs);
     }
   } else {
-    // ---------------- exchange / softmax / epilogue (warps 2..5) ----------------
+    // ---------------- exchange / softmax / epilogue (warps 2..9) ----------------
+    // Warp w covers TMEM lane quarter q = w % 4 (heads 32q..32q+31) and columns
+    // 32c..32c+31 of each 64-row tile, c = (w - 2) / 4; the two warps of a quarter agree
+    // on each row's maximum (and, at the end, its sum) through shared memory and the
+    // quarter's mbarrier kRed + q, one phase per tile.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
     const int64_t qrow = (int64_t)m * p.H + h;
+    const uint32_t col0 = 32u * (uint32_t)half;      // first tile column of this warp
     float m_ref = -INFINITY, l = 0.f;
+    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [3][2 half][128 rows]
 
     const uint32_t recv_local = s0 + kOffRecv;
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
-    const uint32_t free_bar_peer = map_to_rank(bar(kSendFree), peer);
 
-    // Partial scores of tile j: TMEM -> bf16 -> the peer's receive buffer.
-    // Layout there: [8 chunks][128 rows][16 B], chunk c holding columns 8c..8c+7.
-    auto send = [&](int j) -> bool {
+    // Own fp32 partial scores of tile j (this warp's 32 columns) into x, and the same
+    // rounded to bf16 to the peer.  Exchange layout (staging and receive buffers alike):
+    // 8 blocks of 2 KB, block (half, quarter) = [4 chunks][32 rows][16 B], chunk k
+    // holding tile columns 32*half + 8k .. +7.
+    const uint32_t xoff = (uint32_t)(half * 4 + quarter) * kWarpXBytes;
+    auto send = [&](int j, float (&x)[32]) -> bool {
       const int buf = j & 1;
       if (!warp_wait(bar(kSFull + buf), (uint32_t)(j >> 1) & 1u)) return false;
-      if (j >= 2 && !warp_wait_cluster(bar(kSendFree + buf), (uint32_t)((j - 2) >> 1) & 1u))
-        return false;
       tc_fence_after();
-      uint32_t r[32], pk[32];
-      tmem_ld32(tb + lane_off + kTmemS + 64u * buf, r);
+      uint32_t r[32];
+      tmem_ld32(tb + lane_off + kTmemS + 64u * buf + col0, r);
       tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSFree + buf));
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) pk[c] = f2_to_bf2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
-      tmem_ld32(tb + lane_off + kTmemS + 64u * buf + 32u, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pk[16 + c] = f2_to_bf2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
-      const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + (uint32_t)h * 16u;
+      for (int c = 0; c < 16; ++c) {
+        x[2 * c] = __uint_as_float(r[2 * c]);
+        x[2 * c + 1] = __uint_as_float(r[2 * c + 1]);
+        pk[c] = f2_to_bf2(x[2 * c], x[2 * c + 1]);
+      }
+      // The peer's receive buffer `buf` is reused two tiles later without a handshake:
+      // this warp sends tile j only after it has read tile j-1 from the peer, which the
+      // peer sent only after its own reads of tile j-2 from that buffer.
+      const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + xoff + (uint32_t)lane * 16u;
       const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(dst + (uint32_t)c * 2048u, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3], rb);
+      for (int c = 0; c < 4; ++c)
+        st_async_v4(dst + (uint32_t)c * 512u, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3], rb);
       return true;
     };
 
+    float xc[32], xn[32];
     if (ntiles > 0) {
-      // q~ half of this head into TMEM (A operand of the score MMA).
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank);
+      // This warp's 128 of the 256 q~ columns of its head into TMEM (A operand of the
+      // score MMA, bf16 pairs packed in 32-bit columns).
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * half);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -313,61 +348,50 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           r[4 * v + 2] = w.z;
           r[4 * v + 3] = w.w;
         }
-        tmem_st32(tb + lane_off + kTmemQ + 32u * c, r);
+        tmem_st32(tb + lane_off + kTmemQ + 64u * half + 32u * c, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
-      if (h == 0) {
+      if (h == 0 && half == 0) {
         mbar_arrive_expect_tx(bar(kRecvFull + 0), kRecvBytes);
         if (ntiles > 1) mbar_arrive_expect_tx(bar(kRecvFull + 1), kRecvBytes);
       }
-      if (!send(0)) aborted = true;
+      if (!send(0, xc)) aborted = true;
     }
 
     for (int i = 0; i < ntiles && !aborted; ++i) {
       const int buf = i & 1;
       const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      // Keep the exchange one tile ahead of the softmax.
-      if (i + 1 < ntiles && !send(i + 1)) {
+      if (!warp_wait_cluster(bar(kRecvFull + buf), ph)) {
         aborted = true;
         break;
       }
-      if (!warp_wait(bar(kRecvFull + buf), ph)) {
-        aborted = true;
-        break;
-      }
-      // Re-arm this buffer's barrier for tile i+2 before telling the peer it may send it.
-      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
-      // Own fp32 partial (still in TMEM) + the peer's bf16 partial.
-      float x[kN];
+      // Re-arm this buffer's barrier for tile i+2.  The peer sends tile i+2 only after it
+      // has received tile i+1 from every warp here, which each sends after reading tile i,
+      // so no waiter misses a phase.
+      if (h == 0 && half == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
+      // Own fp32 partial + the peer's bf16 partial.
       {
-        uint32_t r[32];
-        tmem_ld32(tb + lane_off + kTmemS + 64u * buf, r);
-        tmem_ld_wait();
+        const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + xoff + (uint32_t)lane * 16u;
+        uint4 w[4];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-        tmem_ld32(tb + lane_off + kTmemS + 64u * buf + 32u, r);
-        tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) w[c] = ld_shared_u4(rl + (uint32_t)c * 512u);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + buf));
-      const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + (uint32_t)h * 16u;
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 w = ld_shared_u4(rl + (uint32_t)c * 2048u);
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
-          x[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
+          for (int u = 0; u < 4; ++u) {
+            xc[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
+            xc[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
+          }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(free_bar_peer + 8u * (uint32_t)buf);
+      // Keep the exchange one tile ahead of the softmax.
+      if (i + 1 < ntiles && !send(i + 1, xn)) {
+        aborted = true;
+        break;
+      }
 
       // Readable rows of this tile.
       const int t = t0 + i * kN;
@@ -378,37 +402,45 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       if (valid < kN) {
 #pragma unroll
-        for (int j = 0; j < kN; ++j)
-          if (j >= valid) x[j] = -INFINITY;
+        for (int j = 0; j < 32; ++j)
+          if ((int)col0 + j >= valid) xc[j] = -INFINITY;
       }
       float mx;
       {
-        float t16[16];
+        float t8[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) t16[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(x[j + 32], x[j + 48]));
+        for (int j = 0; j < 8; ++j) t8[j] = fmaxf(fmaxf(xc[j], xc[j + 8]), fmaxf(xc[j + 16], xc[j + 24]));
 #pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
+        for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
-          for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
-        mx = t16[0] * p.scale_log2;
+          for (int j = 0; j < w; ++j) t8[j] = fmaxf(t8[j], t8[j + w]);
+        // Both warps of the quarter see the same row maximum.
+        red[(buf * 2 + half) * 128 + h] = t8[0];
+        mbar_arrive(bar(kRed + quarter));
+        if (!warp_wait(bar(kRed + quarter), (uint32_t)i & 1u)) {
+          aborted = true;
+          break;
+        }
+        mx = fmaxf(t8[0], red[(buf * 2 + (half ^ 1)) * 128 + h]) * p.scale_log2;
       }
       // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
       const float alpha = grow ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
       if (__any_sync(0xffffffffu, grow && i > 0)) {
-        // Rescale this warp's rows of O once PV(i-1) has landed.
+        // Rescale this warp's rows and half of the O columns once PV(i-1) has landed.
         const int jp = i - 1;
         if (!warp_wait(bar(kPvDone + (jp & 1)), (uint32_t)(jp >> 1) & 1u)) aborted = true;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
-          tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
+          const uint32_t ta = tb + lane_off + kTmemO + 128u * half + 32u * c;
+          tmem_ld32(ta, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(tb + lane_off + kTmemO + 32u * c, r);
+          tmem_st32(ta, r);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -424,17 +456,18 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       const uint32_t prow = s0 + kOffP + (uint32_t)buf * kPBytes + (uint32_t)h * 128u;
       float ps = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float a = ex2_approx(fmaf(x[8 * c + 2 * u], p.scale_log2, neg));
-          const float d = ex2_approx(fmaf(x[8 * c + 2 * u + 1], p.scale_log2, neg));
+          const float a = ex2_approx(fmaf(xc[8 * c + 2 * u], p.scale_log2, neg));
+          const float d = ex2_approx(fmaf(xc[8 * c + 2 * u + 1], p.scale_log2, neg));
           ps += a + d;
           w[u] = f2_to_bf2(a, d);
         }
-        // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7).
-        st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+        // 128B swizzle: 16-byte chunk k of row h sits at chunk k ^ (h & 7).
+        const int k = 4 * half + c;
+        st_shared_u4(prow + (uint32_t)((k ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
       }
       l += ps;
 
@@ -443,7 +476,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       if (valid < kN) {
         const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const int nrow = kN - valid;
-        for (int idx = h; idx < nrow * 32; idx += 128) {      // 4 boxes x 8 chunks per row
+        for (int idx = tid - 64; idx < nrow * 32; idx += 32 * kSoftmaxWarps) {   // 4 boxes x 8 chunks per row
           const int row = valid + idx / 32, c = idx % 32;
           st_shared_v4_zero(stage + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u +
                             (uint32_t)(c & 7) * 16u);
@@ -451,24 +484,35 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kPFull + buf));
+#pragma unroll
+      for (int j = 0; j < 32; ++j) xc[j] = xn[j];
     }
 
-    // Epilogue: O half / l -> global.
+    // Epilogue: this warp's 128 O columns of its rows, divided by the row sum.
+    float lt = l;
+    if (ntiles > 0 && !aborted) {
+      red[(2 * 2 + half) * 128 + h] = l;
+      mbar_arrive(bar(kRed + quarter));
+      if (warp_wait(bar(kRed + quarter), (uint32_t)ntiles & 1u))
+        lt = l + red[(2 * 2 + (half ^ 1)) * 128 + h];
+      else
+        aborted = true;
+    }
     const int64_t rows_all = (int64_t)p.B * p.S * p.H;
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
-    float* out = p.o_out + orow * kDc + 256 * rank;
-    const bool have = ntiles > 0 && l > 0.f;
+    float* out = p.o_out + orow * kDc + 256 * rank + 128 * half;
+    const bool have = ntiles > 0 && lt > 0.f;
     if (ntiles > 0 && !aborted) {
       const int last = ntiles - 1;
       if (!warp_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u)) aborted = true;
     }
     tc_fence_after();
-    const float inv = have ? 1.f / l : 0.f;
+    const float inv = have ? 1.f / lt : 0.f;
     if (ntiles > 0 && !aborted) {
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
+        tmem_ld32(tb + lane_off + kTmemO + 128u * half + 32u * c, r);
         tmem_ld_wait();
         if (head_ok) {
           // A row that saw no readable position (l == 0) is written as exact zeros.
@@ -481,10 +525,10 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         }
       }
     } else if (head_ok) {
-      for (int v = 0; v < 64; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int v = 0; v < 32; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (head_ok && rank == 0)
-      p.lse_out[orow] = have ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    if (head_ok && rank == 0 && half == 0)
+      p.lse_out[orow] = have ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
   }
 
   if (aborted) raise_flag(p.status, kFlagTimeout);
