@@ -25,12 +25,14 @@
 //     adds an error of the same order as storing q~ in bf16 (2^-8 of the partial sum).
 //     Each CTA adds its own fp32 partial to the peer's bf16 partial and normalises its
 //     half of O with its own softmax sums, so the two halves need not agree bit for bit;
-//   * the exchange runs one tile ahead of the softmax, P (bf16) goes to shared memory
+//   * P (bf16) goes to shared memory
 //     in the 128B-swizzled K-major layout, and each CTA accumulates its 256 columns of
 //     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
-// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-9 run the
-// exchange, the online softmax and the epilogue, two warps per TMEM lane quarter (32
-// heads), each on 32 of the 64 columns of a tile.
+// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-5 (one per
+// TMEM lane quarter of 32 heads) swap the partial scores with the peer and write the
+// full scores back to TMEM, warps 6-13 (two per quarter, 32 of the 64 columns of a tile
+// each) run the online softmax and the epilogue.  Exchange and softmax of different
+// tiles overlap.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
 // output is rescaled only when the maximum grows by more than 2^8).
 // Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
@@ -48,22 +50,23 @@ using namespace ptx;
 
 constexpr int kN = 64;                            // cache rows per tile
 constexpr int kStages = 4;
+constexpr int kExchWarps = 4;                     // one per TMEM lane quarter
 constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+constexpr int kThreads = 32 * (2 + kExchWarps + kSoftmaxWarps);
 constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
 constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
-constexpr uint32_t kWarpXBytes = 32 * 32 * 2;     // one warp's share: 32 rows x 32 columns
+constexpr uint32_t kQuarterXBytes = 32 * kN * 2;  // one lane quarter's share: 32 rows x 64 columns
 constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
 
 constexpr uint32_t kOffQRope = kStages * kStageBytes;
 constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
 constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
-constexpr uint32_t kOffRed = kOffBars + 256;      // row maxima / sums swapped by warp pairs
-constexpr uint32_t kRedBytes = 3 * 2 * 128 * 4;   // [tile parity 0, 1 | sums][half][row]
+constexpr uint32_t kOffRed = kOffBars + 256;      // row sums swapped by warp pairs
+constexpr uint32_t kRedBytes = 2 * 128 * 4;       // [half][row]
 constexpr uint32_t kOffSlot = kOffRed + kRedBytes;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -81,15 +84,16 @@ enum Bar {
   kKvFull = 0,                   // [kStages] TMA -> MMA
   kKvEmpty = kStages,            // [kStages] MMA -> TMA
   kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
-  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: score buffer read (8 warps)
+  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: full scores read (8 warps)
   kPFull = 2 * kStages + 4,      // [2] softmax -> MMA: P in shared memory (256 threads)
   kPvDone = 2 * kStages + 6,     // [2] MMA -> softmax: PV finished (P buffer, O stable)
   kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by one thread here)
   kQFull = 2 * kStages + 10,
   kQReady = 2 * kStages + 11,
   kDrain = 2 * kStages + 12,
-  kRed = 2 * kStages + 13,       // [4] the two warps of a lane quarter swapped maxima / sums
-  kNumBars = 2 * kStages + 17
+  kRed = 2 * kStages + 13,       // [4] the two softmax warps of a lane quarter swapped sums
+  kSReady = 2 * kStages + 17,    // [2] exchange -> softmax: full scores in TMEM (4 warps)
+  kNumBars = 2 * kStages + 19
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -150,7 +154,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_init(bar(kRecvFull + i), 1);
     }
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQReady), 32 * kSoftmaxWarps);
+    mbar_init(bar(kQReady), 32 * kExchWarps);
+    for (int i = 0; i < 2; ++i) mbar_init(bar(kSReady + i), kExchWarps);
     mbar_init(bar(kDrain), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kRed + q), 64);
     fence_mbar_init();
@@ -214,36 +219,35 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
       const uint32_t id_pv = idesc_bf16(128, 256, false, true);
       // QK(i): partial scores of tile i into S buffer i & 1.
+      // Shared-memory matrix descriptors are built once per tile; the 14-bit start
+      // address field holds (address >> 4), so stepping through a tile adds a
+      // compile-time constant to the 64-bit descriptor, keeping the issue loop short.
+      const uint64_t qrope_desc = smem_desc(s0 + kOffQRope, 16, 512, kSwizzle64B);
+      // QK(i): partial scores of tile i into S buffer i & 1.  Steps 0-15: latent half
+      // (A = q~ half from TMEM, B = cache rows, K-major, 128B swizzle); steps 16-17: rope
+      // half (A = q^R half from smem, B = k^R half, 64B swizzle).
       auto issue_qk = [&](int i) {
-        tc_fence_after();
         const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
-        // latent half: A = q~ half from TMEM, B = cache rows (K-major, 128B swizzle)
+        const uint64_t kv = smem_desc(stage, 16, 1024, kSwizzle128B);
+        const uint64_t kr = smem_desc(stage + 4 * kBoxBytes, 16, 512, kSwizzle64B);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint32_t box = stage + (uint32_t)(k >> 2) * kBoxBytes + (uint32_t)(k & 3) * 32u;
-          mma_ts(d, tb + kTmemQ + 8u * k, smem_desc(box, 16, 1024, kSwizzle128B), id_qk, k > 0);
-        }
-        // rope half: A = q^R half (smem), B = k^R half (64B swizzle)
+        for (int k = 0; k < 16; ++k)
+          mma_ts(d, tb + kTmemQ + 8u * k, kv + (((k >> 2) * kBoxBytes + (k & 3) * 32u) >> 4), id_qk, k > 0);
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
-          mma_ss(d, smem_desc(s0 + kOffQRope + 32u * k, 16, 512, kSwizzle64B),
-                 smem_desc(stage + 4 * kBoxBytes + 32u * k, 16, 512, kSwizzle64B), id_qk, 1);
+        for (int k = 0; k < 2; ++k) mma_ss(d, qrope_desc + 2u * k, kr + 2u * k, id_qk, 1);
         mma_commit(bar(kSFull + (i & 1)));
       };
-      // PV(i): O half += P(i) . V(i), then release the stage and the P buffer.
+      // PV(i): O half += P(i) . V(i), then release the stage and the P buffer.  A = P
+      // (smem, K-major), B = the staged tile read MN-major (N = 256 latent columns over
+      // four 64-column boxes, K = 16 rows per step).
       auto issue_pv = [&](int i) {
-        tc_fence_after();
         const int buf = i & 1;
-        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
-        const uint32_t pbuf = s0 + kOffP + (uint32_t)buf * kPBytes;
-        // A = P (smem, K-major), B = the staged tile read MN-major (N = 256 latent
-        // columns over four 64-column boxes, K = 16 rows per step).
+        const uint64_t pd = smem_desc(s0 + kOffP + (uint32_t)buf * kPBytes, 16, 1024, kSwizzle128B);
+        const uint64_t vd = smem_desc(s0 + (uint32_t)(i % kStages) * kStageBytes, 8192, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k)
-          mma_ss(tb + kTmemO, smem_desc(pbuf + 32u * k, 16, 1024, kSwizzle128B),
-                 smem_desc(stage + 2048u * k, 8192, 1024, kSwizzle128B), id_pv,
-                 (i > 0 || k > 0) ? 1u : 0u);
+          mma_ss(tb + kTmemO, pd + 2u * k, vd + 128u * k, id_pv, (i > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(kKvEmpty + i % kStages));
         mma_commit(bar(kPvDone + buf));
       };
@@ -253,19 +257,21 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       };
       if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
       // Issue whichever MMA is ready: QK(j) once its tile has landed and S buffer j & 1
-      // has been read, PV(i) once P(i) is in shared memory.  Neither waits behind the
-      // other, so a PV never waits for the next tile's HBM load.
+      // has been read, PV(i) once P(i) is in shared memory (a PV first, so that it does
+      // not wait behind a QK chain).
       int next_qk = 0, next_pv = 0;
       uint64_t t_idle = 0;
       uint32_t polls = 0;
       while (!aborted && next_pv < ntiles) {
         bool progressed = false;
-        if (next_qk < ntiles && qk_ready(next_qk)) {
-          issue_qk(next_qk++);
+        if (next_pv < next_qk && mbar_poll(bar(kPFull + (next_pv & 1)), (uint32_t)(next_pv >> 1) & 1u)) {
+          tc_fence_after();
+          issue_pv(next_pv++);
           progressed = true;
         }
-        if (next_pv < next_qk && mbar_poll(bar(kPFull + (next_pv & 1)), (uint32_t)(next_pv >> 1) & 1u)) {
-          issue_pv(next_pv++);
+        if (next_qk < ntiles && qk_ready(next_qk)) {
+          tc_fence_after();
+          issue_qk(next_qk++);
           progressed = true;
         }
         if (progressed) {
@@ -279,66 +285,25 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mma_commit(bar(kDrain));
       mbar_wait(bar(kDrain), 0, kWaitNs);
     }
-  } else {
-    // ---------------- exchange / softmax / epilogue (warps 2..9) ----------------
-    // Warp w covers TMEM lane quarter q = w % 4 (heads 32q..32q+31) and columns
-    // 32c..32c+31 of each 64-row tile, c = (w - 2) / 4; the two warps of a quarter agree
-    // on each row's maximum (and, at the end, its sum) through shared memory and the
-    // quarter's mbarrier kRed + q, one phase per tile.
+  } else if (warp < 2 + kExchWarps) {
+    // ---------------- exchange (warps 2..5, one per TMEM lane quarter) ----------------
+    // Per tile: own fp32 partial scores (64 columns of 32 heads) out of TMEM, a bf16 copy
+    // to the peer, the peer's bf16 partial in, the sum written back over the partial.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
     const int64_t qrow = (int64_t)m * p.H + h;
-    const uint32_t col0 = 32u * (uint32_t)half;      // first tile column of this warp
-    float m_ref = -INFINITY, l = 0.f;
-    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [3][2 half][128 rows]
-
+    const uint32_t xoff = (uint32_t)quarter * kQuarterXBytes + (uint32_t)lane * 16u;
     const uint32_t recv_local = s0 + kOffRecv;
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
-
-    // Own fp32 partial scores of tile j (this warp's 32 columns) into x, and the same
-    // rounded to bf16 to the peer.  Exchange layout (staging and receive buffers alike):
-    // 8 blocks of 2 KB, block (half, quarter) = [4 chunks][32 rows][16 B], chunk k
-    // holding tile columns 32*half + 8k .. +7.
-    const uint32_t xoff = (uint32_t)(half * 4 + quarter) * kWarpXBytes;
-    auto send = [&](int j, float (&x)[32]) -> bool {
-      const int buf = j & 1;
-      if (!warp_wait(bar(kSFull + buf), (uint32_t)(j >> 1) & 1u)) return false;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tb + lane_off + kTmemS + 64u * buf + col0, r);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + buf));
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        x[2 * c] = __uint_as_float(r[2 * c]);
-        x[2 * c + 1] = __uint_as_float(r[2 * c + 1]);
-        pk[c] = f2_to_bf2(x[2 * c], x[2 * c + 1]);
-      }
-      // The peer's receive buffer `buf` is reused two tiles later without a handshake:
-      // this warp sends tile j only after it has read tile j-1 from the peer, which the
-      // peer sent only after its own reads of tile j-2 from that buffer.
-      const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + xoff + (uint32_t)lane * 16u;
-      const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        st_async_v4(dst + (uint32_t)c * 512u, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3], rb);
-      return true;
-    };
-
-    float xc[32], xn[32];
     if (ntiles > 0) {
-      // This warp's 128 of the 256 q~ columns of its head into TMEM (A operand of the
-      // score MMA, bf16 pairs packed in 32-bit columns).
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * half);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      // This head's 256 q~ columns into TMEM (A operand of the score MMA, bf16 pairs
+      // packed in 32-bit columns).
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -348,51 +313,105 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           r[4 * v + 2] = w.z;
           r[4 * v + 3] = w.w;
         }
-        tmem_st32(tb + lane_off + kTmemQ + 64u * half + 32u * c, r);
+        tmem_st32(tb + lane_off + kTmemQ + 32u * c, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
-      if (h == 0 && half == 0) {
+      if (h == 0) {
         mbar_arrive_expect_tx(bar(kRecvFull + 0), kRecvBytes);
         if (ntiles > 1) mbar_arrive_expect_tx(bar(kRecvFull + 1), kRecvBytes);
       }
-      if (!send(0, xc)) aborted = true;
     }
-
     for (int i = 0; i < ntiles && !aborted; ++i) {
       const int buf = i & 1;
       const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      const uint32_t ts = tb + lane_off + kTmemS + 64u * buf;
+      if (!warp_wait(bar(kSFull + buf), ph)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      float x[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(ts, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+        tmem_ld32(ts + 32u, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
+      }
+      // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7.
+      // Buffer `buf` is reused two tiles later without a handshake: the peer sends
+      // tile i+2 only after it has received tile i+1 from every warp here, which each
+      // sends after reading tile i.
+      {
+        const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + xoff;
+        const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(dst + (uint32_t)c * 512u, f2_to_bf2(x[8 * c], x[8 * c + 1]),
+                      f2_to_bf2(x[8 * c + 2], x[8 * c + 3]), f2_to_bf2(x[8 * c + 4], x[8 * c + 5]),
+                      f2_to_bf2(x[8 * c + 6], x[8 * c + 7]), rb);
+      }
       if (!warp_wait_cluster(bar(kRecvFull + buf), ph)) {
         aborted = true;
         break;
       }
-      // Re-arm this buffer's barrier for tile i+2.  The peer sends tile i+2 only after it
-      // has received tile i+1 from every warp here, which each sends after reading tile i,
-      // so no waiter misses a phase.
-      if (h == 0 && half == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
-      // Own fp32 partial + the peer's bf16 partial.
+      // Re-arm for tile i+2: the peer sends it only after every warp here has read tile i.
+      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
       {
-        const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + xoff + (uint32_t)lane * 16u;
-        uint4 w[4];
+        const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + xoff;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = ld_shared_u4(rl + (uint32_t)c * 512u);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = ld_shared_u4(rl + (uint32_t)c * 512u);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            xc[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
-            xc[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
+            x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
+            x[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
           }
         }
       }
-      // Keep the exchange one tile ahead of the softmax.
-      if (i + 1 < ntiles && !send(i + 1, xn)) {
+      // The full scores replace the partial in TMEM for the softmax warps.
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
+        tmem_st32(ts, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[32 + j]);
+        tmem_st32(ts + 32u, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSReady + buf));
+    }
+  } else {
+    // ---------------- softmax / epilogue (warps 6..13) ----------------
+    // Warp w covers TMEM lane quarter q = w % 4 (heads 32q..32q+31) and writes P for
+    // columns 32c..32c+31 of each tile, c = (w - 6) / 4.  Both warps of a quarter read
+    // all 64 scores of their rows, so they agree on each row's maximum without talking.
+    const int quarter = warp & 3;
+    const int half = (warp - 2 - kExchWarps) >> 2;
+    const int h = 32 * quarter + lane;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const bool head_ok = h < p.H;
+    const int64_t qrow = (int64_t)m * p.H + h;
+    float m_ref = -INFINITY, l = 0.f;
+
+    for (int i = 0; i < ntiles && !aborted; ++i) {
+      const int buf = i & 1;
+      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+      if (!warp_wait(bar(kSReady + buf), ph)) {
         aborted = true;
         break;
       }
-
+      tc_fence_after();
       // Readable rows of this tile.
       const int t = t0 + i * kN;
       int valid = min(kN, t1 - t);
@@ -400,28 +419,34 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         const int page = tile_page(p, b, t);
         if (page < 0 || page >= p.num_pages) valid = 0;
       }
-      if (valid < kN) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((int)col0 + j >= valid) xc[j] = -INFINITY;
-      }
+      // This warp's 32 columns are kept; the other 32 only enter the row maximum.
+      float x[32];
       float mx;
       {
-        float t8[8];
+        const uint32_t ts = tb + lane_off + kTmemS + 64u * buf;
+        const int c_own = 32 * half, c_oth = 32 * (half ^ 1);
+        uint32_t r[32];
+        tmem_ld32(ts + (uint32_t)c_own, r);
+        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) t8[j] = fmaxf(fmaxf(xc[j], xc[j + 8]), fmaxf(xc[j + 16], xc[j + 24]));
+        for (int j = 0; j < 32; ++j) x[j] = (c_own + j < valid) ? __uint_as_float(r[j]) : -INFINITY;
+        tmem_ld32(ts + (uint32_t)c_oth, r);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kSFree + buf));
+        float t16[16];
 #pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) t8[j] = fmaxf(t8[j], t8[j + w]);
-        // Both warps of the quarter see the same row maximum.
-        red[(buf * 2 + half) * 128 + h] = t8[0];
-        mbar_arrive(bar(kRed + quarter));
-        if (!warp_wait(bar(kRed + quarter), (uint32_t)i & 1u)) {
-          aborted = true;
-          break;
+        for (int j = 0; j < 16; ++j) {
+          const float o0 = (c_oth + j < valid) ? __uint_as_float(r[j]) : -INFINITY;
+          const float o1 = (c_oth + j + 16 < valid) ? __uint_as_float(r[j + 16]) : -INFINITY;
+          t16[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(o0, o1));
         }
-        mx = fmaxf(t8[0], red[(buf * 2 + (half ^ 1)) * 128 + h]) * p.scale_log2;
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+        mx = t16[0] * p.scale_log2;
       }
       // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
       const bool grow = mx > m_ref + kRescaleThreshold;
@@ -460,8 +485,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float a = ex2_approx(fmaf(xc[8 * c + 2 * u], p.scale_log2, neg));
-          const float d = ex2_approx(fmaf(xc[8 * c + 2 * u + 1], p.scale_log2, neg));
+          const int j = 8 * c + 2 * u;
+          const float a = ex2_approx(fmaf(x[j], p.scale_log2, neg));
+          const float d = ex2_approx(fmaf(x[j + 1], p.scale_log2, neg));
           ps += a + d;
           w[u] = f2_to_bf2(a, d);
         }
@@ -476,25 +502,25 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       if (valid < kN) {
         const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const int nrow = kN - valid;
-        for (int idx = tid - 64; idx < nrow * 32; idx += 32 * kSoftmaxWarps) {   // 4 boxes x 8 chunks per row
-          const int row = valid + idx / 32, c = idx % 32;
+        for (int idx = tid - 32 * (2 + kExchWarps); idx < nrow * 32; idx += 32 * kSoftmaxWarps) {
+          const int row = valid + idx / 32, c = idx % 32;   // 4 boxes x 8 chunks per row
           st_shared_v4_zero(stage + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u +
                             (uint32_t)(c & 7) * 16u);
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kPFull + buf));
-#pragma unroll
-      for (int j = 0; j < 32; ++j) xc[j] = xn[j];
     }
 
-    // Epilogue: this warp's 128 O columns of its rows, divided by the row sum.
+    // Epilogue: this warp's 128 O columns of its rows, divided by the row sum (the two
+    // warps of a quarter each summed their own 32 columns of every tile).
+    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2 half][128 rows]
     float lt = l;
     if (ntiles > 0 && !aborted) {
-      red[(2 * 2 + half) * 128 + h] = l;
+      red[half * 128 + h] = l;
       mbar_arrive(bar(kRed + quarter));
-      if (warp_wait(bar(kRed + quarter), (uint32_t)ntiles & 1u))
-        lt = l + red[(2 * 2 + (half ^ 1)) * 128 + h];
+      if (warp_wait(bar(kRed + quarter), 0))
+        lt = l + red[(half ^ 1) * 128 + h];
       else
         aborted = true;
     }
