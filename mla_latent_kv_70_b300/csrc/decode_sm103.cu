@@ -28,7 +28,8 @@
 //   * P (bf16) goes to shared memory
 //     in the 128B-swizzled K-major layout, and each CTA accumulates its 256 columns of
 //     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
-// Warp roles per CTA: warp 0 issues TMA, warp 1 issues tcgen05.mma, warps 2-5 (one per
+// Warp roles per CTA: warp 0 issues TMA, warp 1 issues the score MMAs (QK) and warp 14
+// the aggregation MMAs (PV), so that neither waits behind the other; warps 2-5 (one per
 // TMEM lane quarter of 32 heads) swap the partial scores with the peer and write the
 // full scores back to TMEM, warps 6-13 (two per quarter, 32 of the 64 columns of a tile
 // each) run the online softmax and the epilogue.  Exchange and softmax of different
@@ -52,7 +53,8 @@ constexpr int kN = 64;                            // cache rows per tile
 constexpr int kStages = 4;
 constexpr int kExchWarps = 4;                     // one per TMEM lane quarter
 constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quarter
-constexpr int kThreads = 32 * (2 + kExchWarps + kSoftmaxWarps);
+constexpr int kPvWarp = 2 + kExchWarps + kSoftmaxWarps;   // the warp that issues PV
+constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
@@ -93,7 +95,8 @@ enum Bar {
   kDrain = 2 * kStages + 12,
   kRed = 2 * kStages + 13,       // [4] the two softmax warps of a lane quarter swapped sums
   kSReady = 2 * kStages + 17,    // [2] exchange -> softmax: full scores in TMEM (4 warps)
-  kNumBars = 2 * kStages + 19
+  kDrainPv = 2 * kStages + 19,
+  kNumBars = 2 * kStages + 20
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -157,6 +160,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     mbar_init(bar(kQReady), 32 * kExchWarps);
     for (int i = 0; i < 2; ++i) mbar_init(bar(kSReady + i), kExchWarps);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kDrainPv), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kRed + q), 64);
     fence_mbar_init();
   }
@@ -214,19 +218,24 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       if (!mbar_wait(bar(kQFull), 0, kWaitNs)) aborted = true;
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- QK issuer ----------------
+    // QK(i): partial scores of tile i into S buffer i & 1, once the tile has landed and
+    // the softmax has read S buffer i & 1 (tile i-2).  Steps 0-15: latent half (A = q~
+    // half from TMEM, B = cache rows, K-major, 128B swizzle); steps 16-17: rope half
+    // (A = q^R half from smem, B = k^R half, 64B swizzle).  Shared-memory descriptors are
+    // built once per tile: the 14-bit start field holds (address >> 4), so stepping
+    // through a tile adds a compile-time constant to the 64-bit descriptor.
     if (lane == 0 && ntiles > 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
-      const uint32_t id_pv = idesc_bf16(128, 256, false, true);
-      // QK(i): partial scores of tile i into S buffer i & 1.
-      // Shared-memory matrix descriptors are built once per tile; the 14-bit start
-      // address field holds (address >> 4), so stepping through a tile adds a
-      // compile-time constant to the 64-bit descriptor, keeping the issue loop short.
       const uint64_t qrope_desc = smem_desc(s0 + kOffQRope, 16, 512, kSwizzle64B);
-      // QK(i): partial scores of tile i into S buffer i & 1.  Steps 0-15: latent half
-      // (A = q~ half from TMEM, B = cache rows, K-major, 128B swizzle); steps 16-17: rope
-      // half (A = q^R half from smem, B = k^R half, 64B swizzle).
-      auto issue_qk = [&](int i) {
+      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
+      for (int i = 0; i < ntiles && !aborted; ++i) {
+        if ((i >= 2 && !mbar_wait(bar(kSFree + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u, kWaitNs)) ||
+            !mbar_wait(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u, kWaitNs)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
         const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
         const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
         const uint64_t kv = smem_desc(stage, 16, 1024, kSwizzle128B);
@@ -237,12 +246,26 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) mma_ss(d, qrope_desc + 2u * k, kr + 2u * k, id_qk, 1);
         mma_commit(bar(kSFull + (i & 1)));
-      };
-      // PV(i): O half += P(i) . V(i), then release the stage and the P buffer.  A = P
-      // (smem, K-major), B = the staged tile read MN-major (N = 256 latent columns over
-      // four 64-column boxes, K = 16 rows per step).
-      auto issue_pv = [&](int i) {
+      }
+      mma_commit(bar(kDrain));
+      mbar_wait(bar(kDrain), 0, kWaitNs);
+    }
+  } else if (warp == kPvWarp) {
+    // ---------------- PV issuer ----------------
+    // PV(i): O half += P(i) . V(i) once P(i) is in shared memory, then release the
+    // stage and the P buffer.  A separate issuing warp lets a PV enter the tensor pipe
+    // while a QK chain (18 dependent MMAs) is still being issued.  A = P (smem, K-major),
+    // B = the staged tile read MN-major (N = 256 latent columns over four 64-column
+    // boxes, K = 16 rows per step).
+    if (lane == 0 && ntiles > 0) {
+      const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      for (int i = 0; i < ntiles; ++i) {
         const int buf = i & 1;
+        if (!mbar_wait(bar(kPFull + buf), (uint32_t)(i >> 1) & 1u, kWaitNs)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
         const uint64_t pd = smem_desc(s0 + kOffP + (uint32_t)buf * kPBytes, 16, 1024, kSwizzle128B);
         const uint64_t vd = smem_desc(s0 + (uint32_t)(i % kStages) * kStageBytes, 8192, 1024, kSwizzle128B);
 #pragma unroll
@@ -250,40 +273,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           mma_ss(tb + kTmemO, pd + 2u * k, vd + 128u * k, id_pv, (i > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar(kKvEmpty + i % kStages));
         mma_commit(bar(kPvDone + buf));
-      };
-      auto qk_ready = [&](int i) {
-        return (i < 2 || mbar_poll(bar(kSFree + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u)) &&
-               mbar_poll(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u);
-      };
-      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
-      // Issue whichever MMA is ready: QK(j) once its tile has landed and S buffer j & 1
-      // has been read, PV(i) once P(i) is in shared memory (a PV first, so that it does
-      // not wait behind a QK chain).
-      int next_qk = 0, next_pv = 0;
-      uint64_t t_idle = 0;
-      uint32_t polls = 0;
-      while (!aborted && next_pv < ntiles) {
-        bool progressed = false;
-        if (next_pv < next_qk && mbar_poll(bar(kPFull + (next_pv & 1)), (uint32_t)(next_pv >> 1) & 1u)) {
-          tc_fence_after();
-          issue_pv(next_pv++);
-          progressed = true;
-        }
-        if (next_qk < ntiles && qk_ready(next_qk)) {
-          tc_fence_after();
-          issue_qk(next_qk++);
-          progressed = true;
-        }
-        if (progressed) {
-          t_idle = 0;
-        } else if ((++polls & 63u) == 0) {
-          const uint64_t now = globaltimer();
-          if (t_idle == 0) t_idle = now;
-          else if (now - t_idle > kWaitNs) aborted = true;
-        }
       }
-      mma_commit(bar(kDrain));
-      mbar_wait(bar(kDrain), 0, kWaitNs);
+      mma_commit(bar(kDrainPv));
+      mbar_wait(bar(kDrainPv), 0, kWaitNs);
     }
   } else if (warp < 2 + kExchWarps) {
     // ---------------- exchange (warps 2..5, one per TMEM lane quarter) ----------------

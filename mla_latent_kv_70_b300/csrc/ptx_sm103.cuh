@@ -45,13 +45,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
                : "memory");
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or about kSuspendNs pass, so waiting warps do not take issue slots from the
+// warps that share their sub-partition.
+constexpr uint32_t kSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return done != 0;
 }
@@ -72,10 +77,10 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return done != 0;
 }
@@ -89,9 +94,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   };
   if (test()) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (test()) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
