@@ -30,10 +30,11 @@
 //     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
 // Warp roles per CTA: warp 0 issues TMA, warp 1 issues the score MMAs (QK) and warp 14
 // the aggregation MMAs (PV), so that neither waits behind the other; warps 2-5 (one per
-// TMEM lane quarter of 32 heads) swap the partial scores with the peer and write the
-// full scores back to TMEM, warps 6-13 (two per quarter, 32 of the 64 columns of a tile
-// each) run the online softmax and the epilogue.  Exchange and softmax of different
-// tiles overlap.
+// TMEM lane quarter of 32 heads) read the partial scores out of TMEM (freeing the S
+// buffer for the next QK at once), swap them with the peer, and leave the full scores
+// relative to each row's tile maximum in shared memory (fp16); warps 6-13 (two per
+// quarter, 32 of the 64 columns of a tile each) run the online softmax and the
+// epilogue.  Exchange and softmax of different tiles overlap.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
 // output is rescaled only when the maximum grows by more than 2^8).
 // Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
@@ -62,11 +63,14 @@ constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
 constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
 constexpr uint32_t kQuarterXBytes = 32 * kN * 2;  // one lane quarter's share: 32 rows x 64 columns
 constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
+constexpr uint32_t kScoreBytes = 128 * kN * 2;    // full scores handed to the softmax, fp16
 
 constexpr uint32_t kOffQRope = kStages * kStageBytes;
 constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
-constexpr uint32_t kOffBars = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffScore = kOffP + kPBytes;
+constexpr uint32_t kOffTmax = kOffScore + kScoreBytes;   // [128] tile maxima, log2 units
+constexpr uint32_t kOffBars = kOffTmax + 128 * 4;
 constexpr uint32_t kOffRed = kOffBars + 256;      // row sums swapped by warp pairs
 constexpr uint32_t kRedBytes = 2 * 128 * 4;       // [half][row]
 constexpr uint32_t kOffSlot = kOffRed + kRedBytes;
@@ -86,15 +90,16 @@ enum Bar {
   kKvFull = 0,                   // [kStages] TMA -> MMA
   kKvEmpty = kStages,            // [kStages] MMA -> TMA
   kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
-  kSFree = 2 * kStages + 2,      // [2] softmax -> MMA: full scores read (8 warps)
-  kPFull = 2 * kStages + 4,      // [2] softmax -> MMA: P in shared memory (256 threads)
-  kPvDone = 2 * kStages + 6,     // [2] MMA -> softmax: PV finished (P buffer, O stable)
+  kSFree = 2 * kStages + 2,      // [2] exchange -> QK issuer: S buffer read (4 warps)
+  kPFull = 2 * kStages + 4,      // [2] softmax -> PV issuer: P(i) in shared memory (256 threads)
+  kPvDone = 2 * kStages + 6,     // [2] PV issuer -> softmax: PV(i) finished (P buffer, O stable)
   kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by one thread here)
   kQFull = 2 * kStages + 10,
   kQReady = 2 * kStages + 11,
   kDrain = 2 * kStages + 12,
   kRed = 2 * kStages + 13,       // [4] the two softmax warps of a lane quarter swapped sums
-  kSReady = 2 * kStages + 17,    // [2] exchange -> softmax: full scores in TMEM (4 warps)
+  kSReady = 2 * kStages + 17,    // exchange -> softmax: a tile's scores in smem (128 threads)
+  kScoreFree = 2 * kStages + 18, // softmax -> exchange: the score buffer has been read (8 warps)
   kDrainPv = 2 * kStages + 19,
   kNumBars = 2 * kStages + 20
 };
@@ -151,14 +156,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
-      mbar_init(bar(kSFree + i), kSoftmaxWarps);
+      mbar_init(bar(kSFree + i), kExchWarps);
       mbar_init(bar(kPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(kPvDone + i), 1);
       mbar_init(bar(kRecvFull + i), 1);
     }
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQReady), 32 * kExchWarps);
-    for (int i = 0; i < 2; ++i) mbar_init(bar(kSReady + i), kExchWarps);
+    mbar_init(bar(kSReady), 32 * kExchWarps);
+    mbar_init(bar(kScoreFree), kSoftmaxWarps);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
     for (int q = 0; q < 4; ++q) mbar_init(bar(kRed + q), 64);
@@ -266,7 +272,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           break;
         }
         tc_fence_after();
-        const uint64_t pd = smem_desc(s0 + kOffP + (uint32_t)buf * kPBytes, 16, 1024, kSwizzle128B);
+        const uint64_t pd = smem_desc(s0 + kOffP, 16, 1024, kSwizzle128B);
         const uint64_t vd = smem_desc(s0 + (uint32_t)(i % kStages) * kStageBytes, 8192, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k)
@@ -324,18 +330,22 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         break;
       }
       tc_fence_after();
+      // Own fp32 partial scores; the S buffer is free for QK(i+2) once they are read.
       float x[64];
       {
-        uint32_t r[32];
-        tmem_ld32(ts, r);
+        uint32_t r0[32], r1[32];
+        tmem_ld32(ts, r0);
+        tmem_ld32(ts + 32u, r1);   // both requested before one wait (~290 cycles each)
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-        tmem_ld32(ts + 32u, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[32 + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __uint_as_float(r0[j]);
+          x[32 + j] = __uint_as_float(r1[j]);
+        }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kSFree + buf));
       // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7.
       // Buffer `buf` is reused two tiles later without a handshake: the peer sends
       // tile i+2 only after it has received tile i+1 from every warp here, which each
@@ -368,26 +378,61 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           }
         }
       }
-      // The full scores replace the partial in TMEM for the softmax warps.
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[j]);
-        tmem_st32(ts, r);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(x[32 + j]);
-        tmem_st32(ts + 32u, r);
+      // Readable rows of this tile, the row maximum over them (log2 units), and the
+      // scores relative to it.  The softmax takes exp2 of these, so they are stored as
+      // fp16: its error near 0, where the weights are largest, is under 2^-11 of the
+      // value (far below the bf16 rounding of P), and -inf marks an unreadable row.
+      const int t = t0 + i * kN;
+      int valid = min(kN, t1 - t);
+      if (p.block_table) {
+        const int page = tile_page(p, b, t);
+        if (page < 0 || page >= p.num_pages) valid = 0;
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSReady + buf));
+      if (valid < kN) {
+#pragma unroll
+        for (int j = 0; j < kN; ++j)
+          if (j >= valid) x[j] = -INFINITY;
+      }
+      float mx;
+      {
+        float t16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t16[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(x[j + 32], x[j + 48]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+        mx = t16[0] * p.scale_log2;
+      }
+      const float negmx = (mx == -INFINITY) ? 0.f : -mx;
+      if (i >= 1 && !warp_wait(bar(kScoreFree), (uint32_t)(i - 1) & 1u)) {
+        aborted = true;
+        break;
+      }
+      {
+        const uint32_t row = s0 + kOffScore + (uint32_t)h * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            __half2 v = __floats2half2_rn(fmaf(x[8 * c + 2 * u], p.scale_log2, negmx),
+                                          fmaf(x[8 * c + 2 * u + 1], p.scale_log2, negmx));
+            w[u] = *reinterpret_cast<uint32_t*>(&v);
+          }
+          // Chunk c of row h at chunk c ^ (h & 7): conflict-free for row-per-lane access.
+          st_shared_u4(row + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+        }
+        reinterpret_cast<float*>(smem + kOffTmax)[h] = mx;
+      }
+      mbar_arrive(bar(kSReady));
     }
   } else {
     // ---------------- softmax / epilogue (warps 6..13) ----------------
-    // Warp w covers TMEM lane quarter q = w % 4 (heads 32q..32q+31) and writes P for
-    // columns 32c..32c+31 of each tile, c = (w - 6) / 4.  Both warps of a quarter read
-    // all 64 scores of their rows, so they agree on each row's maximum without talking.
+    // Warp w covers heads 32q..32q+31, q = w % 4 (its TMEM lane quarter, for O), and
+    // writes P for columns 32c..32c+31 of each tile, c = (w - 6) / 4, from the scores and
+    // row maxima the exchange warps leave in shared memory: both warps of a quarter
+    // see the same maximum without talking.
     const int quarter = warp & 3;
     const int half = (warp - 2 - kExchWarps) >> 2;
     const int h = 32 * quarter + lane;
@@ -398,48 +443,37 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 
     for (int i = 0; i < ntiles && !aborted; ++i) {
       const int buf = i & 1;
-      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      if (!warp_wait(bar(kSReady + buf), ph)) {
+      if (!warp_wait(bar(kSReady), (uint32_t)i & 1u)) {
         aborted = true;
         break;
       }
-      tc_fence_after();
-      // Readable rows of this tile.
+      // Readable rows of this tile (for clearing the V rows past them below).
       const int t = t0 + i * kN;
       int valid = min(kN, t1 - t);
       if (p.block_table) {
         const int page = tile_page(p, b, t);
         if (page < 0 || page >= p.num_pages) valid = 0;
       }
-      // This warp's 32 columns are kept; the other 32 only enter the row maximum.
+      // This warp's 32 scores, relative to the tile maximum mx (log2 units).
       float x[32];
-      float mx;
+      const float mx = reinterpret_cast<const float*>(smem + kOffTmax)[h];
       {
-        const uint32_t ts = tb + lane_off + kTmemS + 64u * buf;
-        const int c_own = 32 * half, c_oth = 32 * (half ^ 1);
-        uint32_t r[32];
-        tmem_ld32(ts + (uint32_t)c_own, r);
-        tmem_ld_wait();
+        const uint32_t row = s0 + kOffScore + (uint32_t)h * 128u;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) x[j] = (c_own + j < valid) ? __uint_as_float(r[j]) : -INFINITY;
-        tmem_ld32(ts + (uint32_t)c_oth, r);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kSFree + buf));
-        float t16[16];
+        for (int c = 0; c < 4; ++c) {
+          const int k = 4 * half + c;
+          const uint4 w = ld_shared_u4(row + (uint32_t)((k ^ (h & 7)) << 4));
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float o0 = (c_oth + j < valid) ? __uint_as_float(r[j]) : -INFINITY;
-          const float o1 = (c_oth + j + 16 < valid) ? __uint_as_float(r[j + 16]) : -INFINITY;
-          t16[j] = fmaxf(fmaxf(x[j], x[j + 16]), fmaxf(o0, o1));
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[u]));
+            x[8 * c + 2 * u] = f.x;
+            x[8 * c + 2 * u + 1] = f.y;
+          }
         }
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
-        mx = t16[0] * p.scale_log2;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kScoreFree));
       // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
@@ -464,13 +498,14 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       l *= alpha;
       m_ref = m_new;
-      // P buffer `buf` is free once PV(i-2) is done.
-      if (i >= 2 && !warp_wait(bar(kPvDone + buf), (uint32_t)((i - 2) >> 1) & 1u)) {
+      // The P buffer is free once PV(i-1) is done.
+      if (i >= 1 && !warp_wait(bar(kPvDone + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
         aborted = true;
         break;
       }
-      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      const uint32_t prow = s0 + kOffP + (uint32_t)buf * kPBytes + (uint32_t)h * 128u;
+      // p = 2^(x + mx - m_ref); a tile with no readable row (mx = -inf) gives p = 0.
+      const float neg = (mx == -INFINITY) ? -INFINITY : mx - m_ref;
+      const uint32_t prow = s0 + kOffP + (uint32_t)h * 128u;
       float ps = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -478,8 +513,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = 8 * c + 2 * u;
-          const float a = ex2_approx(fmaf(x[j], p.scale_log2, neg));
-          const float d = ex2_approx(fmaf(x[j + 1], p.scale_log2, neg));
+          const float a = ex2_approx(x[j] + neg);
+          const float d = ex2_approx(x[j + 1] + neg);
           ps += a + d;
           w[u] = f2_to_bf2(a, d);
         }
