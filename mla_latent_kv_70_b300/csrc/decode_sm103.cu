@@ -32,8 +32,8 @@
 // the aggregation MMAs (PV), so that neither waits behind the other; warps 2-5 (one per
 // TMEM lane quarter of 32 heads) read the partial scores out of TMEM (freeing the S
 // buffer for the next QK at once), swap them with the peer, and leave the full scores
-// relative to each row's tile maximum in shared memory (fp16); warps 6-13 (two per
-// quarter, 32 of the 64 columns of a tile each) run the online softmax and the
+// relative to each row's tile maximum in shared memory (fp16), two warps per quarter
+// taking alternate tiles; warps 10-13 (one per quarter) run the online softmax and the
 // epilogue.  Exchange and softmax of different tiles overlap.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
 // output is rescaled only when the maximum grows by more than 2^8).
@@ -52,8 +52,8 @@ using namespace ptx;
 
 constexpr int kN = 64;                            // cache rows per tile
 constexpr int kStages = 4;
-constexpr int kExchWarps = 4;                     // one per TMEM lane quarter
-constexpr int kSoftmaxWarps = 8;                  // two per TMEM lane quarter
+constexpr int kExchWarps = 8;                     // two per TMEM lane quarter (even / odd tiles)
+constexpr int kSoftmaxWarps = 4;                  // one per TMEM lane quarter
 constexpr int kPvWarp = 2 + kExchWarps + kSoftmaxWarps;   // the warp that issues PV
 constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
@@ -71,9 +71,7 @@ constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
 constexpr uint32_t kOffScore = kOffP + kPBytes;
 constexpr uint32_t kOffTmax = kOffScore + kScoreBytes;   // [128] tile maxima, log2 units
 constexpr uint32_t kOffBars = kOffTmax + 128 * 4;
-constexpr uint32_t kOffRed = kOffBars + 256;      // row sums swapped by warp pairs
-constexpr uint32_t kRedBytes = 2 * 128 * 4;       // [half][row]
-constexpr uint32_t kOffSlot = kOffRed + kRedBytes;
+constexpr uint32_t kOffSlot = kOffBars + 256;
 constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kOffP % 1024 == 0, "P tiles need 1024-byte alignment (128B swizzle atoms)");
@@ -97,11 +95,11 @@ enum Bar {
   kQFull = 2 * kStages + 10,
   kQReady = 2 * kStages + 11,
   kDrain = 2 * kStages + 12,
-  kRed = 2 * kStages + 13,       // [4] the two softmax warps of a lane quarter swapped sums
   kSReady = 2 * kStages + 17,    // exchange -> softmax: a tile's scores in smem (128 threads)
   kScoreFree = 2 * kStages + 18, // softmax -> exchange: the score buffer has been read (8 warps)
   kDrainPv = 2 * kStages + 19,
-  kNumBars = 2 * kStages + 20
+  kRecvRead = 2 * kStages + 20,  // exchange -> exchange: a tile's peer partial read (4 warps)
+  kNumBars = 2 * kStages + 21
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -156,18 +154,18 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
-      mbar_init(bar(kSFree + i), kExchWarps);
+      mbar_init(bar(kSFree + i), kExchWarps / 2);
       mbar_init(bar(kPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(kPvDone + i), 1);
       mbar_init(bar(kRecvFull + i), 1);
     }
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQReady), 32 * kExchWarps);
-    mbar_init(bar(kSReady), 32 * kExchWarps);
+    mbar_init(bar(kSReady), 32 * kExchWarps / 2);
+    mbar_init(bar(kRecvRead), kExchWarps / 2);
     mbar_init(bar(kScoreFree), kSoftmaxWarps);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
-    for (int q = 0; q < 4; ++q) mbar_init(bar(kRed + q), 64);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -190,6 +188,20 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       prefetch_tmap(&maps.q_rope);
       mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
       tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+      // Row coordinate of tile i in the tensor maps (a page past the pool for a bad
+      // block-table entry: the copy then fills zeros and the tile is masked).
+      auto tile_row = [&](int i, bool flag) -> int {
+        const int t = t0 + i * kN;
+        if (p.block_table) {
+          const int page = tile_page(p, b, t);
+          if (page < 0 || page >= p.num_pages) {
+            if (flag) raise_flag(p.status, kFlagBlockTable);
+            return p.num_pages * kPage;
+          }
+          return page * kPage;
+        }
+        return (int)((int64_t)b * p.kv_seq_stride + t);
+      };
       int issued = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
@@ -198,19 +210,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           aborted = true;
           break;
         }
-        const int t = t0 + i * kN;
-        int y;
-        if (p.block_table) {
-          const int page = tile_page(p, b, t);
-          if (page < 0 || page >= p.num_pages) {
-            raise_flag(p.status, kFlagBlockTable);
-            y = p.num_pages * kPage;   // past the pool: the copy fills zeros
-          } else {
-            y = page * kPage;
-          }
-        } else {
-          y = (int)((int64_t)b * p.kv_seq_stride + t);
-        }
+        const int y = tile_row(i, true);
         const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
         mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
         for (int j = 0; j < 4; ++j)
@@ -284,10 +284,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_wait(bar(kDrainPv), 0, kWaitNs);
     }
   } else if (warp < 2 + kExchWarps) {
-    // ---------------- exchange (warps 2..5, one per TMEM lane quarter) ----------------
-    // Per tile: own fp32 partial scores (64 columns of 32 heads) out of TMEM, a bf16 copy
-    // to the peer, the peer's bf16 partial in, the sum written back over the partial.
+    // ---------------- exchange (warps 2..9) ----------------
+    // Warp w covers TMEM lane quarter q = w % 4 and the tiles i with i % 2 == e,
+    // e = (w - 2) / 4 (S buffer e, receive buffer e): two warps per quarter, so that one
+    // waits for the peer's partial of its tile while the other sends the next.  Per
+    // tile: own fp32 partial scores (64 columns of 32 heads) out of TMEM, a bf16 copy to
+    // the peer, the peer's bf16 partial in, the row maximum, and the scores relative to
+    // it (fp16) into shared memory for the softmax warps.
     const int quarter = warp & 3;
+    const int e = (warp - 2) >> 2;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
@@ -297,11 +302,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
     if (ntiles > 0) {
-      // This head's 256 q~ columns into TMEM (A operand of the score MMA, bf16 pairs
-      // packed in 32-bit columns).
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank);
+      // Half (e) of this head's 256 q~ columns into TMEM (A operand of the score MMA,
+      // bf16 pairs packed in 32-bit columns).
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * e);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -311,18 +316,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           r[4 * v + 2] = w.z;
           r[4 * v + 3] = w.w;
         }
-        tmem_st32(tb + lane_off + kTmemQ + 32u * c, r);
+        tmem_st32(tb + lane_off + kTmemQ + 64u * e + 32u * c, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
-      if (h == 0) {
-        mbar_arrive_expect_tx(bar(kRecvFull + 0), kRecvBytes);
-        if (ntiles > 1) mbar_arrive_expect_tx(bar(kRecvFull + 1), kRecvBytes);
-      }
+      if (h == 0 && e < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + e), kRecvBytes);
     }
-    for (int i = 0; i < ntiles && !aborted; ++i) {
-      const int buf = i & 1;
+    for (int i = e; i < ntiles && !aborted; i += 2) {
+      const int buf = e;
       const uint32_t ph = (uint32_t)(i >> 1) & 1u;
       const uint32_t ts = tb + lane_off + kTmemS + 64u * buf;
       if (!warp_wait(bar(kSFull + buf), ph)) {
@@ -332,24 +334,21 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       tc_fence_after();
       // Own fp32 partial scores; the S buffer is free for QK(i+2) once they are read.
       float x[64];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(ts, r0);
-        tmem_ld32(ts + 32u, r1);   // both requested before one wait (~290 cycles each)
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = __uint_as_float(r0[j]);
-          x[32 + j] = __uint_as_float(r1[j]);
-        }
-      }
+      tmem_ld32f<0>(ts, x);
+      tmem_ld32f<32>(ts + 32u, x);   // both requested before one wait (~290 cycles each)
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kSFree + buf));
       // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7.
-      // Buffer `buf` is reused two tiles later without a handshake: the peer sends
-      // tile i+2 only after it has received tile i+1 from every warp here, which each
-      // sends after reading tile i.
+      // Receive buffer `buf` is reused two tiles later without a remote handshake: tile
+      // i goes out only after the warps of tile i-1 here have read its peer partial
+      // (kRecvRead), and the peer follows the same rule, so it sends tile i+2 only after
+      // it has received tile i+1 from us, i.e. after we have read tile i.
+      if (i >= 1 && !warp_wait(bar(kRecvRead), (uint32_t)(i - 1) & 1u)) {
+        aborted = true;
+        break;
+      }
       {
         const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + xoff;
         const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
@@ -363,7 +362,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         aborted = true;
         break;
       }
-      // Re-arm for tile i+2: the peer sends it only after every warp here has read tile i.
+      // Re-arm for tile i+2: the peer sends it only after our warps have read tile i.
       if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
       {
         const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + xoff;
@@ -378,6 +377,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kRecvRead));
       // Readable rows of this tile, the row maximum over them (log2 units), and the
       // scores relative to it.  The softmax takes exp2 of these, so they are stored as
       // fp16: its error near 0, where the weights are largest, is under 2^-11 of the
@@ -428,13 +429,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_arrive(bar(kSReady));
     }
   } else {
-    // ---------------- softmax / epilogue (warps 6..13) ----------------
-    // Warp w covers heads 32q..32q+31, q = w % 4 (its TMEM lane quarter, for O), and
-    // writes P for columns 32c..32c+31 of each tile, c = (w - 6) / 4, from the scores and
-    // row maxima the exchange warps leave in shared memory: both warps of a quarter
-    // see the same maximum without talking.
+    // ---------------- softmax / epilogue (warps 10..13) ----------------
+    // Warp w covers heads 32q..32q+31, q = w % 4 (its TMEM lane quarter, for O), and all
+    // 64 columns of each tile, from the scores and row maxima the exchange warps leave in
+    // shared memory.
     const int quarter = warp & 3;
-    const int half = (warp - 2 - kExchWarps) >> 2;
     const int h = 32 * quarter + lane;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
@@ -454,22 +453,18 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         const int page = tile_page(p, b, t);
         if (page < 0 || page >= p.num_pages) valid = 0;
       }
-      // This warp's 32 scores, relative to the tile maximum mx (log2 units).
-      float x[32];
+      // The 64 scores of this row, relative to the tile maximum mx (log2 units).
+      uint32_t xh[32];   // fp16 pairs
       const float mx = reinterpret_cast<const float*>(smem + kOffTmax)[h];
       {
         const uint32_t row = s0 + kOffScore + (uint32_t)h * 128u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int k = 4 * half + c;
-          const uint4 w = ld_shared_u4(row + (uint32_t)((k ^ (h & 7)) << 4));
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&ww[u]));
-            x[8 * c + 2 * u] = f.x;
-            x[8 * c + 2 * u + 1] = f.y;
-          }
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = ld_shared_u4(row + (uint32_t)((c ^ (h & 7)) << 4));
+          xh[4 * c] = w.x;
+          xh[4 * c + 1] = w.y;
+          xh[4 * c + 2] = w.z;
+          xh[4 * c + 3] = w.w;
         }
       }
       __syncwarp();
@@ -478,27 +473,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
       const float alpha = grow ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-      if (__any_sync(0xffffffffu, grow && i > 0)) {
-        // Rescale this warp's rows and half of the O columns once PV(i-1) has landed.
-        const int jp = i - 1;
-        if (!warp_wait(bar(kPvDone + (jp & 1)), (uint32_t)(jp >> 1) & 1u)) aborted = true;
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          const uint32_t ta = tb + lane_off + kTmemO + 128u * half + 32u * c;
-          tmem_ld32(ta, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(ta, r);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-      }
       l *= alpha;
       m_ref = m_new;
-      // The P buffer is free once PV(i-1) is done.
+      // The P buffer is free, and O stable, once PV(i-1) is done.
       if (i >= 1 && !warp_wait(bar(kPvDone + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
         aborted = true;
         break;
@@ -508,21 +485,37 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       const uint32_t prow = s0 + kOffP + (uint32_t)h * 128u;
       float ps = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = 8 * c + 2 * u;
-          const float a = ex2_approx(x[j] + neg);
-          const float d = ex2_approx(x[j + 1] + neg);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xh[4 * c + u]));
+          const float a = ex2_approx(f.x + neg);
+          const float d = ex2_approx(f.y + neg);
           ps += a + d;
           w[u] = f2_to_bf2(a, d);
         }
-        // 128B swizzle: 16-byte chunk k of row h sits at chunk k ^ (h & 7).
-        const int k = 4 * half + c;
-        st_shared_u4(prow + (uint32_t)((k ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+        // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7).
+        st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
       }
       l += ps;
+
+      // Rescale this warp's rows of O (PV(i-1) has landed); xh is no longer live here.
+      if (__any_sync(0xffffffffu, grow && i > 0)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          const uint32_t ta = tb + lane_off + kTmemO + 32u * c;
+          tmem_ld32(ta, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st32(ta, r);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      }
 
       // Rows past the readable range may hold anything (even NaN): clear them in the
       // V columns of the staged tile so that 0-weighted rows add exactly 0.
@@ -539,49 +532,44 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_arrive(bar(kPFull + buf));
     }
 
-    // Epilogue: this warp's 128 O columns of its rows, divided by the row sum (the two
-    // warps of a quarter each summed their own 32 columns of every tile).
-    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2 half][128 rows]
-    float lt = l;
-    if (ntiles > 0 && !aborted) {
-      red[half * 128 + h] = l;
-      mbar_arrive(bar(kRed + quarter));
-      if (warp_wait(bar(kRed + quarter), 0))
-        lt = l + red[(half ^ 1) * 128 + h];
-      else
-        aborted = true;
-    }
+    // Epilogue: this warp's rows of the O half, divided by the row sum.
     const int64_t rows_all = (int64_t)p.B * p.S * p.H;
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
-    float* out = p.o_out + orow * kDc + 256 * rank + 128 * half;
-    const bool have = ntiles > 0 && lt > 0.f;
+    float* out = p.o_out + orow * kDc + 256 * rank;
+    const bool have = ntiles > 0 && l > 0.f;
     if (ntiles > 0 && !aborted) {
       const int last = ntiles - 1;
       if (!warp_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u)) aborted = true;
     }
     tc_fence_after();
-    const float inv = have ? 1.f / lt : 0.f;
+    const float inv = have ? 1.f / l : 0.f;
     if (ntiles > 0 && !aborted) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tb + lane_off + kTmemO + 128u * half + 32u * c, r);
+      for (int c = 0; c < 8; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tb + lane_off + kTmemO + 32u * c, r0);
+        tmem_ld32(tb + lane_off + kTmemO + 32u * (c + 1), r1);
         tmem_ld_wait();
         if (head_ok) {
           // A row that saw no readable position (l == 0) is written as exact zeros.
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
+          for (int v = 0; v < 8; ++v) {
             reinterpret_cast<float4*>(out + 32 * c)[v] =
-                have ? make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                   __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv)
+                have ? make_float4(__uint_as_float(r0[4 * v]) * inv, __uint_as_float(r0[4 * v + 1]) * inv,
+                                   __uint_as_float(r0[4 * v + 2]) * inv, __uint_as_float(r0[4 * v + 3]) * inv)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            reinterpret_cast<float4*>(out + 32 * (c + 1))[v] =
+                have ? make_float4(__uint_as_float(r1[4 * v]) * inv, __uint_as_float(r1[4 * v + 1]) * inv,
+                                   __uint_as_float(r1[4 * v + 2]) * inv, __uint_as_float(r1[4 * v + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
       }
     } else if (head_ok) {
-      for (int v = 0; v < 32; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int v = 0; v < 64; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (head_ok && rank == 0 && half == 0)
-      p.lse_out[orow] = have ? (m_ref + log2f(lt)) * kLn2 : -INFINITY;
+    if (head_ok && rank == 0)
+      p.lse_out[orow] = have ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   }
 
   if (aborted) raise_flag(p.status, kFlagTimeout);

@@ -306,6 +306,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// tmem_ld32 into floats x[OFF .. OFF+31] of a larger array, without a staging copy.
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&r)[N]) {
+  static_assert(OFF + 32 <= N, "range");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=f"(r[OFF + 0]), "=f"(r[OFF + 1]), "=f"(r[OFF + 2]), "=f"(r[OFF + 3]), "=f"(r[OFF + 4]),
+        "=f"(r[OFF + 5]), "=f"(r[OFF + 6]), "=f"(r[OFF + 7]), "=f"(r[OFF + 8]), "=f"(r[OFF + 9]),
+        "=f"(r[OFF + 10]), "=f"(r[OFF + 11]), "=f"(r[OFF + 12]), "=f"(r[OFF + 13]), "=f"(r[OFF + 14]),
+        "=f"(r[OFF + 15]), "=f"(r[OFF + 16]), "=f"(r[OFF + 17]), "=f"(r[OFF + 18]), "=f"(r[OFF + 19]),
+        "=f"(r[OFF + 20]), "=f"(r[OFF + 21]), "=f"(r[OFF + 22]), "=f"(r[OFF + 23]), "=f"(r[OFF + 24]),
+        "=f"(r[OFF + 25]), "=f"(r[OFF + 26]), "=f"(r[OFF + 27]), "=f"(r[OFF + 28]), "=f"(r[OFF + 29]),
+        "=f"(r[OFF + 30]), "=f"(r[OFF + 31])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
