@@ -298,7 +298,8 @@ def main():
         pos = torch.arange(case.t_cap, dtype=torch.int32, device=dev).repeat(case.B)
         mla.mla_rope_inplace(kv, 576, case.B * case.t_cap, 512, pos, case.theta)
     step = mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
-                          num_splits=case.num_splits, causal=case.causal, rope_theta=case.theta)
+                          num_splits=case.num_splits, causal=case.causal, rope_theta=case.theta,
+                          total_rows=case.total_tokens)
     stream = torch.cuda.current_stream()
 
     def run_step(ev=None):

@@ -95,18 +95,25 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const ml
 
 /*
  * Workspace needed by mla_decode_latent for `num_splits` splits (0 = the automatic
- * choice for this shape, see mla_decode_num_splits).  0 when one split is used.
+ * choice for this shape, mla_decode_num_splits with total_rows = 0).  0 when one split
+ * is used.
  * Layout: fp32 partial o_lat [splits,B,S,H,512] then fp32 partial lse [splits,B,S,H].
  */
 size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen);
 
 /*
- * The split count mla_decode_latent uses when passed num_splits = 0: enough
- * (sequence, split) work units to fill the device's SMs, never more splits than
- * 64-row tiles in the longest sequence, at most MLA_MAX_SPLITS.  max_seqlen is the
- * caller's bound on seqlens[] (a host value).
+ * A split count for mla_decode_latent.  Split k of a sequence covers its rows
+ * [k*C, (k+1)*C), C = ceil(max_seqlen / num_splits) rounded up to 64 (the same C for
+ * every sequence), so short sequences leave their trailing splits empty.  The count is
+ * chosen to fill the device's SMs with (query token, split) units of two SMs each while
+ * limiting the extra traffic of split partials, never more splits than 64-row tiles in
+ * the longest sequence, at most MLA_MAX_SPLITS.  max_seqlen is the caller's bound on
+ * seqlens[] (a host value); total_rows, if > 0, is the sum of seqlens[] (a host value
+ * a serving scheduler knows), which lets a ragged batch split its long sequences more;
+ * 0 assumes every sequence is max_seqlen long.  mla_decode_latent with num_splits = 0
+ * uses this function with total_rows = 0.
  */
-int mla_decode_num_splits(int B, int S, int H, int max_seqlen);
+int mla_decode_num_splits(int B, int S, int H, int max_seqlen, int64_t total_rows);
 
 /*
  * mla_decode_latent -- attention of the absorbed queries straight over the latent
@@ -134,8 +141,9 @@ int mla_decode_num_splits(int B, int S, int H, int max_seqlen);
  *   block_table  int32 [B, max_pages] device or NULL; page_size must be 64
  *   scale        softmax scale, 1/sqrt(d_nope + d_r) = 1/sqrt(192) for DeepSeek-V3
  *                ([CALC] "RoPE 경로를 분리한 이유": not 1/sqrt(d_c + d_r))
- *   num_splits   0 = automatic; 1..MLA_MAX_SPLITS splits the cache axis of every
- *                sequence into equal ranges merged by log-sum-exp
+ *   num_splits   0 = automatic; 1..MLA_MAX_SPLITS splits the cache axis into chunks
+ *                of ceil(max_seqlen / num_splits) rows (rounded up to 64), merged by
+ *                log-sum-exp (see mla_decode_num_splits)
  *   max_seqlen   host-side bound on seqlens[] (used to plan splits; rows past it
  *                are never read)
  *   o_lat        fp32 [B,S,H,512] output;   lse fp32 [B,S,H] output

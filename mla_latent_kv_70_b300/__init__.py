@@ -31,7 +31,7 @@ SIGNATURES = {
     "mla_device_sm_count": (_I, []),
     "mla_absorb_q": (_I, [_P, _P, _P, _P, _F, _I, _I, _I, _P, _P]),
     "mla_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
-    "mla_decode_num_splits": (_I, [_I, _I, _I, _I]),
+    "mla_decode_num_splits": (_I, [_I, _I, _I, _I, _I64]),
     "mla_decode_latent": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _P, _P, _P, _SZ, _P, _P]),
     "mla_decode_latent_noalloc": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -108,8 +108,8 @@ def mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen) -> int:
     return int(lib().mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen))
 
 
-def mla_decode_num_splits(B, S, H, max_seqlen) -> int:
-    return int(lib().mla_decode_num_splits(B, S, H, max_seqlen))
+def mla_decode_num_splits(B, S, H, max_seqlen, total_rows=0) -> int:
+    return int(lib().mla_decode_num_splits(B, S, H, max_seqlen, int(total_rows)))
 
 
 def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, block_table=None,

@@ -28,22 +28,31 @@ int sm_count_cached() {
   return count;
 }
 
-// Split count for the CTA-pair decode: each (query token, split) unit occupies two SMs.
-// Pick the count that minimises (cache bytes + partial round trip) / wave efficiency.
-int auto_splits(int B, int S, int H, int max_seqlen, int sms) {
+// Split count for the CTA-pair decode: each non-empty (query token, split) unit occupies
+// two SMs.  A split is a chunk of C = ceil(max_seqlen / s) rows (rounded to 64), so the
+// run takes about waves(s) x C row-times, where waves(s) = ceil(units / pair slots) and
+// units ~ total_rows / C plus half a chunk per query token for the ragged ends; splitting
+// adds a round trip of fp32 partials (513 values per head per unit).  Pick the count with
+// the least estimated traffic-time, in bytes moved by the whole GPU.
+int auto_splits(int B, int S, int H, int max_seqlen, int64_t total_rows, int sms) {
   if (sms <= 0) sms = 148;
+  if (max_seqlen <= 0) return 1;
   const int slots = sms / 2;
-  const int units = B * S;
   const int tiles = (max_seqlen + 63) / 64;
-  const double cache = (double)units * (double)max_seqlen * 1152.0;
+  const int64_t tokens = (int64_t)B * S;
+  const double rows = total_rows > 0 ? (double)total_rows : (double)B * (double)max_seqlen;
   int best = 1;
   double best_cost = 0.0;
-  for (int s = 1; s <= MLA_MAX_SPLITS && s <= (tiles > 0 ? tiles : 1); ++s) {
-    const int n = units * s;
-    const int waves = (n + slots - 1) / slots;
-    const double eff = (double)n / ((double)slots * waves);
-    const double partial = s > 1 ? (double)n * H * (kDc + 1) * 4.0 * 2.0 : 0.0;
-    const double cost = (cache + partial) / eff;
+  for (int s = 1; s <= MLA_MAX_SPLITS && s <= tiles; ++s) {
+    int chunk = (max_seqlen + s - 1) / s;
+    chunk = (chunk + 63) & ~63;
+    double units = rows * S / chunk + 0.5 * (double)tokens;
+    units = units < (double)tokens ? (double)tokens : units;
+    const double cap = (double)tokens * s;
+    units = units > cap ? cap : units;
+    const double waves = ceil(units / slots);
+    const double cost = waves * chunk * 1152.0 * slots +
+                        (s > 1 ? units * H * (kDc + 1) * 4.0 * 2.0 : 0.0);
     if (s == 1 || cost < best_cost * 0.98) {
       best = s;
       best_cost = cost;
@@ -93,14 +102,14 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const ml
       reinterpret_cast<__nv_bfloat16*>(q_cat), static_cast<cudaStream_t>(stream)));
 }
 
-int mla_decode_num_splits(int B, int S, int H, int max_seqlen) {
+int mla_decode_num_splits(int B, int S, int H, int max_seqlen, int64_t total_rows) {
   if (B < 1 || S < 1 || max_seqlen < 0) return 1;
-  return auto_splits(B, S, H, max_seqlen, sm_count_cached());
+  return auto_splits(B, S, H, max_seqlen, total_rows, sm_count_cached());
 }
 
 size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen) {
   if (B < 1 || S < 1 || H < 1 || num_splits < 0 || num_splits > MLA_MAX_SPLITS) return 0;
-  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen);
+  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen, 0);
   if (splits <= 1) return 0;
   const size_t rows = (size_t)B * S * H;
   return (size_t)splits * rows * (kDc + 1) * sizeof(float);
@@ -125,7 +134,7 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
   } else {
     if (kv_seq_stride < max_seqlen || kv_seq_stride < 0) return MLA_ERR_INVALID;
   }
-  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen);
+  const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen, 0);
   const size_t need = mla_decode_workspace_bytes(B, S, H, splits, max_seqlen);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
     return MLA_ERR_WORKSPACE;

@@ -76,14 +76,17 @@ struct DecodeParams {
   int32_t* status;
 };
 
-// Rows [t0, t1) of sequence b that split `split` covers for query token s.
+// Rows [t0, t1) of sequence b that split `split` covers for query token s.  Splits are
+// chunks of C = ceil(max_seqlen / num_splits) rows (rounded up to the 64-row tile), the
+// same for every sequence, so a short sequence uses fewer splits than a long one and
+// its trailing splits are empty (t0 >= t1).
 __device__ __forceinline__ void split_range(const DecodeParams& p, int T, int s, int split,
                                             int& t0, int& t1) {
   int n_vis = T;
   if (p.causal) n_vis = min(T, max(0, T - p.S + s + 1));
-  int chunk = (T + p.num_splits - 1) / p.num_splits;
+  int chunk = (p.max_seqlen + p.num_splits - 1) / p.num_splits;
   chunk = (chunk + 63) & ~63;
-  t0 = split * chunk;
+  t0 = min(split * chunk, n_vis);
   t1 = min(t0 + chunk, n_vis);
 }
 

@@ -147,6 +147,24 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   split_range(p, T, s, split, t0, t1);
   const int ntiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
 
+  const int64_t rows_all = (int64_t)p.B * p.S * p.H;
+  if (ntiles == 0) {
+    // Nothing to read (an empty sequence, or a split past its end): both CTAs of the
+    // pair leave before any shared set-up.  A split's partial is marked empty by its
+    // lse alone (the merge skips it); an unsplit row is written as o_lat = 0, lse = -inf.
+    for (int h = tid; h < p.H; h += kThreads) {
+      const int64_t qrow = (int64_t)m * p.H + h;
+      if (p.num_splits > 1) {
+        if (rank == 0) p.lse_out[(int64_t)split * rows_all + qrow] = -INFINITY;
+      } else {
+        float4* out = reinterpret_cast<float4*>(p.o_out + qrow * kDc + 256 * rank);
+        for (int v = 0; v < 64; ++v) out[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rank == 0) p.lse_out[qrow] = -INFINITY;
+      }
+    }
+    return;
+  }
+
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kKvFull + i), 1);
@@ -533,7 +551,6 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     }
 
     // Epilogue: this warp's rows of the O half, divided by the row sum.
-    const int64_t rows_all = (int64_t)p.B * p.S * p.H;
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
     float* out = p.o_out + orow * kDc + 256 * rank;
     const bool have = ntiles > 0 && l > 0.f;

@@ -16,14 +16,14 @@ from . import (D_C, D_V, ROW, mla_absorb_q, mla_decode_latent, mla_decode_num_sp
 
 class DecodeStep:
     def __init__(self, B, S, H, w_uk, w_uv, *, max_seqlen, num_splits=0, causal=False,
-                 rope_theta=10000.0, scale=None, device="cuda"):
+                 rope_theta=10000.0, scale=None, total_rows=0, device="cuda"):
         self.B, self.S, self.H = B, S, H
         self.w_uk, self.w_uv = w_uk, w_uv
         self.max_seqlen = int(max_seqlen)
         self.causal = causal
         self.rope_theta = rope_theta
         self.scale = scale if scale is not None else 1.0 / math.sqrt(128 + 64)
-        self.num_splits = num_splits or mla_decode_num_splits(B, S, H, self.max_seqlen)
+        self.num_splits = num_splits or mla_decode_num_splits(B, S, H, self.max_seqlen, total_rows)
         ws = mla_decode_workspace_bytes(B, S, H, self.num_splits, self.max_seqlen)
         self.workspace = torch.empty(ws // 4, dtype=torch.float32, device=device) if ws else None
         self.q_cat = torch.empty(B, S, H, ROW, dtype=torch.bfloat16, device=device)

@@ -41,7 +41,7 @@ class DeviceCase:
         st = mla.DecodeStep(c.B, c.S, c.H, self.w_uk, self.w_uv,
                             max_seqlen=max_seqlen or max(c.seqlens),
                             num_splits=c.num_splits if num_splits is None else num_splits,
-                            causal=c.causal, rope_theta=c.theta)
+                            causal=c.causal, rope_theta=c.theta, total_rows=c.total_tokens)
         st(self.q_nope, self.q_rope, self.kv, self.seqlens, block_table=self.block_table,
            q_pos=self.q_pos)
         torch.cuda.synchronize()
