@@ -302,21 +302,22 @@ def main():
                           total_rows=case.total_tokens)
     stream = torch.cuda.current_stream()
 
-    def run_step(ev=None):
-        mla.mla_absorb_q(q_nope, q_rope, w_uk, q_pos, case.theta, step.q_cat, stream)
-        if ev:
-            ev[0].record(stream)
+    def run_step(st, marks=None):
+        """One step on stream `st`; `marks(i)` records the decode boundaries."""
+        mla.mla_absorb_q(q_nope, q_rope, w_uk, q_pos, case.theta, step.q_cat, st)
+        if marks:
+            marks(0)
         mla.mla_decode_latent(step.q_cat, kv, seqlens, step.o_lat, step.lse, scale=case.scale,
                               max_seqlen=step.max_seqlen, block_table=block_table,
                               causal=case.causal, num_splits=step.num_splits,
-                              workspace=step.workspace, status=step.status, stream=stream)
-        if ev:
-            ev[1].record(stream)
-        mla.mla_out_proj_uv(step.o_lat, w_uv, step.o, stream)
+                              workspace=step.workspace, status=step.status, stream=st)
+        if marks:
+            marks(1)
+        mla.mla_out_proj_uv(step.o_lat, w_uv, step.o, st)
 
     clocks = ClockSampler(dev)
     for _ in range(args.warmup):
-        run_step()
+        run_step(stream)
     torch.cuda.synchronize()
 
     def barrier():
@@ -324,21 +325,54 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # Timed region: K steps, CUDA events on the launching stream.
-    dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
+    # The K timed steps are captured once into a CUDA graph (the library makes no host
+    # synchronisation, so a decode step is capturable, as serving engines run it) and
+    # replayed as one launch: no host launch gaps between the kernels.  Event-record
+    # nodes around every decode give the decode kernel's duration inside the same run.
+    timing = "cuda graph of the timed steps"
+    try:
+        from cuda.bindings import runtime as cudart
+        evs = [(cudart.cudaEventCreate()[1], cudart.cudaEventCreate()[1]) for _ in range(args.steps)]
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        with torch.cuda.graph(graph, stream=cap):
+            cs = torch.cuda.current_stream()
+            for i in range(args.steps):
+                def marks(j, i=i):
+                    err = cudart.cudaEventRecordWithFlags(evs[i][j], cs.cuda_stream,
+                                                          cudart.cudaEventRecordExternal)[0]
+                    assert err == cudart.cudaError_t.cudaSuccess, err
+                run_step(cs, marks)
+        graph.replay()                      # one untimed replay
+        torch.cuda.synchronize()
+        use_graph = True
+    except Exception as e:  # noqa: BLE001
+        timing = f"eager launches (graph capture failed: {e!r})"
+        use_graph = False
+
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.start_smi()
     barrier()
     clocks.active = True
     start.record(stream)
-    for i in range(args.steps):
-        run_step(dec_events[i])
+    if use_graph:
+        graph.replay()
+    else:
+        dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(args.steps)]
+        for i in range(args.steps):
+            run_step(stream, lambda j, i=i: dec_events[i][j].record(stream))
     end.record(stream)
     barrier()
     clocks.active = False
     total_ms = start.elapsed_time(end)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_events]
+    if use_graph:
+        dec_ms = [cudart.cudaEventElapsedTime(a, b)[1] for a, b in evs]
+        for a, b in evs:
+            cudart.cudaEventDestroy(a)
+            cudart.cudaEventDestroy(b)
+    else:
+        dec_ms = [a.elapsed_time(b) for a, b in dec_events]
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -413,6 +447,7 @@ def main():
                        "causal": case.causal, "rope": case.rope,
                        "l2": f"inputs larger than L2: {cache_b / 1e6:.0f} MB cache read per step"
                              if cache_b > 126e6 else "inputs fit in L2 (no flush)",
+                       "timing": timing,
                        "parallelism": f"dp{world} (independent replicas, no collective)"},
             "clocks": clock_info,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

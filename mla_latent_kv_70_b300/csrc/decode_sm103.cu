@@ -148,7 +148,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   const int ntiles = t1 > t0 ? (t1 - t0 + kN - 1) / kN : 0;
 
   const int64_t rows_all = (int64_t)p.B * p.S * p.H;
+  grid_dep_launch();
   if (ntiles == 0) {
+    grid_dep_wait();   // the outputs below may still be read by the previous kernel
     // Nothing to read (an empty sequence, or a split past its end): both CTAs of the
     // pair leave before any shared set-up.  A split's partial is marked empty by its
     // lse alone (the merge skips it); an unsplit row is written as o_lat = 0, lse = -inf.
@@ -197,6 +199,10 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   const uint32_t tb = *tmem_slot;
 
   bool aborted = false;
+  // Programmatic dependent launch: the TMA warp requests the first cache tiles (which no
+  // earlier kernel writes) before waiting for the previous kernel; every other thread
+  // waits here, before reading q_cat or writing outputs.
+  if (warp != 0) grid_dep_wait();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -204,8 +210,6 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       prefetch_tmap(&maps.kv_lat);
       prefetch_tmap(&maps.kv_rope);
       prefetch_tmap(&maps.q_rope);
-      mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
-      tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
       // Row coordinate of tile i in the tensor maps (a page past the pool for a bad
       // block-table entry: the copy then fills zeros and the tile is masked).
       auto tile_row = [&](int i, bool flag) -> int {
@@ -235,6 +239,12 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           tma_load_2d(stage + j * kBoxBytes, &maps.kv_lat, bar(kKvFull + st), 256 * (int)rank + 64 * j, y);
         tma_load_2d(stage + 4 * kBoxBytes, &maps.kv_rope, bar(kKvFull + st), kDc + 32 * (int)rank, y);
         ++issued;
+        if (i == min(kStages, ntiles) - 1) {
+          // The ring is full: now wait for the previous kernel, then fetch q^R from q_cat.
+          grid_dep_wait();
+          mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
+          tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+        }
       }
       // No copy may still be landing when the CTA exits.
       for (int i = max(0, issued - kStages); i < issued; ++i)
@@ -624,8 +634,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
     attr_done = true;
   }
   const int units = p.B * p.S * p.num_splits;
-  k_decode_sm103<<<2 * units, kThreads, kSmemBytes, st>>>(maps, p);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_decode_sm103, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

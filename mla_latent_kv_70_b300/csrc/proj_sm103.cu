@@ -55,14 +55,15 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t s0 = smem_addr(smem);
-  const uint32_t bar_full = s0 + kAbsOffBar, bar_mma = bar_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAbsOffBar + 16);
+  const uint32_t bar_full = s0 + kAbsOffBar, bar_mma = bar_full + 16;   // bar_full: [2] K halves
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kAbsOffBar + 24);
 
   const int nh = blockIdx.x, h = blockIdx.y, m0 = blockIdx.z * kTileM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     mbar_init(bar_full, 1);
+    mbar_init(bar_full + 8, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
@@ -75,27 +76,39 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
   tc_fence_after();
   const uint32_t tb = *tmem_slot;
 
+  // The weights do not depend on the previous kernel: they are requested before waiting
+  // for it (programmatic dependent launch); q_cat, which it reads, is written after.
+  grid_dep_launch();
   if (tid == 0) {
     prefetch_tmap(&maps.q);
     prefetch_tmap(&maps.w);
-    mbar_arrive_expect_tx(bar_full, 2 * kAbsABox + 2 * kAbsBBox);
+    // Two K halves (64 wide each) on their own barriers: the first half's MMAs run
+    // while the second half lands.
     for (int j = 0; j < 2; ++j) {
-      tma_load_2d(s0 + j * kAbsABox, &maps.q, bar_full, h * kDn + 64 * j, m0);
-      tma_load_2d(s0 + kAbsOffB + j * kAbsBBox, &maps.w, bar_full, 64 * j, h * kDc + 256 * nh);
+      mbar_arrive_expect_tx(bar_full + 8u * j, kAbsABox + kAbsBBox);
+      tma_load_2d(s0 + kAbsOffB + j * kAbsBBox, &maps.w, bar_full + 8u * j, 64 * j, h * kDc + 256 * nh);
     }
-    // On expiry no MMA is issued; the copies are waited for once more before exit.
-    if (mbar_wait(bar_full, 0, kWaitNs)) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(kTileM, 256, false, false);
-#pragma unroll
-      for (int k = 0; k < kDn / 16; ++k) {
-        const uint32_t off = (uint32_t)(k & 3) * 32u;   // K = 16 bf16 = 32 B inside a swizzle row
-        mma_ss(tb, smem_desc(s0 + (uint32_t)(k >> 2) * kAbsABox + off, 16, 1024, kSwizzle128B),
-               smem_desc(s0 + kAbsOffB + (uint32_t)(k >> 2) * kAbsBBox + off, 16, 1024, kSwizzle128B),
-               idesc, k > 0 ? 1u : 0u);
+  }
+  grid_dep_wait();
+  if (tid == 0) {
+    for (int j = 0; j < 2; ++j)
+      tma_load_2d(s0 + j * kAbsABox, &maps.q, bar_full + 8u * j, h * kDn + 64 * j, m0);
+    // On expiry no further MMA is issued; the copies are waited for once more before exit.
+    const uint32_t idesc = idesc_bf16(kTileM, 256, false, false);
+    bool issued = true;
+    for (int j = 0; j < 2 && issued; ++j) {
+      if (!mbar_wait(bar_full + 8u * j, 0, kWaitNs)) {
+        issued = false;
+        break;
       }
-      mma_commit(bar_mma);
+      tc_fence_after();
+      const uint64_t ad = smem_desc(s0 + (uint32_t)j * kAbsABox, 16, 1024, kSwizzle128B);
+      const uint64_t bd = smem_desc(s0 + kAbsOffB + (uint32_t)j * kAbsBBox, 16, 1024, kSwizzle128B);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)   // K = 16 bf16 = 32 B steps inside a swizzle row
+        mma_ss(tb, ad + 2u * k, bd + 2u * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
     }
+    if (issued) mma_commit(bar_mma);
   }
   __syncwarp();
   const bool ok = !__any_sync(0xffffffffu, !mbar_wait(bar_mma, 0, kWaitNs));
@@ -106,20 +119,23 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
   const int m = m0 + r;
   __nv_bfloat16* out = q_cat + ((size_t)m * H + h) * kRow + 256 * nh;
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    uint32_t v[32];
-    if (ok) {
-      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * c, v);
+  for (int c = 0; c < 8; c += 2) {
+    uint32_t v0[32], v1[32];
+    if (ok) {   // two loads in flight per wait (~290 cycles each)
+      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * c, v0);
+      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * (c + 1), v1);
       tmem_ld_wait();
     }
     if (m < M) {
-      uint32_t pk[16];
+      uint32_t pk[32];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        pk[j] = ok ? f2_to_bf2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0x7FC07FC0u;
+      for (int j = 0; j < 16; ++j) {
+        pk[j] = ok ? f2_to_bf2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])) : 0x7FC07FC0u;
+        pk[16 + j] = ok ? f2_to_bf2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])) : 0x7FC07FC0u;
+      }
       uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      for (int j = 0; j < 8; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     }
   }
 
@@ -140,7 +156,10 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
     }
   }
 
-  if (!ok && tid == 0) mbar_wait(bar_full, 0, kWaitNs);   // no copy may land after exit
+  if (!ok && tid == 0) {   // no copy may land after exit
+    mbar_wait(bar_full, 0, kWaitNs);
+    mbar_wait(bar_full + 8, 0, kWaitNs);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -152,43 +171,50 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
 // ---------------------------------------------------------------------------
 // Value up-projection.  CTA (h, m_blk):
 //   D[128 rows x 128] = bf16(o_lat[rows, h, 0:512]) . W_UV[h] (512 x 128, N contiguous)
-// W_UV[h] arrives by TMA in 8 chunks of 64 K-rows (two 64-wide N boxes each, read
-// MN-major by the MMA).  o_lat is fp32, so the CTA's threads load it, round it to bf16
-// and write it in the 128B-swizzled K-major layout, double-buffered by 64-wide K chunks,
-// one chunk of global loads ahead of the shared-memory stores.
+// All of W_UV[h] (8 chunks of 64 K-rows, two 64-wide N boxes each, read MN-major by the
+// MMA) and the fp32 o_lat rows (64-wide K chunks, a 2-deep ring) arrive by TMA.  The
+// CTA's threads round each fp32 chunk to bf16 into the 128B-swizzled K-major layout of
+// the A operand (double-buffered) while the next chunk lands; one thread issues the
+// MMAs.
 // ---------------------------------------------------------------------------
 constexpr int kOutThreads = 128;
 constexpr int kOutChunks = kDc / 64;                   // 8 K chunks of 64
 constexpr uint32_t kOutBBox = 64 * 128;                // 64 K-rows x 64 bf16
 constexpr uint32_t kOutBChunk = 2 * kOutBBox;          // N = 128
 constexpr uint32_t kOutAChunk = kTileM * 128;          // 128 rows x 64 bf16
+constexpr uint32_t kOutA32Chunk = kTileM * 64 * 4;     // 128 rows x 64 fp32
 constexpr uint32_t kOutOffA = kOutChunks * kOutBChunk;
-constexpr uint32_t kOutOffBar = kOutOffA + 2 * kOutAChunk;
+constexpr uint32_t kOutOffA32 = kOutOffA + 2 * kOutAChunk;
+constexpr uint32_t kOutOffBar = kOutOffA32 + 2 * kOutA32Chunk;
 constexpr uint32_t kOutSmem = kOutOffBar + 128 + 1024;
+static_assert(kOutSmem <= 232448, "shared memory per CTA");
 
 struct OutMaps {
-  CUtensorMap w;   // W_UV viewed as [H*512 rows, 128], box 64 x 64 rows, 128B swizzle
+  CUtensorMap w;     // W_UV viewed as [H*512 rows, 128], box 64 x 64 rows, 128B swizzle
+  CUtensorMap lat;   // o_lat viewed as [M rows, H*512] fp32, box 64 x 128 rows, no swizzle
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
-k_out_proj_uv(const __grid_constant__ OutMaps maps, const float* __restrict__ o_lat, int M, int H,
-              float* __restrict__ o) {
+k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restrict__ o) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t s0 = smem_addr(smem);
   const uint32_t bars = s0 + kOutOffBar;
   auto bar_b = [&](int c) { return bars + 8u * (uint32_t)c; };          // [8] W chunk landed
-  auto bar_a = [&](int i) { return bars + 64u + 8u * (uint32_t)i; };    // [2] A buffer consumed
-  const uint32_t bar_done = bars + 80u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOutOffBar + 96);
+  auto bar_a = [&](int i) { return bars + 64u + 8u * (uint32_t)i; };    // [2] bf16 A buffer consumed
+  auto bar_l = [&](int i) { return bars + 80u + 8u * (uint32_t)i; };    // [2] fp32 chunk landed
+  const uint32_t bar_done = bars + 96u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOutOffBar + 112);
 
   const int h = blockIdx.x, m0 = blockIdx.y * kTileM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int c = 0; c < kOutChunks; ++c) mbar_init(bar_b(c), 1);
-    mbar_init(bar_a(0), 1);
-    mbar_init(bar_a(1), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_a(i), 1);
+      mbar_init(bar_l(i), 1);
+    }
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
@@ -201,54 +227,62 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, const float* __restrict__ o_
   tc_fence_after();
   const uint32_t tb = *tmem_slot;
 
+  auto load_lat = [&](int c) {   // fp32 chunk c of the o_lat rows into ring slot c & 1
+    mbar_arrive_expect_tx(bar_l(c & 1), kOutA32Chunk);
+    tma_load_2d(s0 + kOutOffA32 + (uint32_t)(c & 1) * kOutA32Chunk, &maps.lat, bar_l(c & 1),
+                h * kDc + 64 * c, m0);
+  };
+  // W_UV does not depend on the previous kernel: it is requested before waiting for it
+  // (programmatic dependent launch); o_lat, which that kernel writes, after.
+  grid_dep_launch();
   if (tid == 0) {
     prefetch_tmap(&maps.w);
+    prefetch_tmap(&maps.lat);
     for (int c = 0; c < kOutChunks; ++c) {
       mbar_arrive_expect_tx(bar_b(c), kOutBChunk);
       for (int j = 0; j < 2; ++j)
         tma_load_2d(s0 + c * kOutBChunk + j * kOutBBox, &maps.w, bar_b(c), 64 * j, h * kDc + 64 * c);
     }
   }
+  grid_dep_wait();
+  if (tid == 0) {
+    load_lat(0);
+    load_lat(1);
+  }
 
-  // Thread (warp, lane) covers rows 2*(4*it + warp) + (lane >> 4), it = 0..15, and the
-  // four K values 4*(lane & 15) .. +3 of the current chunk.
+  // Thread (warp, lane) converts rows 2*(4*it + warp) + (lane >> 4), it = 0..15, and the
+  // four K values 4*(lane & 15) .. +3 of the current chunk (a half-warp reads one 256-byte
+  // fp32 row: no bank conflicts).
   const int sub = lane >> 4, kq = lane & 15;
-  float4 ld[16];
-  auto load_chunk = [&](int c) {
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int r = 2 * (4 * it + warp) + sub;
-      const int m = m0 + r;
-      ld[it] = m < M ? *reinterpret_cast<const float4*>(o_lat + ((size_t)m * H + h) * kDc + 64 * c + 4 * kq)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  load_chunk(0);
   bool ok = true;
   for (int c = 0; c < kOutChunks; ++c) {
     const int buf = c & 1;
+    if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(bar_l(buf), (uint32_t)(c >> 1) & 1u, kWaitNs));
     if (c >= 2 && ok) ok = !__any_sync(0xffffffffu, !mbar_wait(bar_a(buf), (uint32_t)((c - 2) >> 1) & 1u, kWaitNs));
+    const uint32_t a32 = s0 + kOutOffA32 + (uint32_t)buf * kOutA32Chunk;
     const uint32_t abase = s0 + kOutOffA + (uint32_t)buf * kOutAChunk;
-#pragma unroll
-    for (int it = 0; it < 16; ++it) {
-      const int r = 2 * (4 * it + warp) + sub;
-      // 128B swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7).
-      const uint32_t addr = abase + (uint32_t)r * 128u + (uint32_t)((((kq >> 1) ^ (r & 7)) << 4) | ((kq & 1) << 3));
-      const uint32_t lo = f2_to_bf2(ld[it].x, ld[it].y), hi = f2_to_bf2(ld[it].z, ld[it].w);
-      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
+    if (ok) {
+#pragma unroll 4
+      for (int it = 0; it < 16; ++it) {
+        const int r = 2 * (4 * it + warp) + sub;
+        const float4 v = ld_shared_v4(a32 + (uint32_t)r * 256u + (uint32_t)kq * 16u);
+        // 128B swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7).
+        const uint32_t addr = abase + (uint32_t)r * 128u + (uint32_t)((((kq >> 1) ^ (r & 7)) << 4) | ((kq & 1) << 3));
+        const uint32_t lo = f2_to_bf2(v.x, v.y), hi = f2_to_bf2(v.z, v.w);
+        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(lo), "r"(hi) : "memory");
+      }
     }
-    if (c + 1 < kOutChunks) load_chunk(c + 1);
     fence_proxy_async_smem();
     ok = __syncthreads_and(ok);   // also tells every thread of an earlier failed wait
-    if (tid == 0) {
-      if (ok && mbar_wait(bar_b(c), 0, kWaitNs)) {
+    if (tid == 0 && ok) {
+      if (c + 2 < kOutChunks) load_lat(c + 2);   // fp32 slot `buf` has been converted
+      if (mbar_wait(bar_b(c), 0, kWaitNs)) {
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(kTileM, kDv, false, true);
+        const uint64_t ad = smem_desc(abase, 16, 1024, kSwizzle128B);
+        const uint64_t bd = smem_desc(s0 + c * kOutBChunk, kOutBBox, 1024, kSwizzle128B);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_ss(tb, smem_desc(abase + 32u * k, 16, 1024, kSwizzle128B),
-                 smem_desc(s0 + c * kOutBChunk + 2048u * k, kOutBBox, 1024, kSwizzle128B), idesc,
-                 (c > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 4; ++k) mma_ss(tb, ad + 2u * k, bd + 128u * k, idesc, (c > 0 || k > 0) ? 1u : 0u);
         mma_commit(bar_a(buf));
       } else {
         ok = false;
@@ -266,24 +300,32 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, const float* __restrict__ o_
   const int m = m0 + r;
   float* out = o + ((size_t)m * H + h) * kDv;
 #pragma unroll 1
-  for (int c = 0; c < kDv / 32; ++c) {
-    uint32_t v[32];
+  for (int c = 0; c < kDv / 32; c += 2) {
+    uint32_t v0[32], v1[32];
     if (ok) {
-      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * c, v);
+      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * c, v0);
+      tmem_ld32(tb + ((uint32_t)(32 * warp) << 16) + 32u * (c + 1), v1);
       tmem_ld_wait();
     }
     if (m < M) {
-      float4* dst = reinterpret_cast<float4*>(out + 32 * c);
+      float4* d0 = reinterpret_cast<float4*>(out + 32 * c);
+      float4* d1 = reinterpret_cast<float4*>(out + 32 * (c + 1));
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        dst[j] = ok ? make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]))
-                    : make_float4(NAN, NAN, NAN, NAN);
+      for (int j = 0; j < 8; ++j) {
+        d0[j] = ok ? make_float4(__uint_as_float(v0[4 * j]), __uint_as_float(v0[4 * j + 1]),
+                                 __uint_as_float(v0[4 * j + 2]), __uint_as_float(v0[4 * j + 3]))
+                   : make_float4(NAN, NAN, NAN, NAN);
+        d1[j] = ok ? make_float4(__uint_as_float(v1[4 * j]), __uint_as_float(v1[4 * j + 1]),
+                                 __uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3]))
+                   : make_float4(NAN, NAN, NAN, NAN);
+      }
     }
   }
 
-  if (!ok && tid == 0)   // no copy may land after exit
+  if (tid == 0) {   // no copy may land after exit
     for (int c = 0; c < kOutChunks; ++c) mbar_wait(bar_b(c), 0, kWaitNs);
+    for (int c = kOutChunks - 2; c < kOutChunks; ++c) mbar_wait(bar_l(c & 1), (uint32_t)(c >> 1) & 1u, kWaitNs);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -315,22 +357,24 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_
   cudaError_t e = set_smem(k_absorb_q, kAbsSmem, attr);
   if (e != cudaSuccess) return e;
   dim3 grid(2, H, (M + kTileM - 1) / kTileM);
-  k_absorb_q<<<grid, kAbsThreads, kAbsSmem, st>>>(maps, q_rope, q_pos, f, M, H, q_cat);
-  return cudaGetLastError();
+  e = launch_pdl(k_absorb_q, grid, dim3(kAbsThreads), kAbsSmem, st, maps, q_rope, q_pos, f, M, H, q_cat);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_out_proj_uv(const float* o_lat, const __nv_bfloat16* w_uv, int M, int H,
                                float* o, cudaStream_t st) {
   OutMaps maps;
   if (!encode_tma_2d(&maps.w, true, w_uv, kDv, (uint64_t)H * kDc, (uint64_t)kDv * 2, 64, 64,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tma_2d(&maps.lat, false, o_lat, (uint64_t)H * kDc, (uint64_t)M, (uint64_t)H * kDc * 4, 64,
+                     kTileM, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   static bool attr = false;
   cudaError_t e = set_smem(k_out_proj_uv, kOutSmem, attr);
   if (e != cudaSuccess) return e;
   dim3 grid(H, (M + kTileM - 1) / kTileM);
-  k_out_proj_uv<<<grid, kOutThreads, kOutSmem, st>>>(maps, o_lat, M, H, o);
-  return cudaGetLastError();
+  e = launch_pdl(k_out_proj_uv, grid, dim3(kOutThreads), kOutSmem, st, maps, M, H, o);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla

@@ -2,6 +2,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "ptx_sm103.cuh"
 
 namespace mla {
 
@@ -14,6 +15,8 @@ RopeFreqs make_rope_freqs(float theta) {
 }
 
 namespace {
+
+using namespace ptx;
 
 __global__ void k_rope_inplace(__nv_bfloat16* __restrict__ x, int64_t row_stride, int64_t rows,
                                int col_offset, const int32_t* __restrict__ pos, RopeFreqs f) {
@@ -32,6 +35,8 @@ __global__ void k_rope_inplace(__nv_bfloat16* __restrict__ x, int64_t row_stride
 __global__ void __launch_bounds__(128)
 k_combine(const float* __restrict__ o_part, const float* __restrict__ lse_part, int splits,
           int64_t rows, float* __restrict__ o, float* __restrict__ lse) {
+  grid_dep_launch();
+  grid_dep_wait();   // the partials come from the previous kernel
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x;
   __shared__ float w_s[MLA_MAX_SPLITS];
@@ -83,8 +88,9 @@ cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t ro
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
                            float* o, float* lse, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  k_combine<<<(unsigned)rows, 128, 0, st>>>(o_part, lse_part, splits, rows, o, lse);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_combine, dim3((unsigned)rows), dim3(128), 0, st, o_part, lse_part,
+                             splits, rows, o, lse);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mla
