@@ -87,6 +87,9 @@ constexpr float kRescaleThreshold = 8.0f;     // log2 units
 enum Bar {
   kKvFull = 0,                   // [kStages] TMA -> MMA
   kKvEmpty = kStages,            // [kStages] MMA -> TMA
+  // A parity wait must never skip a phase, or it can return on the stale completion of
+  // the phase before.  So barriers that the two exchange groups (even / odd tiles) signal
+  // or wait for are kept per tile parity: each waiter then sees every phase of its own.
   kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
   kSFree = 2 * kStages + 2,      // [2] exchange -> QK issuer: S buffer read (4 warps)
   kPFull = 2 * kStages + 4,      // [2] softmax -> PV issuer: P(i) in shared memory (256 threads)
@@ -96,10 +99,10 @@ enum Bar {
   kQReady = 2 * kStages + 11,
   kDrain = 2 * kStages + 12,
   kSReady = 2 * kStages + 17,    // exchange -> softmax: a tile's scores in smem (128 threads)
-  kScoreFree = 2 * kStages + 18, // softmax -> exchange: the score buffer has been read (8 warps)
-  kDrainPv = 2 * kStages + 19,
-  kRecvRead = 2 * kStages + 20,  // exchange -> exchange: a tile's peer partial read (4 warps)
-  kNumBars = 2 * kStages + 21
+  kScoreFree = 2 * kStages + 18, // [2] softmax -> exchange: a tile's scores read (4 warps)
+  kDrainPv = 2 * kStages + 20,
+  kRecvRead = 2 * kStages + 21,  // [2] exchange -> exchange: a tile's peer partial read (4 warps)
+  kNumBars = 2 * kStages + 23
 };
 static_assert(kNumBars * 8 <= 256, "barrier area");
 
@@ -175,6 +178,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kSFull + i), 1);
       mbar_init(bar(kSFree + i), kExchWarps / 2);
+      mbar_init(bar(kScoreFree + i), kSoftmaxWarps);
+      mbar_init(bar(kRecvRead + i), kExchWarps / 2);
       mbar_init(bar(kPFull + i), 32 * kSoftmaxWarps);
       mbar_init(bar(kPvDone + i), 1);
       mbar_init(bar(kRecvFull + i), 1);
@@ -182,8 +187,6 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQReady), 32 * kExchWarps);
     mbar_init(bar(kSReady), 32 * kExchWarps / 2);
-    mbar_init(bar(kRecvRead), kExchWarps / 2);
-    mbar_init(bar(kScoreFree), kSoftmaxWarps);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
     fence_mbar_init();
@@ -373,7 +376,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       // i goes out only after the warps of tile i-1 here have read its peer partial
       // (kRecvRead), and the peer follows the same rule, so it sends tile i+2 only after
       // it has received tile i+1 from us, i.e. after we have read tile i.
-      if (i >= 1 && !warp_wait(bar(kRecvRead), (uint32_t)(i - 1) & 1u)) {
+      if (i >= 1 && !warp_wait(bar(kRecvRead + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
         aborted = true;
         break;
       }
@@ -406,7 +409,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kRecvRead));
+      if (lane == 0) mbar_arrive(bar(kRecvRead + buf));
       // Readable rows of this tile, the row maximum over them (log2 units), and the
       // scores relative to it.  The softmax takes exp2 of these, so they are stored as
       // fp16: its error near 0, where the weights are largest, is under 2^-11 of the
@@ -434,7 +437,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         mx = t16[0] * p.scale_log2;
       }
       const float negmx = (mx == -INFINITY) ? 0.f : -mx;
-      if (i >= 1 && !warp_wait(bar(kScoreFree), (uint32_t)(i - 1) & 1u)) {
+      if (i >= 1 && !warp_wait(bar(kScoreFree + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
         aborted = true;
         break;
       }
@@ -496,7 +499,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kScoreFree));
+      if (lane == 0) mbar_arrive(bar(kScoreFree + buf));
       // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
       const bool grow = mx > m_ref + kRescaleThreshold;
       const float m_new = grow ? mx : m_ref;
