@@ -230,3 +230,50 @@ def test_mtp_causal_full_size():
     dc = DeviceCase(case)
     st = dc.step()
     check_case(dc, st, [0, 64, 127], expanded_heads=[3])
+
+
+# ----------------------------------------------------------------------------
+# Ordering between the kernels of consecutive steps, and split planning
+# ----------------------------------------------------------------------------
+
+def test_back_to_back_steps_see_their_own_inputs():
+    # Each kernel of a step may start before the previous kernel ends (programmatic
+    # dependent launch) and waits for it only before touching shared buffers.  Two steps
+    # issued without a host synchronisation, on the same buffers, with different queries,
+    # must each match the oracle; the first step's outputs are copied out between them
+    # on the stream.
+    case = I.make_case("b2b", 4, 1, 128, [700, 64, 1900, 5], seed=31)
+    dc = DeviceCase(case)
+    import mla_latent_kv_70_b300 as mla
+    st = mla.DecodeStep(case.B, case.S, case.H, dc.w_uk, dc.w_uv, max_seqlen=max(case.seqlens),
+                        num_splits=3)
+    case2 = I.make_case("b2b", 4, 1, 128, [700, 64, 1900, 5], seed=32)
+    qn2, qr2 = (t.cuda() for t in I.queries(case2))
+    st(dc.q_nope, dc.q_rope, dc.kv, dc.seqlens)
+    o1, lse1 = st.o.clone(), st.lse.clone()
+    st(qn2, qr2, dc.kv, dc.seqlens)
+    torch.cuda.synchronize()
+    w_uk, w_uv = (w.double().numpy() for w in I.weights(case))
+    for b in range(case.B):
+        _, r_lse, r_o = oracle_seq(case, b, w_uk, w_uv)
+        assert row_rel_err(o1[b].cpu().numpy(), r_o) <= ROW_REL_TOL
+        assert lse_err(lse1[b].cpu().numpy(), r_lse) <= np.maximum(
+            LSE_ABS_TOL, lse_rounding_bound(case, b, w_uk)).max()
+        # the second step: same cache, the queries of seed 32
+        T = case.seqlens[b]
+        rows = I.seq_rows(case, b)[:T].double().numpy()
+        q_lat = O.absorb_q(I.seq_queries(case2, b)[0].double().numpy(), w_uk)
+        o_lat, lse = O.decode_absorbed_seq(q_lat, I.seq_queries(case2, b)[1].double().numpy(),
+                                           rows[:, :512], rows[:, 512:], case.scale)
+        assert row_rel_err(st.o[b].cpu().numpy(), O.out_proj_uv(o_lat, w_uv)) <= ROW_REL_TOL
+
+
+@pytest.mark.parametrize("splits", [5, 128])
+def test_mostly_empty_splits(splits):
+    # Splits are chunks of ceil(max_seqlen / splits) rows for every sequence: with a short
+    # and a long sequence most of the short one's splits are empty and exit at once.
+    lens = [3, 4000]
+    case = I.make_case("empty_splits", 2, 1, 128, lens, seed=33)
+    dc = DeviceCase(case)
+    st = dc.step(num_splits=splits)
+    check_case(dc, st, range(case.B), derived_lse_tol=True)
