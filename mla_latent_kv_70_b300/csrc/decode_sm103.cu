@@ -18,25 +18,30 @@
 //   * each CTA computes the partial score over its 288 columns into TMEM (A operand =
 //     its half of q~, held in TMEM; the rope half of q from shared memory);
 //   * the partials are swapped through distributed shared memory as bf16, by 16-byte
-//     st.async into the peer's receive buffer, counted (complete_tx) on its mbarrier.
-//     No "buffer free" signal travels back: under HBM load a remote release-arrive took
-//     ~3900 cycles to land, and the data flow already orders each reuse (a CTA sends
-//     tile i+1 only after reading tile i).  bf16 halves the bytes of fp32 partials and
-//     adds an error of the same order as storing q~ in bf16 (2^-8 of the partial sum).
-//     Each CTA adds its own fp32 partial to the peer's bf16 partial and normalises its
-//     half of O with its own softmax sums, so the two halves need not agree bit for bit;
-//   * P (bf16) goes to shared memory
-//     in the 128B-swizzled K-major layout, and each CTA accumulates its 256 columns of
-//     O in TMEM from P and its own V columns (the same shared-memory tile, read MN-major).
-// Warp roles per CTA: warp 0 issues TMA, warp 1 issues the score MMAs (QK) and warp 14
-// the aggregation MMAs (PV), so that neither waits behind the other; warps 2-5 (one per
-// TMEM lane quarter of 32 heads) read the partial scores out of TMEM (freeing the S
-// buffer for the next QK at once), swap them with the peer, and leave the full scores
-// relative to each row's tile maximum in shared memory (fp16), two warps per quarter
-// taking alternate tiles; warps 10-13 (one per quarter) run the online softmax and the
-// epilogue.  Exchange and softmax of different tiles overlap.
+//     st.async into the peer's receive buffer (two, by tile parity), counted (complete_tx)
+//     on its mbarrier.  A buffer is reused for tile i+2 once the peer has read tile i out
+//     of it; the peer says so with a 4-byte st.async counted on our "free" barrier (about
+//     500 cycles under HBM load, where a remote mbarrier.arrive.release took ~3900).
+//     bf16 halves the bytes of fp32 partials and adds an error of the same order as
+//     storing q~ in bf16 (2^-8 of the partial sum).  Each CTA adds its own fp32 partial to
+//     the peer's bf16 partial and normalises its half of O with its own softmax sums, so
+//     the two halves need not agree bit for bit;
+//   * P (bf16) goes to shared memory in the 128B-swizzled K-major layout, and each CTA
+//     accumulates its 256 columns of O in TMEM from P and its own V columns.
+// Shared memory holds the score operands in a short ring (3 latent tiles, 2 rope tiles),
+// released as soon as a tile's score MMAs are done.  The aggregation reads the same latent
+// columns a second time, a few tiles later, into a ring of its own (2 tiles): that read is
+// served by L2, and the score ring no longer stays occupied through exchange, softmax
+// and aggregation (HBM bytes in flight, not tile compute, set the pace of a decode).
+// Warp roles per CTA: warp 0 issues the score-ring TMA, warp 1 the score MMAs (QK), warp
+// 14 the V re-reads and the aggregation MMAs (PV); warps 2-13 form three groups of four
+// (one warp per TMEM lane quarter of 32 heads), group g taking the tiles i with i % 3 == g
+// from partial scores to P: read the partial out of TMEM (freeing the S buffer at once),
+// swap it with the peer, add, row maximum, reference maximum (handed from the group of the
+// previous tile), exp2, P into shared memory.
 // Softmax runs in the log2 domain with a lazily raised reference maximum (the running
-// output is rescaled only when the maximum grows by more than 2^8).
+// output is rescaled only when the maximum grows by more than 2^8); each group keeps its
+// own share of the row sum, merged in the epilogue.
 // Every mbarrier wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -51,30 +56,37 @@ namespace {
 using namespace ptx;
 
 constexpr int kN = 64;                            // cache rows per tile
-constexpr int kStages = 4;
-constexpr int kExchWarps = 8;                     // two per TMEM lane quarter (even / odd tiles)
-constexpr int kSoftmaxWarps = 4;                  // one per TMEM lane quarter
-constexpr int kPvWarp = 2 + kExchWarps + kSoftmaxWarps;   // the warp that issues PV
+constexpr int kQkStages = 3;                      // latent tiles in flight for the score MMAs
+constexpr int kRopeStages = 2;                    // rope tiles (their two MMAs close each chain)
+constexpr int kVStages = 2;                       // latent tiles re-read for the aggregation MMAs
+constexpr int kGroups = 3;                        // score-to-P groups: tile i goes to group i % 3
+constexpr int kGroupWarps = 4;                    // one warp per TMEM lane quarter
+constexpr int kPvWarp = 2 + kGroups * kGroupWarps;   // the warp that issues PV
 constexpr int kThreads = 32 * (kPvWarp + 1);
+constexpr int kGroupThreads = 32 * kGroupWarps;
 constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swizzle)
+constexpr uint32_t kLatBytes = 4 * kBoxBytes;     // 64 rows x this CTA's 256 latent columns
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
-constexpr uint32_t kStageBytes = 4 * kBoxBytes + kRopeBoxBytes;
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
 constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
 constexpr uint32_t kQuarterXBytes = 32 * kN * 2;  // one lane quarter's share: 32 rows x 64 columns
 constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
-constexpr uint32_t kScoreBytes = 128 * kN * 2;    // full scores handed to the softmax, fp16
 
-constexpr uint32_t kOffQRope = kStages * kStageBytes;
+constexpr uint32_t kOffQk = 0;
+constexpr uint32_t kOffRope = kOffQk + kQkStages * kLatBytes;
+constexpr uint32_t kOffV = kOffRope + kRopeStages * kRopeBoxBytes;
+constexpr uint32_t kOffQRope = kOffV + kVStages * kLatBytes;
 constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
-constexpr uint32_t kOffScore = kOffP + kPBytes;
-constexpr uint32_t kOffTmax = kOffScore + kScoreBytes;   // [128] tile maxima, log2 units
-constexpr uint32_t kOffBars = kOffTmax + 128 * 4;
-constexpr uint32_t kOffSlot = kOffBars + 256;
-constexpr uint32_t kSmemBytes = kOffSlot + 16 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kOffMref = kOffP + kPBytes;    // [128] reference maximum per head, log2 units
+constexpr uint32_t kOffBars = kOffMref + 128 * 4;
+constexpr uint32_t kOffSlot = kOffBars + 384;
+constexpr uint32_t kOffSig = kOffSlot + 16;       // [4] landing words of the peer's "buffer free" signals
+constexpr uint32_t kSmemBytes = kOffSig + 16 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kOffP % 1024 == 0, "P tiles need 1024-byte alignment (128B swizzle atoms)");
+static_assert(kOffV % 1024 == 0 && kOffP % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
+static_assert(kOffRope % 512 == 0 && kOffQRope % 512 == 0, "64B-swizzled tiles need 512-byte alignment");
+static_assert(kGroups * kGroupThreads * 4 <= 2 * kRecvBytes, "row sums reuse the receive buffers");
 
 // TMEM columns.
 constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
@@ -85,26 +97,29 @@ constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 enum Bar {
-  kKvFull = 0,                   // [kStages] TMA -> MMA
-  kKvEmpty = kStages,            // [kStages] MMA -> TMA
-  // A parity wait must never skip a phase, or it can return on the stale completion of
-  // the phase before.  So barriers that the two exchange groups (even / odd tiles) signal
-  // or wait for are kept per tile parity: each waiter then sees every phase of its own.
-  kSFull = 2 * kStages,          // [2] MMA -> softmax: partial scores in TMEM
-  kSFree = 2 * kStages + 2,      // [2] exchange -> QK issuer: S buffer read (4 warps)
-  kPFull = 2 * kStages + 4,      // [2] softmax -> PV issuer: P(i) in shared memory (256 threads)
-  kPvDone = 2 * kStages + 6,     // [2] PV issuer -> softmax: PV(i) finished (P buffer, O stable)
-  kRecvFull = 2 * kStages + 8,   // [2] peer partial landed (expect_tx by one thread here)
-  kQFull = 2 * kStages + 10,
-  kQReady = 2 * kStages + 11,
-  kDrain = 2 * kStages + 12,
-  kSReady = 2 * kStages + 17,    // exchange -> softmax: a tile's scores in smem (128 threads)
-  kScoreFree = 2 * kStages + 18, // [2] softmax -> exchange: a tile's scores read (4 warps)
-  kDrainPv = 2 * kStages + 20,
-  kRecvRead = 2 * kStages + 21,  // [2] exchange -> exchange: a tile's peer partial read (4 warps)
-  kNumBars = 2 * kStages + 23
+  kQkFull = 0,                        // [kQkStages] TMA -> QK issuer: latent tile landed
+  kRopeFull = kQkFull + kQkStages,    // [kRopeStages] TMA -> QK issuer: rope tile landed
+  kVFull = kRopeFull + kRopeStages,   // [kVStages] re-read latent tile landed
+  kVEmpty = kVFull + kVStages,        // [kVStages] PV done -> PV issuer
+  // Barriers that a group waits for are kept per group (tile % 3): a parity wait must never
+  // skip a phase, or it can return on the stale completion of the phase before, so every
+  // waiter of a barrier must see each of its phases.
+  kSFull = kVEmpty + kVStages,        // [3] QK(i) done -> group, and -> TMA (its slots are free)
+  kSFree = kSFull + kGroups,          // [3] group -> QK issuer: S buffer read (4 warps)
+  kRecvFull = kSFree + kGroups,       // [3] peer partial landed (expect_tx by one thread here)
+  kRecvFree = kRecvFull + kGroups,    // [2] peer -> here: it has read our tile in its buffer i & 1
+  kFreeSeen = kRecvFree + 2,          // [3] group -> next group: past its kRecvFree wait (4 warps)
+  kSigSent = kFreeSeen + kGroups,     // [3] group -> next group: its "free" signal is out (4 warps)
+  kMref = kSigSent + kGroups,        // [3] group -> next group: reference maximum (128 threads)
+  kPvDone = kMref + kGroups,          // [3] PV issuer -> next group: P buffer free, O stable
+  kPFull = kPvDone + kGroups,         // group -> PV issuer: P(i) in shared memory (128 threads)
+  kQFull,
+  kQReady,
+  kDrain,
+  kDrainPv,
+  kNumBars
 };
-static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(kNumBars * 8 <= 384, "barrier area");
 
 struct Maps {
   CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle
@@ -114,6 +129,20 @@ struct Maps {
 
 __device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int t) {
   return p.block_table[(int64_t)b * p.max_pages + t / kPage];
+}
+
+// Row coordinate of the tile starting at position t in the tensor maps (a page past the pool
+// for a bad block-table entry: the copy then fills zeros and the tile is masked).
+__device__ __forceinline__ int tile_row(const DecodeParams& p, int b, int t, bool flag) {
+  if (p.block_table) {
+    const int page = tile_page(p, b, t);
+    if (page < 0 || page >= p.num_pages) {
+      if (flag) raise_flag(p.status, kFlagBlockTable);
+      return p.num_pages * kPage;
+    }
+    return page * kPage;
+  }
+  return (int)((int64_t)b * p.kv_seq_stride + t);
 }
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
@@ -171,25 +200,32 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   }
 
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kKvFull + i), 1);
-      mbar_init(bar(kKvEmpty + i), 1);
+    for (int i = 0; i < kQkStages; ++i) mbar_init(bar(kQkFull + i), 1);
+    for (int i = 0; i < kRopeStages; ++i) mbar_init(bar(kRopeFull + i), 1);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(bar(kVFull + i), 1);
+      mbar_init(bar(kVEmpty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kSFull + i), 1);
-      mbar_init(bar(kSFree + i), kExchWarps / 2);
-      mbar_init(bar(kScoreFree + i), kSoftmaxWarps);
-      mbar_init(bar(kRecvRead + i), kExchWarps / 2);
-      mbar_init(bar(kPFull + i), 32 * kSoftmaxWarps);
-      mbar_init(bar(kPvDone + i), 1);
-      mbar_init(bar(kRecvFull + i), 1);
+    for (int g = 0; g < kGroups; ++g) {
+      mbar_init(bar(kSFull + g), 1);
+      mbar_init(bar(kSFree + g), kGroupWarps);
+      mbar_init(bar(kRecvFull + g), 1);
+      mbar_init(bar(kFreeSeen + g), kGroupWarps);
+      mbar_init(bar(kSigSent + g), kGroupWarps);
+      mbar_init(bar(kMref + g), kGroupThreads);
+      mbar_init(bar(kPvDone + g), 1);
     }
+    mbar_init(bar(kPFull), kGroupThreads);
     mbar_init(bar(kQFull), 1);
-    mbar_init(bar(kQReady), 32 * kExchWarps);
-    mbar_init(bar(kSReady), 32 * kExchWarps / 2);
+    mbar_init(bar(kQReady), 2 * kGroupThreads);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
+    mbar_init(bar(kRecvFree + 0), 1);
+    mbar_init(bar(kRecvFree + 1), 1);
     fence_mbar_init();
+    // The first waits on kRecvFree are for tiles 2 and 3 (the peer has read tiles 0, 1).
+    if (ntiles > 2) mbar_arrive_expect_tx(bar(kRecvFree + 0), 4 * kGroupWarps);
+    if (ntiles > 3) mbar_arrive_expect_tx(bar(kRecvFree + 1), 4 * kGroupWarps);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -208,134 +244,174 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   if (warp != 0) grid_dep_wait();
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0 && ntiles > 0) {
+    // ---------------- TMA producer: score operands, straight from HBM ----------------
+    // Tile i: its 256 latent columns into QK slot i % 3 (free once QK(i-3) is done) and its
+    // 32 rope columns into rope slot i % 2 (free once QK(i-2) is done).  "QK(j) done" is the commit the score groups wait for (kSFull):
+    // the TMA thread waits for each of its phases in order, and the next phase of that
+    // barrier needs a tile that is requested only after the wait.
+    if (lane == 0) {
       prefetch_tmap(&maps.kv_lat);
       prefetch_tmap(&maps.kv_rope);
       prefetch_tmap(&maps.q_rope);
-      // Row coordinate of tile i in the tensor maps (a page past the pool for a bad
-      // block-table entry: the copy then fills zeros and the tile is masked).
-      auto tile_row = [&](int i, bool flag) -> int {
-        const int t = t0 + i * kN;
-        if (p.block_table) {
-          const int page = tile_page(p, b, t);
-          if (page < 0 || page >= p.num_pages) {
-            if (flag) raise_flag(p.status, kFlagBlockTable);
-            return p.num_pages * kPage;
-          }
-          return page * kPage;
-        }
-        return (int)((int64_t)b * p.kv_seq_stride + t);
+      int issued = 0, rope_issued = 0;
+      bool q_issued = false;
+      // q^R comes from q_cat, which the previous kernel writes: it is requested after the
+      // first tiles (which no kernel writes), and before the first wait that needs QK(0).
+      auto load_q = [&]() {
+        grid_dep_wait();
+        mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
+        tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+        q_issued = true;
       };
-      int issued = 0;
+      auto qk_done = [&](int j) {
+        return mbar_wait(bar(kSFull + j % kGroups), (uint32_t)(j / kGroups) & 1u, kWaitNs);
+      };
       for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(bar(kKvEmpty + st), ph ^ 1u, kWaitNs)) {
+        const int qs = i % kQkStages, rs = i % kRopeStages;
+        const int y = tile_row(p, b, t0 + i * kN, true);
+        if (i >= kRopeStages && !q_issued) load_q();
+        if (i >= kQkStages && !qk_done(i - kQkStages)) {
           aborted = true;
           break;
         }
-        const int y = tile_row(i, true);
-        const uint32_t stage = s0 + (uint32_t)st * kStageBytes;
-        mbar_arrive_expect_tx(bar(kKvFull + st), kStageBytes);
+        mbar_arrive_expect_tx(bar(kQkFull + qs), kLatBytes);
         for (int j = 0; j < 4; ++j)
-          tma_load_2d(stage + j * kBoxBytes, &maps.kv_lat, bar(kKvFull + st), 256 * (int)rank + 64 * j, y);
-        tma_load_2d(stage + 4 * kBoxBytes, &maps.kv_rope, bar(kKvFull + st), kDc + 32 * (int)rank, y);
+          tma_load_2d(s0 + kOffQk + (uint32_t)qs * kLatBytes + j * kBoxBytes, &maps.kv_lat, bar(kQkFull + qs),
+                      256 * (int)rank + 64 * j, y);
         ++issued;
-        if (i == min(kStages, ntiles) - 1) {
-          // The ring is full: now wait for the previous kernel, then fetch q^R from q_cat.
-          grid_dep_wait();
-          mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
-          tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+        if (i >= kRopeStages && !qk_done(i - kRopeStages)) {
+          aborted = true;
+          break;
         }
+        mbar_arrive_expect_tx(bar(kRopeFull + rs), kRopeBoxBytes);
+        tma_load_2d(s0 + kOffRope + (uint32_t)rs * kRopeBoxBytes, &maps.kv_rope, bar(kRopeFull + rs),
+                    kDc + 32 * (int)rank, y);
+        ++rope_issued;
       }
+      if (!q_issued && !aborted) load_q();
       // No copy may still be landing when the CTA exits.
-      for (int i = max(0, issued - kStages); i < issued; ++i)
-        mbar_wait(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u, kWaitNs);
-      if (!mbar_wait(bar(kQFull), 0, kWaitNs)) aborted = true;
+      for (int i = max(0, issued - kQkStages); i < issued; ++i)
+        mbar_wait(bar(kQkFull + i % kQkStages), (uint32_t)(i / kQkStages) & 1u, kWaitNs);
+      for (int i = max(0, rope_issued - kRopeStages); i < rope_issued; ++i)
+        mbar_wait(bar(kRopeFull + i % kRopeStages), (uint32_t)(i / kRopeStages) & 1u, kWaitNs);
+      if (q_issued && !mbar_wait(bar(kQFull), 0, kWaitNs)) aborted = true;
     }
   } else if (warp == 1) {
     // ---------------- QK issuer ----------------
-    // QK(i): partial scores of tile i into S buffer i & 1, once the tile has landed and
-    // the softmax has read S buffer i & 1 (tile i-2).  Steps 0-15: latent half (A = q~
-    // half from TMEM, B = cache rows, K-major, 128B swizzle); steps 16-17: rope half
-    // (A = q^R half from smem, B = k^R half, 64B swizzle).  Shared-memory descriptors are
-    // built once per tile: the 14-bit start field holds (address >> 4), so stepping
-    // through a tile adds a compile-time constant to the 64-bit descriptor.
-    if (lane == 0 && ntiles > 0) {
+    // QK(i): partial scores of tile i into S buffer i & 1, once group (i-2) % 3 has read
+    // that buffer: 16 latent MMAs (A = q~ half from TMEM, B = cache rows, K-major, 128B
+    // swizzle), then two rope MMAs (A = q^R half from smem, B = k^R half, 64B swizzle; the
+    // rope tile is requested last, so it is awaited only here), and one commit.  Every
+    // instruction of this thread queues behind the tcgen05 and shared-memory traffic of the
+    // other warps, so the loop keeps to few waits and one commit (waits placed between the
+    // MMAs of a chain slowed the issue down).  Shared-memory descriptors hold (address >> 4)
+    // in their 14-bit start field, so stepping through a tile adds a compile-time constant
+    // to the 64-bit descriptor.
+    if (lane == 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
       const uint64_t qrope_desc = smem_desc(s0 + kOffQRope, 16, 512, kSwizzle64B);
       if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
       for (int i = 0; i < ntiles && !aborted; ++i) {
-        if ((i >= 2 && !mbar_wait(bar(kSFree + (i & 1)), (uint32_t)((i - 2) >> 1) & 1u, kWaitNs)) ||
-            !mbar_wait(bar(kKvFull + i % kStages), (uint32_t)(i / kStages) & 1u, kWaitNs)) {
+        const int qs = i % kQkStages, rs = i % kRopeStages;
+        const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
+        if ((i >= 2 && !mbar_wait(bar(kSFree + (i - 2) % kGroups), (uint32_t)((i - 2) / kGroups) & 1u, kWaitNs)) ||
+            !mbar_wait(bar(kQkFull + qs), (uint32_t)(i / kQkStages) & 1u, kWaitNs)) {
           aborted = true;
           break;
         }
         tc_fence_after();
-        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
-        const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
-        const uint64_t kv = smem_desc(stage, 16, 1024, kSwizzle128B);
-        const uint64_t kr = smem_desc(stage + 4 * kBoxBytes, 16, 512, kSwizzle64B);
+        const uint64_t kv = smem_desc(s0 + kOffQk + (uint32_t)qs * kLatBytes, 16, 1024, kSwizzle128B);
+        const uint64_t kr = smem_desc(s0 + kOffRope + (uint32_t)rs * kRopeBoxBytes, 16, 512, kSwizzle64B);
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          mma_ts(d, tb + kTmemQ + 8u * k, kv + (((k >> 2) * kBoxBytes + (k & 3) * 32u) >> 4), id_qk, k > 0);
+          mma_ts(d, tb + kTmemQ + 8u * k, kv + (((k >> 2) * kBoxBytes + (k & 3) * 32u) >> 4), id_qk, k > 0 ? 1u : 0u);
+        if (!mbar_wait(bar(kRopeFull + rs), (uint32_t)(i / kRopeStages) & 1u, kWaitNs)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 2; ++k) mma_ss(d, qrope_desc + 2u * k, kr + 2u * k, id_qk, 1);
-        mma_commit(bar(kSFull + (i & 1)));
+        for (int k = 0; k < 2; ++k) mma_ss(d, qrope_desc + 2u * k, kr + 2u * k, id_qk, 1u);
+        mma_commit(bar(kSFull + i % kGroups));
       }
       mma_commit(bar(kDrain));
       mbar_wait(bar(kDrain), 0, kWaitNs);
     }
   } else if (warp == kPvWarp) {
-    // ---------------- PV issuer ----------------
-    // PV(i): O half += P(i) . V(i) once P(i) is in shared memory, then release the
-    // stage and the P buffer.  A separate issuing warp lets a PV enter the tensor pipe
-    // while a QK chain (18 dependent MMAs) is still being issued.  A = P (smem, K-major),
-    // B = the staged tile read MN-major (N = 256 latent columns over four 64-column
-    // boxes, K = 16 rows per step).
-    if (lane == 0 && ntiles > 0) {
+    // ---------------- PV issuer (and the V re-reads) ----------------
+    // The aggregation reads the same 256 latent columns of tile i again, into V slot i % 2,
+    // a few tiles after the score ring fetched them (so from L2).  A stage of the score
+    // ring is thus held only through the score MMAs, not through exchange and softmax.
+    // V(i+1) is requested as soon as PV(i-1) has released its slot.  PV(i): O half +=
+    // P(i) . V(i), A = P (smem, K-major), B = the V tile read MN-major (N = 256 latent
+    // columns over four 64-column boxes, K = 16 rows per step).
+    if (lane == 0) {
       const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      auto load_v = [&](int i) {
+        const int vs = i % kVStages;
+        const int y = tile_row(p, b, t0 + i * kN, false);
+        mbar_arrive_expect_tx(bar(kVFull + vs), kLatBytes);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(s0 + kOffV + (uint32_t)vs * kLatBytes + j * kBoxBytes, &maps.kv_lat, bar(kVFull + vs),
+                      256 * (int)rank + 64 * j, y);
+      };
+      int v_issued = 0;
+      for (; v_issued < min(kVStages, ntiles); ++v_issued) load_v(v_issued);
       for (int i = 0; i < ntiles; ++i) {
-        const int buf = i & 1;
-        if (!mbar_wait(bar(kPFull + buf), (uint32_t)(i >> 1) & 1u, kWaitNs)) {
+        const int vs = i % kVStages;
+        if (i + 1 < ntiles && i + 1 >= kVStages) {
+          if (!mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, kWaitNs)) {
+            aborted = true;
+            break;
+          }
+          load_v(i + 1);
+          ++v_issued;
+        }
+        if (!mbar_wait(bar(kPFull), (uint32_t)i & 1u, kWaitNs) ||
+            !mbar_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, kWaitNs)) {
           aborted = true;
           break;
         }
         tc_fence_after();
         const uint64_t pd = smem_desc(s0 + kOffP, 16, 1024, kSwizzle128B);
-        const uint64_t vd = smem_desc(s0 + (uint32_t)(i % kStages) * kStageBytes, 8192, 1024, kSwizzle128B);
+        const uint64_t vd = smem_desc(s0 + kOffV + (uint32_t)vs * kLatBytes, 8192, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k)
           mma_ss(tb + kTmemO, pd + 2u * k, vd + 128u * k, id_pv, (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar(kKvEmpty + i % kStages));
-        mma_commit(bar(kPvDone + buf));
+        mma_commit(bar(kVEmpty + vs));
+        mma_commit(bar(kPvDone + i % kGroups));
       }
       mma_commit(bar(kDrainPv));
       mbar_wait(bar(kDrainPv), 0, kWaitNs);
+      for (int i = max(0, v_issued - kVStages); i < v_issued; ++i)
+        mbar_wait(bar(kVFull + i % kVStages), (uint32_t)(i / kVStages) & 1u, kWaitNs);
     }
-  } else if (warp < 2 + kExchWarps) {
-    // ---------------- exchange (warps 2..9) ----------------
-    // Warp w covers TMEM lane quarter q = w % 4 and the tiles i with i % 2 == e,
-    // e = (w - 2) / 4 (S buffer e, receive buffer e): two warps per quarter, so that one
-    // waits for the peer's partial of its tile while the other sends the next.  Per
-    // tile: own fp32 partial scores (64 columns of 32 heads) out of TMEM, a bf16 copy to
-    // the peer, the peer's bf16 partial in, the row maximum, and the scores relative to
-    // it (fp16) into shared memory for the softmax warps.
+  } else {
+    // ---------------- score-to-P groups (warps 2..13) ----------------
+    // Group g = (w - 2) / 4 takes the tiles i with i % 3 == g; its warp w covers TMEM lane
+    // quarter w % 4 (heads 32q..32q+31, one head per lane).  Per tile: own fp32 partial
+    // scores out of TMEM, a bf16 copy to the peer, the peer's bf16 partial in, the row
+    // maximum, the reference maximum (handed on from the group of tile i-1), P = 2^(s -
+    // m_ref) into shared memory, and the running output rescaled when m_ref moves.  Each
+    // group keeps its own share of the row sum; the shares are merged at the end.
+    const int g = (warp - 2) / kGroupWarps;
     const int quarter = warp & 3;
-    const int e = (warp - 2) >> 2;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
+    const int gtid = tid - 32 * (2 + g * kGroupWarps);
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
     const int64_t qrow = (int64_t)m * p.H + h;
     const uint32_t xoff = (uint32_t)quarter * kQuarterXBytes + (uint32_t)lane * 16u;
     const uint32_t recv_local = s0 + kOffRecv;
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
-    const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull), peer);
-    if (ntiles > 0) {
-      // Half (e) of this head's 256 q~ columns into TMEM (A operand of the score MMA,
+    const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull + g), peer);
+    const uint32_t free_bar_peer = map_to_rank(bar(kRecvFree), peer);
+    const uint32_t sig_peer = map_to_rank(s0 + kOffSig + 4u * (uint32_t)quarter, peer);
+    float* mref_sh = reinterpret_cast<float*>(smem + kOffMref);
+    if (g < 2) {
+      // Half g of this head's 256 q~ columns into TMEM (A operand of the score MMA,
       // bf16 pairs packed in 32-bit columns).
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * e);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * g);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
@@ -347,60 +423,94 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           r[4 * v + 2] = w.z;
           r[4 * v + 3] = w.w;
         }
-        tmem_st32(tb + lane_off + kTmemQ + 64u * e + 32u * c, r);
+        tmem_st32(tb + lane_off + kTmemQ + 64u * g + 32u * c, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
-      if (h == 0 && e < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + e), kRecvBytes);
     }
-    for (int i = e; i < ntiles && !aborted; i += 2) {
-      const int buf = e;
-      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      const uint32_t ts = tb + lane_off + kTmemS + 64u * buf;
-      if (!warp_wait(bar(kSFull + buf), ph)) {
+    if (h == 0 && g < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + g), kRecvBytes);
+
+    float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
+    for (int i = g; i < ntiles && !aborted; i += kGroups) {
+      const uint32_t ph = (uint32_t)(i / kGroups) & 1u;
+      const uint32_t sb = (uint32_t)(i & 1);          // S buffer and receive buffer
+      if (!warp_wait(bar(kSFull + g), ph)) {
         aborted = true;
         break;
       }
       tc_fence_after();
       // Own fp32 partial scores; the S buffer is free for QK(i+2) once they are read.
       float x[64];
-      tmem_ld32f<0>(ts, x);
-      tmem_ld32f<32>(ts + 32u, x);   // both requested before one wait (~290 cycles each)
-      tmem_ld_wait();
+      {
+        const uint32_t ts = tb + lane_off + kTmemS + 64u * sb;
+        tmem_ld32f<0>(ts, x);
+        tmem_ld32f<32>(ts + 32u, x);   // both requested before one wait
+        tmem_ld_wait();
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kSFree + buf));
-      // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7.
-      // Receive buffer `buf` is reused two tiles later without a remote handshake: tile
-      // i goes out only after the warps of tile i-1 here have read its peer partial
-      // (kRecvRead), and the peer follows the same rule, so it sends tile i+2 only after
-      // it has received tile i+1 from us, i.e. after we have read tile i.
-      if (i >= 1 && !warp_wait(bar(kRecvRead + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
+      if (lane == 0) mbar_arrive(bar(kSFree + g));
+      // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7, into
+      // its receive buffer i & 1, once the peer has read tile i-2 out of it: each of its 4
+      // warps then sends a 4-byte st.async counted on our kRecvFree[i & 1] (a remote
+      // mbarrier arrive is far slower under load).  The groups pass this wait in tile order
+      // (kFreeSeen), so each phase of kRecvFree[i & 1] is awaited after the one before it.
+      if (i >= 1 && !warp_wait(bar(kFreeSeen + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
         aborted = true;
         break;
       }
+      if (i >= 2) {
+        if (!warp_wait_cluster(bar(kRecvFree + sb), (uint32_t)((i - 2) >> 1) & 1u)) {
+          aborted = true;
+          break;
+        }
+        // Re-arm for the wait of tile i+2 (the peer's read of tile i).
+        if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFree + sb), 4 * kGroupWarps);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kFreeSeen + g));
       {
-        const uint32_t dst = recv_peer + (uint32_t)buf * kRecvBytes + xoff;
-        const uint32_t rb = recv_bar_peer + 8u * (uint32_t)buf;
+        const uint32_t dst = recv_peer + sb * kRecvBytes + xoff;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_async_v4(dst + (uint32_t)c * 512u, f2_to_bf2(x[8 * c], x[8 * c + 1]),
                       f2_to_bf2(x[8 * c + 2], x[8 * c + 3]), f2_to_bf2(x[8 * c + 4], x[8 * c + 5]),
-                      f2_to_bf2(x[8 * c + 6], x[8 * c + 7]), rb);
+                      f2_to_bf2(x[8 * c + 6], x[8 * c + 7]), recv_bar_peer);
       }
-      if (!warp_wait_cluster(bar(kRecvFull + buf), ph)) {
+      if (!warp_wait_cluster(bar(kRecvFull + g), ph)) {
         aborted = true;
         break;
       }
-      // Re-arm for tile i+2: the peer sends it only after our warps have read tile i.
-      if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + buf), kRecvBytes);
+      // Re-arm for tile i+3 (its bytes can only come after the phase of tile i completed:
+      // the peer sends tile i+3 after our "free" signal for tile i+1).
+      if (h == 0 && i + kGroups < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + g), kRecvBytes);
       {
-        const uint32_t rl = recv_local + (uint32_t)buf * kRecvBytes + xoff;
+        const uint32_t rl = recv_local + sb * kRecvBytes + xoff;
+        uint4 w[8];
+        uint32_t sig = 0;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 w = ld_shared_u4(rl + (uint32_t)c * 512u);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          w[c] = ld_shared_u4(rl + (uint32_t)c * 512u);
+          sig ^= w[c].x;
+        }
+        // Every lane's loads have returned (sig depends on them) before lane 0 tells the
+        // peer that buffer i & 1 may be overwritten (by tile i+2, if there is one).  The
+        // signals go out in tile order (kSigSent): the peer sends tile i+3, which lands on
+        // kRecvFull of this group, only after our signal for tile i+1, hence after this
+        // group's phase of tile i has completed and been read.
+        asm volatile("" ::"r"(sig));
+        if (i >= 1 && !warp_wait(bar(kSigSent + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+          aborted = true;
+          break;
+        }
+        if (lane == 0) {
+          if (i + 2 < ntiles) st_async_b32(sig_peer, sig, free_bar_peer + 8u * sb);
+          mbar_arrive(bar(kSigSent + g));
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
@@ -408,12 +518,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kRecvRead + buf));
-      // Readable rows of this tile, the row maximum over them (log2 units), and the
-      // scores relative to it.  The softmax takes exp2 of these, so they are stored as
-      // fp16: its error near 0, where the weights are largest, is under 2^-11 of the
-      // value (far below the bf16 rounding of P), and -inf marks an unreadable row.
+      // Readable rows of this tile and the row maximum over them (log2 units).
       const int t = t0 + i * kN;
       int valid = min(kN, t1 - t);
       if (p.block_table) {
@@ -436,102 +541,51 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
         mx = t16[0] * p.scale_log2;
       }
-      const float negmx = (mx == -INFINITY) ? 0.f : -mx;
-      if (i >= 1 && !warp_wait(bar(kScoreFree + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
-        aborted = true;
-        break;
-      }
-      {
-        const uint32_t row = s0 + kOffScore + (uint32_t)h * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            __half2 v = __floats2half2_rn(fmaf(x[8 * c + 2 * u], p.scale_log2, negmx),
-                                          fmaf(x[8 * c + 2 * u + 1], p.scale_log2, negmx));
-            w[u] = *reinterpret_cast<uint32_t*>(&v);
-          }
-          // Chunk c of row h at chunk c ^ (h & 7): conflict-free for row-per-lane access.
-          st_shared_u4(row + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+      // Lazy reference maximum, handed from tile to tile: it moves only when a tile's
+      // maximum exceeds it by more than 2^8.
+      float m_prev = -INFINITY;
+      if (i >= 1) {
+        if (!warp_wait(bar(kMref + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+          aborted = true;
+          break;
         }
-        reinterpret_cast<float*>(smem + kOffTmax)[h] = mx;
+        m_prev = mref_sh[h];
       }
-      mbar_arrive(bar(kSReady));
-    }
-  } else {
-    // ---------------- softmax / epilogue (warps 10..13) ----------------
-    // Warp w covers heads 32q..32q+31, q = w % 4 (its TMEM lane quarter, for O), and all
-    // 64 columns of each tile, from the scores and row maxima the exchange warps leave in
-    // shared memory.
-    const int quarter = warp & 3;
-    const int h = 32 * quarter + lane;
-    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
-    const bool head_ok = h < p.H;
-    const int64_t qrow = (int64_t)m * p.H + h;
-    float m_ref = -INFINITY, l = 0.f;
-
-    for (int i = 0; i < ntiles && !aborted; ++i) {
-      const int buf = i & 1;
-      if (!warp_wait(bar(kSReady), (uint32_t)i & 1u)) {
-        aborted = true;
-        break;
+      const bool grow = mx > m_prev + kRescaleThreshold;
+      const float m_new = grow ? mx : m_prev;
+      mref_sh[h] = m_new;
+      mbar_arrive(bar(kMref + g));
+      const float alpha = grow ? ex2_approx(m_prev - m_new) : 1.f;   // 0 when m_prev = -inf
+      if (m_g != m_new) {
+        l_g *= ex2_approx(m_g - m_new);
+        m_g = m_new;
       }
-      // Readable rows of this tile (for clearing the V rows past them below).
-      const int t = t0 + i * kN;
-      int valid = min(kN, t1 - t);
-      if (p.block_table) {
-        const int page = tile_page(p, b, t);
-        if (page < 0 || page >= p.num_pages) valid = 0;
-      }
-      // The 64 scores of this row, relative to the tile maximum mx (log2 units).
-      uint32_t xh[32];   // fp16 pairs
-      const float mx = reinterpret_cast<const float*>(smem + kOffTmax)[h];
-      {
-        const uint32_t row = s0 + kOffScore + (uint32_t)h * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 w = ld_shared_u4(row + (uint32_t)((c ^ (h & 7)) << 4));
-          xh[4 * c] = w.x;
-          xh[4 * c + 1] = w.y;
-          xh[4 * c + 2] = w.z;
-          xh[4 * c + 3] = w.w;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kScoreFree + buf));
-      // Lazy maximum: move the reference only when the tile exceeds it by > 2^8.
-      const bool grow = mx > m_ref + kRescaleThreshold;
-      const float m_new = grow ? mx : m_ref;
-      const float alpha = grow ? ex2_approx(m_ref - m_new) : 1.f;   // 0 when m_ref = -inf
-      l *= alpha;
-      m_ref = m_new;
-      // The P buffer is free, and O stable, once PV(i-1) is done.
-      if (i >= 1 && !warp_wait(bar(kPvDone + ((i - 1) & 1)), (uint32_t)((i - 1) >> 1) & 1u)) {
-        aborted = true;
-        break;
-      }
-      // p = 2^(x + mx - m_ref); a tile with no readable row (mx = -inf) gives p = 0.
-      const float neg = (mx == -INFINITY) ? -INFINITY : mx - m_ref;
-      const uint32_t prow = s0 + kOffP + (uint32_t)h * 128u;
+      // p = 2^(s * scale_log2 - m_ref); unreadable rows (s = -inf) give p = 0, and so does
+      // every row while no readable row has been seen (m_ref = -inf).
+      const float bias = (m_new == -INFINITY) ? 0.f : -m_new;
+      uint32_t pw[32];
       float ps = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xh[4 * c + u]));
-          const float a = ex2_approx(f.x + neg);
-          const float d = ex2_approx(f.y + neg);
-          ps += a + d;
-          w[u] = f2_to_bf2(a, d);
-        }
-        // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7).
-        st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), w[0], w[1], w[2], w[3]);
+      for (int j = 0; j < 32; ++j) {
+        const float a = ex2_approx(fmaf(x[2 * j], p.scale_log2, bias));
+        const float d = ex2_approx(fmaf(x[2 * j + 1], p.scale_log2, bias));
+        ps += a + d;
+        pw[j] = f2_to_bf2(a, d);
       }
-      l += ps;
-
-      // Rescale this warp's rows of O (PV(i-1) has landed); xh is no longer live here.
+      l_g += ps;
+      // The P buffer is free, and O stable, once PV(i-1) is done.
+      if (i >= 1 && !warp_wait(bar(kPvDone + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+        aborted = true;
+        break;
+      }
+      {
+        const uint32_t prow = s0 + kOffP + (uint32_t)h * 128u;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)   // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7)
+          st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
+                       pw[4 * c + 3]);
+      }
+      // Rescale this warp's rows of O to the new reference (PV(i-1) has landed).
       if (__any_sync(0xffffffffu, grow && i > 0)) {
         tc_fence_after();
 #pragma unroll 1
@@ -547,59 +601,62 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         tmem_st_wait();
         tc_fence_before();
       }
-
       // Rows past the readable range may hold anything (even NaN): clear them in the
-      // V columns of the staged tile so that 0-weighted rows add exactly 0.
+      // re-read V tile so that 0-weighted rows add exactly 0.
       if (valid < kN) {
-        const uint32_t stage = s0 + (uint32_t)(i % kStages) * kStageBytes;
+        const int vs = i % kVStages;
+        if (!warp_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u)) {
+          aborted = true;
+          break;
+        }
+        const uint32_t vt = s0 + kOffV + (uint32_t)vs * kLatBytes;
         const int nrow = kN - valid;
-        for (int idx = tid - 32 * (2 + kExchWarps); idx < nrow * 32; idx += 32 * kSoftmaxWarps) {
+        for (int idx = gtid; idx < nrow * 32; idx += kGroupThreads) {
           const int row = valid + idx / 32, c = idx % 32;   // 4 boxes x 8 chunks per row
-          st_shared_v4_zero(stage + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u +
-                            (uint32_t)(c & 7) * 16u);
+          st_shared_v4_zero(vt + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u + (uint32_t)(c & 7) * 16u);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(kPFull + buf));
+      mbar_arrive(bar(kPFull));
     }
 
-    // Epilogue: this warp's rows of the O half, divided by the row sum.
+    // Epilogue.  The groups' row-sum shares, each moved to the final reference maximum,
+    // are summed through shared memory (the receive buffers are idle now); then each
+    // group writes its columns chunks c = g, g+3, g+6 of the O half divided by the sum.
+    named_bar_sync(1, kGroups * kGroupThreads);
+    const float m_fin = mref_sh[h];
+    float* lsh = reinterpret_cast<float*>(smem + kOffRecv);
+    lsh[g * 128 + h] = (l_g > 0.f) ? l_g * ex2_approx(m_g - m_fin) : 0.f;
+    named_bar_sync(1, kGroups * kGroupThreads);
+    const float l = lsh[h] + lsh[128 + h] + lsh[256 + h];
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
     float* out = p.o_out + orow * kDc + 256 * rank;
-    const bool have = ntiles > 0 && l > 0.f;
-    if (ntiles > 0 && !aborted) {
+    const bool have = !aborted && l > 0.f;
+    if (!aborted) {
       const int last = ntiles - 1;
-      if (!warp_wait(bar(kPvDone + (last & 1)), (uint32_t)(last >> 1) & 1u)) aborted = true;
+      if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u)) aborted = true;
     }
     tc_fence_after();
     const float inv = have ? 1.f / l : 0.f;
-    if (ntiles > 0 && !aborted) {
 #pragma unroll 1
-      for (int c = 0; c < 8; c += 2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tb + lane_off + kTmemO + 32u * c, r0);
-        tmem_ld32(tb + lane_off + kTmemO + 32u * (c + 1), r1);
+    for (int c = g; c < 8; c += kGroups) {
+      uint32_t r[32];
+      if (!aborted) {
+        tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
         tmem_ld_wait();
-        if (head_ok) {
-          // A row that saw no readable position (l == 0) is written as exact zeros.
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            reinterpret_cast<float4*>(out + 32 * c)[v] =
-                have ? make_float4(__uint_as_float(r0[4 * v]) * inv, __uint_as_float(r0[4 * v + 1]) * inv,
-                                   __uint_as_float(r0[4 * v + 2]) * inv, __uint_as_float(r0[4 * v + 3]) * inv)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            reinterpret_cast<float4*>(out + 32 * (c + 1))[v] =
-                have ? make_float4(__uint_as_float(r1[4 * v]) * inv, __uint_as_float(r1[4 * v + 1]) * inv,
-                                   __uint_as_float(r1[4 * v + 2]) * inv, __uint_as_float(r1[4 * v + 3]) * inv)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
       }
-    } else if (head_ok) {
-      for (int v = 0; v < 64; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (head_ok) {
+        // A row that saw no readable position (l == 0) is written as exact zeros.
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          reinterpret_cast<float4*>(out + 32 * c)[v] =
+              have ? make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                 __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    if (head_ok && rank == 0)
-      p.lse_out[orow] = have ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    if (g == 0 && head_ok && rank == 0)
+      p.lse_out[orow] = have ? (m_fin + log2f(l)) * kLn2 : -INFINITY;
   }
 
   if (aborted) raise_flag(p.status, kFlagTimeout);

@@ -150,6 +150,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
       : "memory");
 }
 
+// Asynchronous 4-byte store into another CTA's shared memory, counted on its mbarrier: a
+// cheap signal to the peer (under HBM load it lands in about 500 cycles, where a remote
+// mbarrier.arrive.release took several thousand).
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+               "r"(v), "r"(remote_bar)
+               : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to another CTA's
 // shared memory (address from mapa), counted (complete_tx) on that CTA's mbarrier.  The
 // copy reads its source through the async proxy: generic stores to it must be fenced
