@@ -108,7 +108,9 @@ class ClockSampler:
     """SM clock and clock-event reasons sampled while `active` is set.
 
     NVML (handle found by the device's UUID, so CUDA_VISIBLE_DEVICES remapping is
-    harmless); if NVML is unusable, `nvidia-smi -lms` on the device's PCI bus id."""
+    harmless); if NVML is unusable, `nvidia-smi -lms` on the device's PCI bus id, started
+    before the warm-up and filtered to the samples stamped inside the timed region (or the
+    two that bracket it, when the region is shorter than the sampling period)."""
     REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
@@ -118,6 +120,7 @@ class ClockSampler:
         self.reasons = set()
         self.max_mhz = None
         self.active = False
+        self.window = [None, None]   # host wall-clock times of the timed region
         self.error = None
         self._stop = False
         self.nv = None
@@ -158,18 +161,27 @@ class ClockSampler:
                     self.error = f"nvml sample: {e!r}"
             time.sleep(0.001)
 
+    def begin(self):
+        self.window[0] = time.time()
+        self.active = True
+
+    def end(self):
+        self.active = False
+        self.window[1] = time.time()
+
+    SMI_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
     def start_smi(self):
-        """Fallback sampler: nvidia-smi on this device, 20 ms period."""
-        if self.nv is not None:
+        """Fallback sampler: nvidia-smi on this device, 20 ms period, from now on."""
+        if self.nv is not None or self.proc is not None:
             return
         import shutil
         import subprocess
         if not shutil.which("nvidia-smi"):
             return
-        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
-        self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.bus}", f"--query-gpu={q}",
+        self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.bus}", f"--query-gpu={self.SMI_FIELDS}",
                                       "--format=csv,noheader,nounits", "-lms", "20"],
                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
 
@@ -179,22 +191,54 @@ class ClockSampler:
         if self.proc is not None:
             self.proc.terminate()
             out = self.proc.communicate(timeout=5)[0]
-            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-            for line in out.splitlines():
-                f = [x.strip() for x in line.split(",")]
-                if len(f) < 6 or not f[0].isdigit():
-                    continue
-                self.samples.append(int(f[0]))
-                self.max_mhz = int(f[1]) if f[1].isdigit() else self.max_mhz
-                for name, v in zip(names, f[2:]):
-                    if v.lower() == "active":
-                        self.reasons.add(name)
+            mhz, max_mhz, reasons, how = smi_window(out.splitlines(), *self.window)
+            self.samples += mhz
+            self.max_mhz = max_mhz if max_mhz is not None else self.max_mhz
+            self.reasons |= reasons
+            if how:
+                self.error = how
         d = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
              "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
              "samples": len(self.samples)}
-        if self.error and not self.samples:
-            d["error"] = self.error
+        if self.error:
+            d["note" if self.samples else "error"] = self.error
         return d
+
+
+def smi_window(lines, t0, t1):
+    """Samples of `nvidia-smi --query-gpu=<ClockSampler.SMI_FIELDS> --format=csv,noheader,
+    nounits` stamped inside [t0, t1] (host epoch seconds).  When none falls inside (a region
+    shorter than the period), the last sample before and the first after are used instead.
+    Returns (sm MHz list, max MHz, reason names, note or None)."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 7 or not f[1].isdigit():
+            continue
+        try:
+            ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            continue
+        rows.append((ts, f))
+    if not rows or t0 is None or t1 is None:
+        return [], None, set(), "nvidia-smi: no samples"
+    inside = [f for ts, f in rows if t0 <= ts <= t1]
+    note = None
+    if not inside:
+        before = [f for ts, f in rows if ts < t0][-1:]
+        after = [f for ts, f in rows if ts > t1][:1]
+        inside = before + after
+        note = "nvidia-smi: region shorter than the 20 ms period; bracketing samples"
+    max_mhz = None
+    reasons = set()
+    for f in inside:
+        max_mhz = int(f[2]) if f[2].isdigit() else max_mhz
+        for name, v in zip(names, f[3:]):
+            if v.lower() == "active":
+                reasons.add(name)
+    return [int(f[1]) for f in inside], max_mhz, reasons, note
 
 
 def blas_threads():
@@ -316,6 +360,7 @@ def main():
         mla.mla_out_proj_uv(step.o_lat, w_uv, step.o, st)
 
     clocks = ClockSampler(dev)
+    clocks.start_smi()          # no-op with NVML; nvidia-smi needs a moment to start
     for _ in range(args.warmup):
         run_step(stream)
     torch.cuda.synchronize()
@@ -351,9 +396,8 @@ def main():
         use_graph = False
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks.start_smi()
     barrier()
-    clocks.active = True
+    clocks.begin()
     start.record(stream)
     if use_graph:
         graph.replay()
@@ -364,7 +408,7 @@ def main():
             run_step(stream, lambda j, i=i: dec_events[i][j].record(stream))
     end.record(stream)
     barrier()
-    clocks.active = False
+    clocks.end()
     total_ms = start.elapsed_time(end)
     if use_graph:
         dec_ms = [cudart.cudaEventElapsedTime(a, b)[1] for a, b in evs]
