@@ -139,20 +139,43 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
     }
   }
 
-  // The RoPE slice q_cat[..., 512:576]: rotated at the query position, or copied.
-  if (nh == 0) {
+  // The RoPE slice q_cat[..., 512:576]: rotated at the query position, or copied.  The
+  // two CTAs of a head share the rows, in 16-byte pieces (8 per row); every thread loads
+  // all of its pieces before it stores any, so the copy costs one memory latency rather
+  // than one per piece.
+  {
+    constexpr int kPieces = kDr * 2 / 16;
+    constexpr int kPerThread = (kTileM * kPieces / 2 + kAbsThreads - 1) / kAbsThreads;
     const int rows = min(kTileM, M - m0);
-    for (int idx = tid; idx < rows * (kDr / 2); idx += kAbsThreads) {
-      const int rr = idx / (kDr / 2), i = idx % (kDr / 2);
-      const size_t mh = (size_t)(m0 + rr) * H + h;
-      const uint32_t w = reinterpret_cast<const uint32_t*>(q_rope + mh * kDr)[i];
-      uint32_t o = w;
-      if (q_pos) {
-        const float2 x = bf2_to_f2(w);
-        const float2 y = rope_pair(x.x, x.y, q_pos[m0 + rr], freqs.inv_freq[i]);
-        o = f2_to_bf2(y.x, y.y);
+    const int half = (rows * kPieces + 1) / 2;
+    const int begin = nh * half, end = min(rows * kPieces, begin + half);
+    uint4 v[kPerThread];
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int idx = begin + tid + u * kAbsThreads;
+      if (idx < end) {
+        const size_t mh = (size_t)(m0 + idx / kPieces) * H + h;
+        v[u] = reinterpret_cast<const uint4*>(q_rope + mh * kDr)[idx % kPieces];
       }
-      reinterpret_cast<uint32_t*>(q_cat + mh * kRow + kDc)[i] = o;
+    }
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int idx = begin + tid + u * kAbsThreads;
+      if (idx < end) {
+        const int rr = idx / kPieces, piece = idx % kPieces;
+        const size_t mh = (size_t)(m0 + rr) * H + h;
+        uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        if (q_pos) {
+          const int pos = q_pos[m0 + rr];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 x = bf2_to_f2(w[j]);
+            const float2 y = rope_pair(x.x, x.y, pos, freqs.inv_freq[4 * piece + j]);
+            w[j] = f2_to_bf2(y.x, y.y);
+          }
+        }
+        reinterpret_cast<uint4*>(q_cat + mh * kRow + kDc)[piece] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
 
@@ -172,10 +195,12 @@ k_absorb_q(const __grid_constant__ AbsorbMaps maps, const __nv_bfloat16* __restr
 // Value up-projection.  CTA (h, m_blk):
 //   D[128 rows x 128] = bf16(o_lat[rows, h, 0:512]) . W_UV[h] (512 x 128, N contiguous)
 // All of W_UV[h] (8 chunks of 64 K-rows, two 64-wide N boxes each, read MN-major by the
-// MMA) and the fp32 o_lat rows (64-wide K chunks, a 2-deep ring) arrive by TMA.  The
-// CTA's threads round each fp32 chunk to bf16 into the 128B-swizzled K-major layout of
-// the A operand (double-buffered) while the next chunk lands; one thread issues the
-// MMAs.
+// MMA) and the fp32 o_lat rows (64-wide K chunks through a 64 KB ring: 2 deep with
+// 128-row boxes, 4 deep with 64-row boxes when M <= 64) arrive by TMA.  The CTA's
+// threads round each fp32 chunk to bf16 into the 128B-swizzled K-major layout of the A
+// operand (double-buffered) while the next chunks land; one thread issues the MMAs.
+// With 64-row boxes, A rows 64..127 are never written: the D rows they produce are
+// past M and not stored.
 // ---------------------------------------------------------------------------
 constexpr int kOutThreads = 128;
 constexpr int kOutChunks = kDc / 64;                   // 8 K chunks of 64
@@ -183,9 +208,11 @@ constexpr uint32_t kOutBBox = 64 * 128;                // 64 K-rows x 64 bf16
 constexpr uint32_t kOutBChunk = 2 * kOutBBox;          // N = 128
 constexpr uint32_t kOutAChunk = kTileM * 128;          // 128 rows x 64 bf16
 constexpr uint32_t kOutA32Chunk = kTileM * 64 * 4;     // 128 rows x 64 fp32
+constexpr uint32_t kOutRingBytes = 2 * kOutA32Chunk;   // fp32 ring: 2 x 128 rows or 4 x 64 rows
+constexpr int kOutMaxRing = 4;
 constexpr uint32_t kOutOffA = kOutChunks * kOutBChunk;
 constexpr uint32_t kOutOffA32 = kOutOffA + 2 * kOutAChunk;
-constexpr uint32_t kOutOffBar = kOutOffA32 + 2 * kOutA32Chunk;
+constexpr uint32_t kOutOffBar = kOutOffA32 + kOutRingBytes;
 constexpr uint32_t kOutSmem = kOutOffBar + 128 + 1024;
 static_assert(kOutSmem <= 232448, "shared memory per CTA");
 
@@ -195,26 +222,26 @@ struct OutMaps {
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
-k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restrict__ o) {
+k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, int box_rows, float* __restrict__ o) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = align1024(smem_raw);
   const uint32_t s0 = smem_addr(smem);
   const uint32_t bars = s0 + kOutOffBar;
   auto bar_b = [&](int c) { return bars + 8u * (uint32_t)c; };          // [8] W chunk landed
   auto bar_a = [&](int i) { return bars + 64u + 8u * (uint32_t)i; };    // [2] bf16 A buffer consumed
-  auto bar_l = [&](int i) { return bars + 80u + 8u * (uint32_t)i; };    // [2] fp32 chunk landed
-  const uint32_t bar_done = bars + 96u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOutOffBar + 112);
+  auto bar_l = [&](int i) { return bars + 80u + 8u * (uint32_t)i; };    // [4] fp32 chunk landed
+  const uint32_t bar_done = bars + 112u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOutOffBar + 120);
+  const uint32_t a32_bytes = (uint32_t)box_rows * 64u * 4u;
+  const int ring = (int)(kOutRingBytes / a32_bytes);   // 2 or 4
 
   const int h = blockIdx.x, m0 = blockIdx.y * kTileM;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int c = 0; c < kOutChunks; ++c) mbar_init(bar_b(c), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_a(i), 1);
-      mbar_init(bar_l(i), 1);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(bar_a(i), 1);
+    for (int i = 0; i < kOutMaxRing; ++i) mbar_init(bar_l(i), 1);
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
@@ -227,10 +254,10 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restr
   tc_fence_after();
   const uint32_t tb = *tmem_slot;
 
-  auto load_lat = [&](int c) {   // fp32 chunk c of the o_lat rows into ring slot c & 1
-    mbar_arrive_expect_tx(bar_l(c & 1), kOutA32Chunk);
-    tma_load_2d(s0 + kOutOffA32 + (uint32_t)(c & 1) * kOutA32Chunk, &maps.lat, bar_l(c & 1),
-                h * kDc + 64 * c, m0);
+  auto load_lat = [&](int c) {   // fp32 chunk c of the o_lat rows into ring slot c % ring
+    const int sl = c % ring;
+    mbar_arrive_expect_tx(bar_l(sl), a32_bytes);
+    tma_load_2d(s0 + kOutOffA32 + (uint32_t)sl * a32_bytes, &maps.lat, bar_l(sl), h * kDc + 64 * c, m0);
   };
   // W_UV does not depend on the previous kernel: it is requested before waiting for it
   // (programmatic dependent launch); o_lat, which that kernel writes, after.
@@ -245,25 +272,24 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restr
     }
   }
   grid_dep_wait();
-  if (tid == 0) {
-    load_lat(0);
-    load_lat(1);
-  }
+  if (tid == 0)
+    for (int c = 0; c < ring; ++c) load_lat(c);
 
-  // Thread (warp, lane) converts rows 2*(4*it + warp) + (lane >> 4), it = 0..15, and the
-  // four K values 4*(lane & 15) .. +3 of the current chunk (a half-warp reads one 256-byte
-  // fp32 row: no bank conflicts).
+  // Thread (warp, lane) converts rows 2*(4*it + warp) + (lane >> 4), it < box_rows / 8,
+  // and the four K values 4*(lane & 15) .. +3 of the current chunk (a half-warp reads one
+  // 256-byte fp32 row: no bank conflicts).
   const int sub = lane >> 4, kq = lane & 15;
+  const int iters = box_rows / 8;
   bool ok = true;
   for (int c = 0; c < kOutChunks; ++c) {
-    const int buf = c & 1;
-    if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(bar_l(buf), (uint32_t)(c >> 1) & 1u, kWaitNs));
+    const int buf = c & 1, sl = c % ring;
+    if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(bar_l(sl), (uint32_t)(c / ring) & 1u, kWaitNs));
     if (c >= 2 && ok) ok = !__any_sync(0xffffffffu, !mbar_wait(bar_a(buf), (uint32_t)((c - 2) >> 1) & 1u, kWaitNs));
-    const uint32_t a32 = s0 + kOutOffA32 + (uint32_t)buf * kOutA32Chunk;
+    const uint32_t a32 = s0 + kOutOffA32 + (uint32_t)sl * a32_bytes;
     const uint32_t abase = s0 + kOutOffA + (uint32_t)buf * kOutAChunk;
     if (ok) {
 #pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
+      for (int it = 0; it < iters; ++it) {
         const int r = 2 * (4 * it + warp) + sub;
         const float4 v = ld_shared_v4(a32 + (uint32_t)r * 256u + (uint32_t)kq * 16u);
         // 128B swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7).
@@ -275,7 +301,7 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restr
     fence_proxy_async_smem();
     ok = __syncthreads_and(ok);   // also tells every thread of an earlier failed wait
     if (tid == 0 && ok) {
-      if (c + 2 < kOutChunks) load_lat(c + 2);   // fp32 slot `buf` has been converted
+      if (c + ring < kOutChunks) load_lat(c + ring);   // fp32 slot `sl` has been converted
       if (mbar_wait(bar_b(c), 0, kWaitNs)) {
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(kTileM, kDv, false, true);
@@ -324,7 +350,7 @@ k_out_proj_uv(const __grid_constant__ OutMaps maps, int M, int H, float* __restr
 
   if (tid == 0) {   // no copy may land after exit
     for (int c = 0; c < kOutChunks; ++c) mbar_wait(bar_b(c), 0, kWaitNs);
-    for (int c = kOutChunks - 2; c < kOutChunks; ++c) mbar_wait(bar_l(c & 1), (uint32_t)(c >> 1) & 1u, kWaitNs);
+    for (int c = kOutChunks - ring; c < kOutChunks; ++c) mbar_wait(bar_l(c % ring), (uint32_t)(c / ring) & 1u, kWaitNs);
   }
   tc_fence_before();
   __syncthreads();
@@ -364,16 +390,17 @@ cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_
 cudaError_t launch_out_proj_uv(const float* o_lat, const __nv_bfloat16* w_uv, int M, int H,
                                float* o, cudaStream_t st) {
   OutMaps maps;
+  const int box_rows = M <= 64 ? 64 : kTileM;   // no padding rows in the fp32 ring when M <= 64
   if (!encode_tma_2d(&maps.w, true, w_uv, kDv, (uint64_t)H * kDc, (uint64_t)kDv * 2, 64, 64,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tma_2d(&maps.lat, false, o_lat, (uint64_t)H * kDc, (uint64_t)M, (uint64_t)H * kDc * 4, 64,
-                     kTileM, CU_TENSOR_MAP_SWIZZLE_NONE))
+                     box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   static bool attr = false;
   cudaError_t e = set_smem(k_out_proj_uv, kOutSmem, attr);
   if (e != cudaSuccess) return e;
   dim3 grid(H, (M + kTileM - 1) / kTileM);
-  e = launch_pdl(k_out_proj_uv, grid, dim3(kOutThreads), kOutSmem, st, maps, M, H, o);
+  e = launch_pdl(k_out_proj_uv, grid, dim3(kOutThreads), kOutSmem, st, maps, M, H, box_rows, o);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
