@@ -81,6 +81,21 @@ def test_ragged_contiguous_edges(H, splits):
     assert np.all(np.isneginf(st.lse[6].cpu().numpy()))
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+def test_every_tile_count_up_to_13(splits):
+    # The decode kernel cycles its barriers with period 6 tiles (three score groups, two
+    # receive buffers, two rope and V slots, three score slots), and re-arms them by the
+    # number of tiles left.  One sequence per tile count 1..13, with ragged last tiles and
+    # NaN past the end, covers every residue twice.
+    lens = [64 * n - (7 * n) % 64 for n in range(1, 14)]
+    case = I.make_case("tile_counts", len(lens), 1, 128, lens, t_cap=13 * 64, seed=11)
+    dc = DeviceCase(case)
+    for b, T in enumerate(lens):
+        dc.kv[b, T:] = float("nan")
+    st = dc.step(num_splits=splits, max_seqlen=13 * 64)
+    check_case(dc, st, range(case.B), derived_lse_tol=True)
+
+
 @pytest.mark.parametrize("splits", [1, 4])
 def test_paged_small(splits):
     lens = [70, 1, 300, 64]
