@@ -68,24 +68,25 @@ constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swi
 constexpr uint32_t kLatBytes = 4 * kBoxBytes;     // 64 rows x this CTA's 256 latent columns
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
-constexpr uint32_t kTileBufBytes = 128 * kN * 2;  // per tile: the peer's bf16 partial, then P (bf16)
-constexpr uint32_t kRecvBytes = kTileBufBytes;
+constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
 constexpr uint32_t kQuarterXBytes = 32 * kN * 2;  // one lane quarter's share: 32 rows x 64 columns
+constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
 
 constexpr uint32_t kOffQk = 0;
 constexpr uint32_t kOffRope = kOffQk + kQkStages * kLatBytes;
 constexpr uint32_t kOffV = kOffRope + kRopeStages * kRopeBoxBytes;
 constexpr uint32_t kOffQRope = kOffV + kVStages * kLatBytes;
-constexpr uint32_t kOffTileBuf = kOffQRope + kQRopeBytes;   // [3] tile buffers, by tile % 3
-constexpr uint32_t kOffMref = kOffTileBuf + kGroups * kTileBufBytes;   // [128] reference maximum, log2 units
+constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
+constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
+constexpr uint32_t kOffMref = kOffP + kPBytes;    // [128] reference maximum per head, log2 units
 constexpr uint32_t kOffBars = kOffMref + 128 * 4;
 constexpr uint32_t kOffSlot = kOffBars + 384;
 constexpr uint32_t kOffSig = kOffSlot + 16;       // [4] landing words of the peer's "buffer free" signals
 constexpr uint32_t kSmemBytes = kOffSig + 16 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kOffV % 1024 == 0 && kOffTileBuf % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
+static_assert(kOffV % 1024 == 0 && kOffP % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
 static_assert(kOffRope % 512 == 0 && kOffQRope % 512 == 0, "64B-swizzled tiles need 512-byte alignment");
-static_assert(kGroups * kGroupThreads * 4 <= kTileBufBytes, "row sums reuse a tile buffer");
+static_assert(kGroups * kGroupThreads * 4 <= 2 * kRecvBytes, "row sums reuse the receive buffers");
 
 // TMEM columns.
 constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
@@ -106,11 +107,13 @@ enum Bar {
   kSFull = kVEmpty + kVStages,        // [3] QK(i) done -> group, and -> TMA (its slots are free)
   kSFree = kSFull + kGroups,          // [3] group -> QK issuer: S buffer read (4 warps)
   kRecvFull = kSFree + kGroups,       // [3] peer partial landed (expect_tx by one thread here)
-  kRecvFree = kRecvFull + kGroups,    // [3] peer -> here: its tile buffer i % 3 is free again
-  kMref = kRecvFree + kGroups,        // [3] group -> next group: reference maximum (128 threads)
-  kPvDone = kMref + kGroups,          // [3] PV issuer -> group: PV(i) done (its P read, O stable)
-  kPFull = kPvDone + kGroups,         // [3] group -> PV issuer: P(i) in its tile buffer (128 threads)
-  kQFull = kPFull + kGroups,
+  kRecvFree = kRecvFull + kGroups,    // [2] peer -> here: it has read our tile in its buffer i & 1
+  kFreeSeen = kRecvFree + 2,          // [3] group -> next group: past its kRecvFree wait (4 warps)
+  kSigSent = kFreeSeen + kGroups,     // [3] group -> next group: its "free" signal is out (4 warps)
+  kMref = kSigSent + kGroups,        // [3] group -> next group: reference maximum (128 threads)
+  kPvDone = kMref + kGroups,          // [3] PV issuer -> next group: P buffer free, O stable
+  kPFull = kPvDone + kGroups,         // group -> PV issuer: P(i) in shared memory (128 threads)
+  kQFull,
   kQReady,
   kDrain,
   kDrainPv,
@@ -207,19 +210,22 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_init(bar(kSFull + g), 1);
       mbar_init(bar(kSFree + g), kGroupWarps);
       mbar_init(bar(kRecvFull + g), 1);
-      mbar_init(bar(kRecvFree + g), 1);
+      mbar_init(bar(kFreeSeen + g), kGroupWarps);
+      mbar_init(bar(kSigSent + g), kGroupWarps);
       mbar_init(bar(kMref + g), kGroupThreads);
       mbar_init(bar(kPvDone + g), 1);
-      mbar_init(bar(kPFull + g), kGroupThreads);
     }
+    mbar_init(bar(kPFull), kGroupThreads);
     mbar_init(bar(kQFull), 1);
     mbar_init(bar(kQReady), 2 * kGroupThreads);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
+    mbar_init(bar(kRecvFree + 0), 1);
+    mbar_init(bar(kRecvFree + 1), 1);
     fence_mbar_init();
-    // The first wait on kRecvFree[g] is for tile g+3 (the peer has finished tile g).
-    for (int g = 0; g < kGroups; ++g)
-      if (g + kGroups < ntiles) mbar_arrive_expect_tx(bar(kRecvFree + g), 4 * kGroupWarps);
+    // The first waits on kRecvFree are for tiles 2 and 3 (the peer has read tiles 0, 1).
+    if (ntiles > 2) mbar_arrive_expect_tx(bar(kRecvFree + 0), 4 * kGroupWarps);
+    if (ntiles > 3) mbar_arrive_expect_tx(bar(kRecvFree + 1), 4 * kGroupWarps);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -337,60 +343,37 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     // a few tiles after the score ring fetched them (so from L2).  A stage of the score
     // ring is thus held only through the score MMAs, not through exchange and softmax.
     // V(i+1) is requested as soon as PV(i-1) has released its slot.  PV(i): O half +=
-    // P(i) . V(i), A = P (tile buffer i % 3, K-major), B = the V tile read MN-major
-    // (N = 256 latent columns over four 64-column boxes, K = 16 rows per step).
-    // Lane 0 waits and issues; on a tile with unreadable rows (the last of a split, or a
-    // bad page) the whole warp clears those rows of the landed V tile first, so that
-    // 0-weighted rows add exactly 0 (they may hold anything, even NaN).  Lane 0 never
-    // leaves the loop early, so the warp meets at every such tile.
-    const uint32_t id_pv = idesc_bf16(128, 256, false, true);
-    auto load_v = [&](int i) {
-      const int vs = i % kVStages;
-      const int y = tile_row(p, b, t0 + i * kN, false);
-      mbar_arrive_expect_tx(bar(kVFull + vs), kLatBytes);
-      for (int j = 0; j < 4; ++j)
-        tma_load_2d(s0 + kOffV + (uint32_t)vs * kLatBytes + j * kBoxBytes, &maps.kv_lat, bar(kVFull + vs),
-                    256 * (int)rank + 64 * j, y);
-    };
-    int v_issued = 0;
-    if (lane == 0)
+    // P(i) . V(i), A = P (smem, K-major), B = the V tile read MN-major (N = 256 latent
+    // columns over four 64-column boxes, K = 16 rows per step).
+    if (lane == 0) {
+      const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      auto load_v = [&](int i) {
+        const int vs = i % kVStages;
+        const int y = tile_row(p, b, t0 + i * kN, false);
+        mbar_arrive_expect_tx(bar(kVFull + vs), kLatBytes);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(s0 + kOffV + (uint32_t)vs * kLatBytes + j * kBoxBytes, &maps.kv_lat, bar(kVFull + vs),
+                      256 * (int)rank + 64 * j, y);
+      };
+      int v_issued = 0;
       for (; v_issued < min(kVStages, ntiles); ++v_issued) load_v(v_issued);
-    for (int i = 0; i < ntiles; ++i) {
-      const int vs = i % kVStages;
-      if (lane == 0 && !aborted) {
+      for (int i = 0; i < ntiles; ++i) {
+        const int vs = i % kVStages;
         if (i + 1 < ntiles && i + 1 >= kVStages) {
-          if (mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, kWaitNs)) {
-            load_v(i + 1);
-            ++v_issued;
-          } else {
+          if (!mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, kWaitNs)) {
             aborted = true;
+            break;
           }
+          load_v(i + 1);
+          ++v_issued;
         }
-        if (!aborted && (!mbar_wait(bar(kPFull + i % kGroups), (uint32_t)(i / kGroups) & 1u, kWaitNs) ||
-                         !mbar_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, kWaitNs)))
+        if (!mbar_wait(bar(kPFull), (uint32_t)i & 1u, kWaitNs) ||
+            !mbar_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, kWaitNs)) {
           aborted = true;
-      }
-      const int t = t0 + i * kN;
-      int valid = min(kN, t1 - t);
-      if (p.block_table) {
-        const int page = tile_page(p, b, t);
-        if (page < 0 || page >= p.num_pages) valid = 0;
-      }
-      if (valid < kN) {
-        if (__shfl_sync(0xffffffffu, aborted ? 0 : 1, 0)) {
-          const uint32_t vt = s0 + kOffV + (uint32_t)vs * kLatBytes;
-          for (int idx = lane; idx < (kN - valid) * 32; idx += 32) {
-            const int row = valid + idx / 32, c = idx % 32;   // 4 boxes x 8 chunks per row
-            st_shared_v4_zero(vt + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u + (uint32_t)(c & 7) * 16u);
-          }
-          fence_proxy_async_smem();
+          break;
         }
-        __syncwarp();
-      }
-      if (lane == 0 && !aborted) {
         tc_fence_after();
-        const uint64_t pd =
-            smem_desc(s0 + kOffTileBuf + (uint32_t)(i % kGroups) * kTileBufBytes, 16, 1024, kSwizzle128B);
+        const uint64_t pd = smem_desc(s0 + kOffP, 16, 1024, kSwizzle128B);
         const uint64_t vd = smem_desc(s0 + kOffV + (uint32_t)vs * kLatBytes, 8192, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < kN / 16; ++k)
@@ -398,8 +381,6 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         mma_commit(bar(kVEmpty + vs));
         mma_commit(bar(kPvDone + i % kGroups));
       }
-    }
-    if (lane == 0) {
       mma_commit(bar(kDrainPv));
       mbar_wait(bar(kDrainPv), 0, kWaitNs);
       for (int i = max(0, v_issued - kVStages); i < v_issued; ++i)
@@ -411,26 +392,20 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     // quarter w % 4 (heads 32q..32q+31, one head per lane).  Per tile: own fp32 partial
     // scores out of TMEM, a bf16 copy to the peer, the peer's bf16 partial in, the row
     // maximum, the reference maximum (handed on from the group of tile i-1), P = 2^(s -
-    // m_ref) into the tile's buffer, and the running output rescaled when m_ref moves.
-    // Each group keeps its own share of the row sum; the shares are merged at the end.
-    //
-    // Tile buffer g (16 KB, one per group) holds the peer's partial of tile i, then P(i)
-    // in place (each warp's 32 rows of P take the same 4 KB as its quarter of the
-    // partial), until PV(i) has read it; then the group tells the peer, with one 4-byte
-    // st.async per warp counted on the peer's kRecvFree[g], that it may send tile i+3.
-    // Consecutive tiles never share a P buffer, so a P is written without waiting for the
-    // PV before it (only a rescale of O waits for it).
+    // m_ref) into shared memory, and the running output rescaled when m_ref moves.  Each
+    // group keeps its own share of the row sum; the shares are merged at the end.
     const int g = (warp - 2) / kGroupWarps;
     const int quarter = warp & 3;
     const int h = 32 * quarter + lane;               // head row == TMEM lane
+    const int gtid = tid - 32 * (2 + g * kGroupWarps);
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const bool head_ok = h < p.H;
     const int64_t qrow = (int64_t)m * p.H + h;
     const uint32_t xoff = (uint32_t)quarter * kQuarterXBytes + (uint32_t)lane * 16u;
-    const uint32_t tbuf = s0 + kOffTileBuf + (uint32_t)g * kTileBufBytes;
-    const uint32_t tbuf_peer = map_to_rank(tbuf, peer);
+    const uint32_t recv_local = s0 + kOffRecv;
+    const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t recv_bar_peer = map_to_rank(bar(kRecvFull + g), peer);
-    const uint32_t free_bar_peer = map_to_rank(bar(kRecvFree + g), peer);
+    const uint32_t free_bar_peer = map_to_rank(bar(kRecvFree), peer);
     const uint32_t sig_peer = map_to_rank(s0 + kOffSig + 4u * (uint32_t)quarter, peer);
     float* mref_sh = reinterpret_cast<float*>(smem + kOffMref);
     if (g < 2) {
@@ -459,7 +434,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
     for (int i = g; i < ntiles && !aborted; i += kGroups) {
       const uint32_t ph = (uint32_t)(i / kGroups) & 1u;
-      const uint32_t sb = (uint32_t)(i & 1);          // S buffer
+      const uint32_t sb = (uint32_t)(i & 1);          // S buffer and receive buffer
       if (!warp_wait(bar(kSFull + g), ph)) {
         aborted = true;
         break;
@@ -477,17 +452,26 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kSFree + g));
       // To the peer: [4 quarters][8 chunks][32 rows][16 B], chunk k = columns 8k..8k+7, into
-      // its tile buffer g, once the peer is done with tile i-3 there.  This group waits for
-      // every phase of kRecvFree[g] in turn.
-      if (i >= kGroups) {
-        if (!warp_wait_cluster(bar(kRecvFree + g), (uint32_t)((i - kGroups) / kGroups) & 1u)) {
+      // its receive buffer i & 1, once the peer has read tile i-2 out of it: each of its 4
+      // warps then sends a 4-byte st.async counted on our kRecvFree[i & 1] (a remote
+      // mbarrier arrive is far slower under load).  The groups pass this wait in tile order
+      // (kFreeSeen), so each phase of kRecvFree[i & 1] is awaited after the one before it.
+      if (i >= 1 && !warp_wait(bar(kFreeSeen + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+        aborted = true;
+        break;
+      }
+      if (i >= 2) {
+        if (!warp_wait_cluster(bar(kRecvFree + sb), (uint32_t)((i - 2) >> 1) & 1u)) {
           aborted = true;
           break;
         }
-        if (h == 0 && i + kGroups < ntiles) mbar_arrive_expect_tx(bar(kRecvFree + g), 4 * kGroupWarps);
+        // Re-arm for the wait of tile i+2 (the peer's read of tile i).
+        if (h == 0 && i + 2 < ntiles) mbar_arrive_expect_tx(bar(kRecvFree + sb), 4 * kGroupWarps);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kFreeSeen + g));
       {
-        const uint32_t dst = tbuf_peer + xoff;
+        const uint32_t dst = recv_peer + sb * kRecvBytes + xoff;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_async_v4(dst + (uint32_t)c * 512u, f2_to_bf2(x[8 * c], x[8 * c + 1]),
@@ -498,15 +482,35 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         aborted = true;
         break;
       }
-      // Re-arm for tile i+3: the peer sends it only after our "free" signal for tile i,
-      // which follows this phase.
+      // Re-arm for tile i+3 (its bytes can only come after the phase of tile i completed:
+      // the peer sends tile i+3 after our "free" signal for tile i+1).
       if (h == 0 && i + kGroups < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + g), kRecvBytes);
       {
-        const uint32_t rl = tbuf + xoff;
+        const uint32_t rl = recv_local + sb * kRecvBytes + xoff;
+        uint4 w[8];
+        uint32_t sig = 0;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 w = ld_shared_u4(rl + (uint32_t)c * 512u);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+          w[c] = ld_shared_u4(rl + (uint32_t)c * 512u);
+          sig ^= w[c].x;
+        }
+        // Every lane's loads have returned (sig depends on them) before lane 0 tells the
+        // peer that buffer i & 1 may be overwritten (by tile i+2, if there is one).  The
+        // signals go out in tile order (kSigSent): the peer sends tile i+3, which lands on
+        // kRecvFull of this group, only after our signal for tile i+1, hence after this
+        // group's phase of tile i has completed and been read.
+        asm volatile("" ::"r"(sig));
+        if (i >= 1 && !warp_wait(bar(kSigSent + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+          aborted = true;
+          break;
+        }
+        if (lane == 0) {
+          if (i + 2 < ntiles) st_async_b32(sig_peer, sig, free_bar_peer + 8u * sb);
+          mbar_arrive(bar(kSigSent + g));
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
@@ -549,14 +553,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       const bool grow = mx > m_prev + kRescaleThreshold;
       const float m_new = grow ? mx : m_prev;
-      // A warp that moves its reference rescales its rows of O, which needs PV(i-1) done;
-      // it hands the new reference on only after that wait, so that the group of tile
-      // i-1 cannot have finished a later tile (PV(i+2)) before the wait looks at the phase.
-      const bool rescale = __any_sync(0xffffffffu, grow && i > 0);
-      if (!rescale) {
-        mref_sh[h] = m_new;
-        mbar_arrive(bar(kMref + g));
-      }
+      mref_sh[h] = m_new;
+      mbar_arrive(bar(kMref + g));
       const float alpha = grow ? ex2_approx(m_prev - m_new) : 1.f;   // 0 when m_prev = -inf
       if (m_g != m_new) {
         l_g *= ex2_approx(m_g - m_new);
@@ -575,21 +573,20 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         pw[j] = f2_to_bf2(a, d);
       }
       l_g += ps;
-      // P(i) over this warp's quarter of the tile buffer: every lane has read its part of
-      // the peer's partial (the adds above consumed it) before any lane overwrites it.
-      __syncwarp();
+      // The P buffer is free, and O stable, once PV(i-1) is done.
+      if (i >= 1 && !warp_wait(bar(kPvDone + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+        aborted = true;
+        break;
+      }
       {
-        const uint32_t prow = s0 + kOffTileBuf + (uint32_t)g * kTileBufBytes + (uint32_t)h * 128u;
+        const uint32_t prow = s0 + kOffP + (uint32_t)h * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)   // 128B swizzle: 16-byte chunk c of row h sits at chunk c ^ (h & 7)
           st_shared_u4(prow + (uint32_t)((c ^ (h & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2],
                        pw[4 * c + 3]);
       }
-      if (rescale) {
-        if (!warp_wait(bar(kPvDone + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
-          aborted = true;
-          break;
-        }
+      // Rescale this warp's rows of O to the new reference (PV(i-1) has landed).
+      if (__any_sync(0xffffffffu, grow && i > 0)) {
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
@@ -603,36 +600,42 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         }
         tmem_st_wait();
         tc_fence_before();
-        mref_sh[h] = m_new;
-        mbar_arrive(bar(kMref + g));
+      }
+      // Rows past the readable range may hold anything (even NaN): clear them in the
+      // re-read V tile so that 0-weighted rows add exactly 0.
+      if (valid < kN) {
+        const int vs = i % kVStages;
+        if (!warp_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u)) {
+          aborted = true;
+          break;
+        }
+        const uint32_t vt = s0 + kOffV + (uint32_t)vs * kLatBytes;
+        const int nrow = kN - valid;
+        for (int idx = gtid; idx < nrow * 32; idx += kGroupThreads) {
+          const int row = valid + idx / 32, c = idx % 32;   // 4 boxes x 8 chunks per row
+          st_shared_v4_zero(vt + (uint32_t)(c >> 3) * kBoxBytes + (uint32_t)row * 128u + (uint32_t)(c & 7) * 16u);
+        }
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(kPFull + g));
-      // Once PV(i) has read P(i), the tile buffer may take the peer's tile i+3.
-      if (!warp_wait(bar(kPvDone + g), ph)) {
-        aborted = true;
-        break;
-      }
-      if (lane == 0 && i + kGroups < ntiles) st_async_b32(sig_peer, (uint32_t)i, free_bar_peer);
+      mbar_arrive(bar(kPFull));
     }
 
-    // Epilogue.  Once the last PV is done (every tile buffer is idle, and O is final), the
-    // groups' row-sum shares, each moved to the final reference maximum, are summed through
-    // a tile buffer; then each group writes its column chunks c = g, g+3, g+6 of the O half
-    // divided by the sum.
-    if (!aborted) {
-      const int last = ntiles - 1;
-      if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u)) aborted = true;
-    }
+    // Epilogue.  The groups' row-sum shares, each moved to the final reference maximum,
+    // are summed through shared memory (the receive buffers are idle now); then each
+    // group writes its columns chunks c = g, g+3, g+6 of the O half divided by the sum.
     named_bar_sync(1, kGroups * kGroupThreads);
     const float m_fin = mref_sh[h];
-    float* lsh = reinterpret_cast<float*>(smem + kOffTileBuf);
+    float* lsh = reinterpret_cast<float*>(smem + kOffRecv);
     lsh[g * 128 + h] = (l_g > 0.f) ? l_g * ex2_approx(m_g - m_fin) : 0.f;
     named_bar_sync(1, kGroups * kGroupThreads);
     const float l = lsh[h] + lsh[128 + h] + lsh[256 + h];
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
     float* out = p.o_out + orow * kDc + 256 * rank;
     const bool have = !aborted && l > 0.f;
+    if (!aborted) {
+      const int last = ntiles - 1;
+      if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u)) aborted = true;
+    }
     tc_fence_after();
     const float inv = have ? 1.f / l : 0.f;
 #pragma unroll 1
