@@ -57,6 +57,22 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of `x` over all ranks: a job takes as long as its slowest rank.  Uses the
+    initialised process group (NCCL on GPUs: pass the rank's device; gloo: the CPU)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_step, ms_per_step):
+    """Units per second over the whole job: every rank processes `units_per_step` per step."""
+    return world * units_per_step / (ms_per_step / 1e3)
+
+
 def algorithmic(case):
     """Bytes and FLOPs of one latent-attention launch, by definition (no overheads)."""
     pairs = 0
@@ -417,10 +433,7 @@ def main():
             cudart.cudaEventDestroy(b)
     else:
         dec_ms = [a.elapsed_time(b) for a, b in dec_events]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     status = int(step.status.item())
     clock_info = clocks.stop()
 
@@ -448,15 +461,12 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     ms_per_step = total_ms / args.steps
     tokens_per_step = case.B * case.S
-    value = world * tokens_per_step / (ms_per_step / 1e3)
-    e2e_value = world * tokens_per_step / (e2e_ms / args.steps / 1e3)
+    value = whole_job_rate(world, tokens_per_step, ms_per_step)
+    e2e_value = whole_job_rate(world, tokens_per_step, e2e_ms / args.steps)
 
     cache_b, alg_b, flops = algorithmic(case)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()

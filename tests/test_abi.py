@@ -86,3 +86,35 @@ def test_other_calls_reject_bad_arguments(lib):
     assert lib.mla_rope_inplace(P, 576, 10, 512, None, 1e4, None) == 1
     assert lib.mla_rope_inplace(P, 576, 10, 520, P, 1e4, None) == 1
     assert lib.mla_rope_inplace(P, 576, 10, 511, P, 1e4, None) == 1
+
+
+# ----------------------------------------------------------------------------
+# Split planner (host logic; without a GPU it assumes 148 SMs, as on a B300)
+# ----------------------------------------------------------------------------
+
+def test_planner_invariants(lib):
+    for B, S, H, T in [(1, 1, 128, 1), (4, 1, 16, 256), (64, 1, 128, 4096), (2, 1, 128, 131072),
+                       (128, 2, 128, 8192), (1, 1, 128, 10 ** 6), (300, 1, 128, 64)]:
+        s = mla.mla_decode_num_splits(B, S, H, T)
+        assert 1 <= s <= 128                      # MLA_MAX_SPLITS
+        assert s <= -(-T // 64)                   # never more splits than 64-row tiles
+    assert mla.mla_decode_num_splits(8, 1, 128, 0) == 1
+
+
+@pytest.mark.parametrize("name,expected", [("tiny", 4), ("dsv3", 1), ("ragged_paged", 12),
+                                           ("long_splitkv", 36), ("mtp", 2)])
+def test_planner_choices_for_the_workloads(lib, name, expected):
+    # The counts the measured results were taken with: a full machine of CTA pairs is
+    # left unsplit; long or ragged batches are split to fill waves of 74 pairs.
+    from mla_latent_kv_70_b300 import inputs as I
+    c = getattr(I, name)()
+    assert mla.mla_decode_num_splits(c.B, c.S, c.H, max(c.seqlens), c.total_tokens) == expected
+
+
+def test_planner_uses_the_total_row_hint(lib):
+    # Without the hint the planner assumes every sequence is max_seqlen long; a ragged
+    # batch (about half that on average) fills fewer waves and is split more.
+    from mla_latent_kv_70_b300 import inputs as I
+    c = I.ragged_paged()
+    T = max(c.seqlens)
+    assert mla.mla_decode_num_splits(c.B, 1, 128, T, c.total_tokens) > mla.mla_decode_num_splits(c.B, 1, 128, T)
