@@ -272,7 +272,7 @@ def blas_threads():
     return len(os.sched_getaffinity(0))
 
 
-def cpu_baseline(case, min_seconds=5.0, max_seqs=None):
+def cpu_baseline(case, min_seconds=10.0, max_seqs=None):
     """Time the fp64 oracle (as it stands) over whole sequences of the workload."""
     import numpy as np  # noqa: F401
     import oracle as O
