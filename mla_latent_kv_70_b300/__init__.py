@@ -65,11 +65,19 @@ def lib() -> ctypes.CDLL:
     return _LIB
 
 
-def _ptr(t):
+_BF16, _F32, _I32 = torch.bfloat16, torch.float32, torch.int32
+
+
+def _ptr(t, dtype=None):
+    """Device address of tensor `t` (None -> NULL; an int passes through as an address).
+    The library reads each buffer with the element type its header states, so a tensor of
+    another dtype is refused here rather than misread."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"libmla expects a {dtype} tensor here, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError("libmla takes device tensors")
     if not t.is_contiguous():
@@ -100,8 +108,8 @@ def mla_absorb_q(q_nope, q_rope, w_uk, q_pos, rope_theta, q_cat, stream=None):
     """q_cat[b,s,h] = [q_nope[b,s,h] . W_UK[h]^T | RoPE(q_rope[b,s,h], q_pos[b,s])]."""
     B, S, H, _ = q_nope.shape
     _check("mla_absorb_q", lib().mla_absorb_q(
-        _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(q_pos), float(rope_theta), B, S, H,
-        _ptr(q_cat), _stream(stream)))
+        _ptr(q_nope, _BF16), _ptr(q_rope, _BF16), _ptr(w_uk, _BF16), _ptr(q_pos, _I32),
+        float(rope_theta), B, S, H, _ptr(q_cat, _BF16), _stream(stream)))
 
 
 def mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen) -> int:
@@ -124,10 +132,10 @@ def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, bloc
         kv_seq_stride = kv_seq_stride or kv.shape[1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("mla_decode_latent", lib().mla_decode_latent(
-        _ptr(q_cat), _ptr(kv), int(kv_seq_stride), _ptr(seqlens), _ptr(block_table), max_pages,
-        page_size, num_pages, B, S, H, int(bool(causal)), float(scale), int(num_splits),
-        int(max_seqlen), _ptr(o_lat), _ptr(lse), _ptr(workspace), ws_bytes, _ptr(status),
-        _stream(stream)))
+        _ptr(q_cat, _BF16), _ptr(kv, _BF16), int(kv_seq_stride), _ptr(seqlens, _I32),
+        _ptr(block_table, _I32), max_pages, page_size, num_pages, B, S, H, int(bool(causal)),
+        float(scale), int(num_splits), int(max_seqlen), _ptr(o_lat, _F32), _ptr(lse, _F32),
+        _ptr(workspace), ws_bytes, _ptr(status, _I32), _stream(stream)))
 
 
 def mla_decode_latent_noalloc(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen,
@@ -142,27 +150,29 @@ def mla_decode_latent_noalloc(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seql
         num_pages, max_pages = 0, 0
         kv_seq_stride = kv_seq_stride or kv.shape[1]
     _check("mla_decode_latent_noalloc", lib().mla_decode_latent_noalloc(
-        _ptr(q_cat), _ptr(kv), int(kv_seq_stride), _ptr(seqlens), _ptr(block_table), max_pages,
-        page_size, num_pages, B, S, H, int(bool(causal)), float(scale), int(num_splits),
-        int(max_seqlen), _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
+        _ptr(q_cat, _BF16), _ptr(kv, _BF16), int(kv_seq_stride), _ptr(seqlens, _I32),
+        _ptr(block_table, _I32), max_pages, page_size, num_pages, B, S, H, int(bool(causal)),
+        float(scale), int(num_splits), int(max_seqlen), _ptr(o_lat, _F32), _ptr(lse, _F32),
+        _ptr(status, _I32), _stream(stream)))
 
 
 def mla_combine_partials(o_part, lse_part, o_lat, lse, stream=None):
     splits = o_part.shape[0]
     rows = lse_part.numel() // splits
     _check("mla_combine_partials", lib().mla_combine_partials(
-        _ptr(o_part), _ptr(lse_part), splits, rows, _ptr(o_lat), _ptr(lse), _stream(stream)))
+        _ptr(o_part, _F32), _ptr(lse_part, _F32), splits, rows, _ptr(o_lat, _F32), _ptr(lse, _F32),
+        _stream(stream)))
 
 
 def mla_out_proj_uv(o_lat, w_uv, o, stream=None):
     B, S, H, _ = o_lat.shape
-    _check("mla_out_proj_uv", lib().mla_out_proj_uv(_ptr(o_lat), _ptr(w_uv), B, S, H, _ptr(o),
-                                                    _stream(stream)))
+    _check("mla_out_proj_uv", lib().mla_out_proj_uv(_ptr(o_lat, _F32), _ptr(w_uv, _BF16), B, S, H,
+                                                    _ptr(o, _F32), _stream(stream)))
 
 
 def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):
-    _check("mla_rope_inplace", lib().mla_rope_inplace(_ptr(x), int(row_stride), int(rows),
-                                                      int(col_offset), _ptr(pos), float(theta),
+    _check("mla_rope_inplace", lib().mla_rope_inplace(_ptr(x, _BF16), int(row_stride), int(rows),
+                                                      int(col_offset), _ptr(pos, _I32), float(theta),
                                                       _stream(stream)))
 
 

@@ -118,3 +118,22 @@ def test_planner_uses_the_total_row_hint(lib):
     c = I.ragged_paged()
     T = max(c.seqlens)
     assert mla.mla_decode_num_splits(c.B, 1, 128, T, c.total_tokens) > mla.mla_decode_num_splits(c.B, 1, 128, T)
+
+
+def test_binding_refuses_wrong_dtypes(lib):
+    # The binding checks each tensor's element type (the library would misread it) before
+    # its device; these CPU tensors stop at the first check that applies.
+    import torch
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    q32 = torch.zeros(2, 1, 16, 128, dtype=torch.float32)
+    with pytest.raises(ValueError, match="bfloat16"):
+        mla.mla_absorb_q(q32, bf(2, 1, 16, 64), bf(16, 512, 128), None, 1e4, bf(2, 1, 16, 576))
+    with pytest.raises(ValueError, match="bfloat16"):
+        mla.mla_decode_latent(torch.zeros(2, 1, 16, 576), bf(2, 64, 576), torch.zeros(2, dtype=torch.int32),
+                              torch.zeros(2, 1, 16, 512), torch.zeros(2, 1, 16), scale=0.07, max_seqlen=64)
+    with pytest.raises(ValueError, match="int32"):
+        mla.mla_rope_inplace(17, 576, 1, 512, torch.zeros(1, dtype=torch.int64), 1e4)
+    with pytest.raises(ValueError, match="float32"):
+        mla.mla_out_proj_uv(bf(2, 1, 16, 512), bf(16, 512, 128), torch.zeros(2, 1, 16, 128))
+    with pytest.raises(ValueError, match="device tensors"):   # right dtypes, host memory
+        mla.mla_out_proj_uv(torch.zeros(2, 1, 16, 512), bf(16, 512, 128), torch.zeros(2, 1, 16, 128))
