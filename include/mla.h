@@ -20,9 +20,13 @@
  *   - H (heads) must be a multiple of 16 and at most 128; S (query tokens per
  *     sequence) is 1..4; B >= 1.
  *   - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte aligned.
- *     The caller owns every buffer; the library allocates no device memory and
- *     keeps no state between calls apart from per-device constants (SM count,
- *     driver entry points) it looks up once.
+ *     The caller owns every buffer; no call allocates device memory.  Between calls
+ *     the library keeps only what it looks up once per device (SM count, the kernels'
+ *     shared-memory opt-in, the scratch address of mla_decode_latent_noalloc) and the
+ *     driver entry point it looks up once per process; these look-ups are safe from
+ *     several host threads and devices.  Every device that loads the library also
+ *     holds the fixed MLA_NOALLOC_SCRATCH_BYTES array that only
+ *     mla_decode_latent_noalloc uses.
  *   - bf16 values are passed as raw 16-bit patterns (mla_bf16).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  The return value reports host-side argument checks and launch
@@ -32,6 +36,15 @@
  *     caller passes one; the affected rows are skipped, never read out of bounds.
  *   - Argument checks run before any CUDA call, so a rejected call never touches
  *     the GPU.
+ *   - The kernels are launched with programmatic dependent launch: each may start
+ *     while the previous kernel on the stream is still running, and waits for it
+ *     before reading what that kernel writes (q_cat, o_lat, partials).  The latent
+ *     decode reads seqlens, block_table and its first cache rows BEFORE that wait.
+ *     So the cache rows, seqlens and block_table of a decode must not be written by
+ *     the kernel issued just before it on the stream if that kernel lets its
+ *     dependents start early (griddepcontrol.launch_dependents); an ordinary
+ *     kernel, a copy, or mla_append_latent / mla_rope_inplace (which do not) are
+ *     safe.
  */
 #ifndef MLA_H
 #define MLA_H
@@ -215,11 +228,28 @@ mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int 
  * `rows` rows (row r starts at x + r*row_stride elements) by position pos[r]:
  * interleaved pairs (2i, 2i+1) turn by pos * theta^(-2i/64) ([MLA] "구현").  Used to
  * put k^R of cache rows at their positions when they are written
- * ([ANATOMY] section 2: the cached k^R carries RoPE).  The angle is reduced in
- * double precision; the rotation runs in fp32 and is stored as bf16.
+ * ([ANATOMY] section 2: the cached k^R carries RoPE).  The angle pos * theta^(-2i/64)
+ * is reduced modulo 2 pi in fp32 with two-term arithmetic (within about 1e-6 rad for
+ * positions 0 <= pos < 2^24, the range this call and mla_absorb_q accept for exact
+ * angles); the rotation runs in fp32 and is stored as bf16.
  */
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream);
+
+/*
+ * mla_debug_inject_timeout -- test hook for the device-side failure path (not a step of
+ * the method).  For the kernels named in `kernels` (bit 0: the latent decode, bit 1: the
+ * key absorption, bit 2: the W_UV projection; 0 turns the hook off) every later launch
+ * from this process shortens its mbarrier wait limit from 2 s to `wait_ms` and withholds
+ * one completion signal of its own (the decode: the score MMAs of each unit's first tile;
+ * the projections: the copy of one weight chunk).  A wait then runs out: the kernel
+ * records MLA_ERR_TIMEOUT in *status_dev (the decode; the projections write NaN), waits
+ * for its own copies and MMAs, frees its tensor memory and exits.  Nothing faults and the
+ * device stays usable; results of the affected calls are documented above (the decode
+ * writes o_lat = 0 and lse = -inf for the units that gave up).  Process-wide; returns
+ * MLA_ERR_INVALID for unknown bits or wait_ms outside (0, 2000].
+ */
+mla_status mla_debug_inject_timeout(int kernels, double wait_ms);
 
 #ifdef __cplusplus
 }

@@ -39,6 +39,7 @@ SIGNATURES = {
     "mla_combine_partials": (_I, [_P, _P, _I, _I64, _P, _P, _P]),
     "mla_out_proj_uv": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "mla_rope_inplace": (_I, [_P, _I64, _I64, _I, _P, _F, _P]),
+    "mla_debug_inject_timeout": (_I, [_I, ctypes.c_double]),
 }
 
 _LIB = None
@@ -174,6 +175,15 @@ def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):
     _check("mla_rope_inplace", lib().mla_rope_inplace(_ptr(x, _BF16), int(row_stride), int(rows),
                                                       int(col_offset), _ptr(pos, _I32), float(theta),
                                                       _stream(stream)))
+
+
+FAULT_DECODE, FAULT_ABSORB, FAULT_OUT_PROJ = 1, 2, 4
+
+
+def mla_debug_inject_timeout(kernels: int, wait_ms: float = 1.0) -> None:
+    """Test hook: the named kernels shorten their waits to `wait_ms` and withhold one
+    completion signal, so that a bounded wait runs out (0 turns it off); see mla.h."""
+    _check("mla_debug_inject_timeout", lib().mla_debug_inject_timeout(int(kernels), float(wait_ms)))
 
 
 from .pipeline import DecodeStep  # noqa: E402,F401

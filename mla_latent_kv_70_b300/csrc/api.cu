@@ -14,20 +14,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool heads_ok(int H) { return H >= 16 && H <= 128 && H % 16 == 0; }
 
-int sm_count_cached() {
-  static int count = -1;
-  if (count < 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-    count = n;
-  }
-  return count;
-}
-
 // Split count for the CTA-pair decode: each non-empty (query token, split) unit occupies
 // two SMs.  A split is a chunk of C = ceil(max_seqlen / s) rows (rounded to 64), so the
 // run takes about waves(s) x C row-times, where waves(s) = ceil(units / pair slots) and
@@ -69,6 +55,26 @@ mla_status launch_status(cudaError_t e) {
 
 }  // namespace
 
+mla_status mla::check_decode_args(const void* q_cat, const void* kv, int64_t kv_seq_stride,
+                                  const int32_t* seqlens, const int32_t* block_table, int max_pages,
+                                  int page_size, int num_pages, int B, int S, int H, float scale,
+                                  int num_splits, int max_seqlen, const float* o_lat, const float* lse) {
+  if (!q_cat || !kv || !seqlens || !o_lat || !lse) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1 || max_seqlen < 0) return MLA_ERR_INVALID;
+  if (!aligned16(q_cat) || !aligned16(kv) || !aligned16(o_lat)) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4) return MLA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
+  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID;
+  if (block_table) {
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID;
+    if ((int64_t)max_pages * kPage < max_seqlen) return MLA_ERR_INVALID;
+  } else {
+    if (kv_seq_stride < max_seqlen || kv_seq_stride < 0) return MLA_ERR_INVALID;
+  }
+  return MLA_OK;
+}
+
 extern "C" {
 
 const char* mla_status_string(int status) {
@@ -84,7 +90,7 @@ const char* mla_status_string(int status) {
   }
 }
 
-int mla_device_sm_count(void) { return sm_count_cached(); }
+int mla_device_sm_count(void) { return mla::device_sm_count(); }
 
 mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* w_uk,
                         const int32_t* q_pos, float rope_theta, int B, int S, int H,
@@ -104,7 +110,7 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const ml
 
 int mla_decode_num_splits(int B, int S, int H, int max_seqlen, int64_t total_rows) {
   if (B < 1 || S < 1 || max_seqlen < 0) return 1;
-  return auto_splits(B, S, H, max_seqlen, total_rows, sm_count_cached());
+  return auto_splits(B, S, H, max_seqlen, total_rows, mla::device_sm_count());
 }
 
 size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen) {
@@ -121,19 +127,10 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
                              float scale, int num_splits, int max_seqlen, float* o_lat,
                              float* lse, void* workspace, size_t workspace_bytes,
                              int32_t* status_dev, mla_stream stream) {
-  if (!q_cat || !kv || !seqlens || !o_lat || !lse) return MLA_ERR_INVALID;
-  if (B < 1 || S < 1 || H < 1 || max_seqlen < 0) return MLA_ERR_INVALID;
-  if (!aligned16(q_cat) || !aligned16(kv) || !aligned16(o_lat)) return MLA_ERR_INVALID;
-  if (!heads_ok(H) || S > 4) return MLA_ERR_UNSUPPORTED;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
-  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID;
-  if (block_table) {
-    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
-    if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID;
-    if ((int64_t)max_pages * kPage < max_seqlen) return MLA_ERR_INVALID;
-  } else {
-    if (kv_seq_stride < max_seqlen || kv_seq_stride < 0) return MLA_ERR_INVALID;
-  }
+  const mla_status bad = mla::check_decode_args(q_cat, kv, kv_seq_stride, seqlens, block_table,
+                                                max_pages, page_size, num_pages, B, S, H, scale,
+                                                num_splits, max_seqlen, o_lat, lse);
+  if (bad != MLA_OK) return bad;
   const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen, 0);
   const size_t need = mla_decode_workspace_bytes(B, S, H, splits, max_seqlen);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))

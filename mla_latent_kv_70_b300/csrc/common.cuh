@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "mla.h"
@@ -40,22 +41,46 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Inverse RoPE frequencies theta^(-2i/64), i = 0..31, computed on the host in double.
+// Inverse RoPE frequencies theta^(-2i/64), i = 0..31, computed on the host in double and
+// carried as two fp32 terms: hi = fp32(f), lo = fp32(f - hi).
 struct RopeFreqs {
-  double inv_freq[kDr / 2];
+  float hi[kDr / 2];
+  float lo[kDr / 2];
 };
 RopeFreqs make_rope_freqs(float theta);
 
-// Rotate one interleaved pair by pos * inv_freq: the angle is formed and reduced to
-// [-pi, pi] in double, the rotation itself runs in fp32.
-__device__ __forceinline__ float2 rope_pair(float x0, float x1, int pos, double inv_freq) {
-  const double two_pi = 6.283185307179586476925286766559;
-  double a = (double)pos * inv_freq;
-  a -= two_pi * rint(a / two_pi);
+// Rotate one interleaved pair by the angle pos * f, reduced to about [-pi, pi] in fp32
+// without losing the angle's low bits (fp64 is slow on this GPU): pos * f is carried as
+// two terms (the product's exact rounding error from an FMA, plus pos * f_lo), and 2 pi is
+// subtracted Cody-Waite style with a two-term 2 pi, whose first step is exact (for
+// positions below 2^24 both terms are multiples of 2^-22 below 2^24 units).  The
+// reduced angle is within about 1e-6 rad of pos * f mod 2 pi.
+__device__ __forceinline__ float2 rope_pair(float x0, float x1, int pos, float f_hi, float f_lo) {
+  constexpr float kTwoPiHi = 6.2831854820251465f;      // fp32(2 pi)
+  constexpr float kTwoPiLo = -1.7484555314695172e-07f; // 2 pi - kTwoPiHi
+  constexpr float kInvTwoPi = 0.15915493667125702f;
+  const float p = (float)pos;
+  const float a_hi = p * f_hi;
+  const float a_lo = fmaf(p, f_lo, fmaf(p, f_hi, -a_hi));
+  const float k = rintf(a_hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiHi, a_hi);
+  r = fmaf(-k, kTwoPiLo, r) + a_lo;
   float s, c;
-  sincosf((float)a, &s, &c);
+  sincosf(r, &s, &c);
   return make_float2(x0 * c - x1 * s, x0 * s + x1 * c);
 }
+
+// Bounded waits.  Every mbarrier wait of the kernels gives up after wait_ns (2 s unless
+// the test hook mla_debug_inject_timeout shortened it); a kernel told to withhold one
+// completion signal (`fault`) makes one of its own waits run out, to exercise the abort
+// path without faulting anything.
+enum : int { kFaultDecode = 1, kFaultAbsorb = 2, kFaultOutProj = 4 };
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+struct WaitConfig {
+  uint64_t wait_ns;
+  int fault;   // 1: withhold the signal, 0: run normally
+};
+WaitConfig wait_config(int kernel_bit);   // device_state.cu
 
 // ---------------------------------------------------------------------------
 // Decode: per-launch parameters shared by the host planner and the kernel.
@@ -76,6 +101,8 @@ struct DecodeParams {
   float* o_out;                // o_lat [B,S,H,512] (1 split) or partials [splits,B,S,H,512]
   float* lse_out;              // lse [B,S,H] or partials [splits,B,S,H]
   int32_t* status;
+  uint64_t wait_ns;            // limit of every mbarrier wait
+  int fault;                   // 1: the score issuer withholds the completion of tile 0
 };
 
 // Rows [t0, t1) of sequence b that split `split` covers for query token s.  Splits are
@@ -119,6 +146,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Per-device host state (device_state.cu).  Devices are numbered below kMaxDevices.
+constexpr int kMaxDevices = 64;
+int current_device();          // the calling thread's current device, -1 if unusable
+int device_sm_count();         // SMs of the current device, 0 if unusable
+// One kernel's opt-in to `bytes` of dynamic shared memory, made once per device.
+struct SmemOptIn {
+  std::atomic<bool> done[kMaxDevices];
+};
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes, SmemOptIn& opt);
+
+// The host-side argument checks of mla_decode_latent other than the workspace (api.cu);
+// they make no CUDA call.
+mla_status check_decode_args(const void* q_cat, const void* kv, int64_t kv_seq_stride,
+                             const int32_t* seqlens, const int32_t* block_table, int max_pages,
+                             int page_size, int num_pages, int B, int S, int H, float scale,
+                             int num_splits, int max_seqlen, const float* o_lat, const float* lse);
+
 // Launchers (defined next to their kernels).
 cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_rope,
                             const __nv_bfloat16* w_uk, const int32_t* q_pos, const RopeFreqs& f,
@@ -130,6 +174,6 @@ cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t ro
                                 cudaStream_t st);
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
                            float* o, float* lse, cudaStream_t st);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode(DecodeParams p, cudaStream_t st);
 
 }  // namespace mla

@@ -17,15 +17,15 @@
 //     of every cache row; its TMA loads only those (each cache byte is read once);
 //   * each CTA computes the partial score over its 288 columns into TMEM (A operand =
 //     its half of q~, held in TMEM; the rope half of q from shared memory);
-//   * the partials are swapped through distributed shared memory as bf16, by 16-byte
-//     st.async into the peer's receive buffer (two, by tile parity), counted (complete_tx)
-//     on its mbarrier.  A buffer is reused for tile i+2 once the peer has read tile i out
-//     of it; the peer says so with a 4-byte st.async counted on our "free" barrier (about
-//     500 cycles under HBM load, where a remote mbarrier.arrive.release took ~3900).
-//     bf16 halves the bytes of fp32 partials and adds an error of the same order as
-//     storing q~ in bf16 (2^-8 of the partial sum).  Each CTA adds its own fp32 partial to
-//     the peer's bf16 partial and normalises its half of O with its own softmax sums, so
-//     the two halves need not agree bit for bit;
+//   * the partials are swapped through distributed shared memory as fp16 (saturating at
+//     +-65504), by 16-byte st.async into the peer's receive buffer (two, by tile parity),
+//     counted (complete_tx) on its mbarrier.  A buffer is reused for tile i+2 once the
+//     peer has read tile i out of it; the peer says so with a 4-byte st.async counted on
+//     our "free" barrier (about 500 cycles under HBM load, where a remote
+//     mbarrier.arrive.release took ~3900).  fp16 halves the bytes of fp32 partials and
+//     rounds a partial by at most 2^-11 of its magnitude (bf16 would round by 2^-8).
+//     Each CTA adds its own fp32 partial to the peer's fp16 partial and normalises its
+//     half of O with its own softmax sums, so the two halves need not agree bit for bit;
 //   * P (bf16) goes to shared memory in the 128B-swizzled K-major layout, and each CTA
 //     accumulates its 256 columns of O in TMEM from P and its own V columns.
 // Shared memory holds the score operands in a short ring (3 latent tiles, 2 rope tiles),
@@ -68,7 +68,7 @@ constexpr uint32_t kBoxBytes = kN * 128;          // 64 rows x 64 bf16 (128B swi
 constexpr uint32_t kLatBytes = 4 * kBoxBytes;     // 64 rows x this CTA's 256 latent columns
 constexpr uint32_t kRopeBoxBytes = kN * 64;       // 64 rows x 32 bf16 (64B swizzle)
 constexpr uint32_t kQRopeBytes = 128 * 64;        // 128 heads x 32 bf16
-constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's bf16 partial scores
+constexpr uint32_t kRecvBytes = 128 * kN * 2;     // peer's fp16 partial scores
 constexpr uint32_t kQuarterXBytes = 32 * kN * 2;  // one lane quarter's share: 32 rows x 64 columns
 constexpr uint32_t kPBytes = 128 * kN * 2;        // P, bf16, 128 rows x 128 B
 
@@ -93,7 +93,6 @@ constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
 constexpr uint32_t kTmemS = 256;    // [256,384) two score buffers of 64 fp32
 constexpr uint32_t kTmemQ = 384;    // [384,512) q~ half: 256 bf16 packed in pairs
 
-constexpr uint64_t kWaitNs = 2000000000ull;   // 2 s per wait
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 enum Bar {
@@ -145,16 +144,21 @@ __device__ __forceinline__ int tile_row(const DecodeParams& p, int b, int t, boo
   return (int)((int64_t)b * p.kv_seq_stride + t);
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, kWaitNs));
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, limit_ns));
 }
 
-__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity) {
-  return !__any_sync(0xffffffffu, !mbar_wait<true>(bar, parity, kWaitNs));
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return !__any_sync(0xffffffffu, !mbar_wait<true>(bar, parity, limit_ns));
 }
 
+// kTestHook: the instance launched only while the test hook mla_debug_inject_timeout is
+// on, whose wait limit comes from the launch and whose score issuer may withhold a
+// completion; the ordinary instance keeps the 2 s limit a compile-time constant.
+template <bool kTestHook>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
+  const uint64_t wait_ns = kTestHook ? p.wait_ns : kDefaultWaitNs;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -264,7 +268,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         q_issued = true;
       };
       auto qk_done = [&](int j) {
-        return mbar_wait(bar(kSFull + j % kGroups), (uint32_t)(j / kGroups) & 1u, kWaitNs);
+        return mbar_wait(bar(kSFull + j % kGroups), (uint32_t)(j / kGroups) & 1u, wait_ns);
       };
       for (int i = 0; i < ntiles; ++i) {
         const int qs = i % kQkStages, rs = i % kRopeStages;
@@ -291,10 +295,10 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       if (!q_issued && !aborted) load_q();
       // No copy may still be landing when the CTA exits.
       for (int i = max(0, issued - kQkStages); i < issued; ++i)
-        mbar_wait(bar(kQkFull + i % kQkStages), (uint32_t)(i / kQkStages) & 1u, kWaitNs);
+        mbar_wait(bar(kQkFull + i % kQkStages), (uint32_t)(i / kQkStages) & 1u, wait_ns);
       for (int i = max(0, rope_issued - kRopeStages); i < rope_issued; ++i)
-        mbar_wait(bar(kRopeFull + i % kRopeStages), (uint32_t)(i / kRopeStages) & 1u, kWaitNs);
-      if (q_issued && !mbar_wait(bar(kQFull), 0, kWaitNs)) aborted = true;
+        mbar_wait(bar(kRopeFull + i % kRopeStages), (uint32_t)(i / kRopeStages) & 1u, wait_ns);
+      if (q_issued && !mbar_wait(bar(kQFull), 0, wait_ns)) aborted = true;
     }
   } else if (warp == 1) {
     // ---------------- QK issuer ----------------
@@ -310,12 +314,12 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16(128, kN, false, false);
       const uint64_t qrope_desc = smem_desc(s0 + kOffQRope, 16, 512, kSwizzle64B);
-      if (!mbar_wait(bar(kQFull), 0, kWaitNs) || !mbar_wait(bar(kQReady), 0, kWaitNs)) aborted = true;
+      if (!mbar_wait(bar(kQFull), 0, wait_ns) || !mbar_wait(bar(kQReady), 0, wait_ns)) aborted = true;
       for (int i = 0; i < ntiles && !aborted; ++i) {
         const int qs = i % kQkStages, rs = i % kRopeStages;
         const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
-        if ((i >= 2 && !mbar_wait(bar(kSFree + (i - 2) % kGroups), (uint32_t)((i - 2) / kGroups) & 1u, kWaitNs)) ||
-            !mbar_wait(bar(kQkFull + qs), (uint32_t)(i / kQkStages) & 1u, kWaitNs)) {
+        if ((i >= 2 && !mbar_wait(bar(kSFree + (i - 2) % kGroups), (uint32_t)((i - 2) / kGroups) & 1u, wait_ns)) ||
+            !mbar_wait(bar(kQkFull + qs), (uint32_t)(i / kQkStages) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -325,17 +329,17 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           mma_ts(d, tb + kTmemQ + 8u * k, kv + (((k >> 2) * kBoxBytes + (k & 3) * 32u) >> 4), id_qk, k > 0 ? 1u : 0u);
-        if (!mbar_wait(bar(kRopeFull + rs), (uint32_t)(i / kRopeStages) & 1u, kWaitNs)) {
+        if (!mbar_wait(bar(kRopeFull + rs), (uint32_t)(i / kRopeStages) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 2; ++k) mma_ss(d, qrope_desc + 2u * k, kr + 2u * k, id_qk, 1u);
-        mma_commit(bar(kSFull + i % kGroups));
+        if (!(kTestHook && p.fault && i == 0)) mma_commit(bar(kSFull + i % kGroups));   // test hook: withheld
       }
       mma_commit(bar(kDrain));
-      mbar_wait(bar(kDrain), 0, kWaitNs);
+      mbar_wait(bar(kDrain), 0, wait_ns);
     }
   } else if (warp == kPvWarp) {
     // ---------------- PV issuer (and the V re-reads) ----------------
@@ -360,15 +364,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       for (int i = 0; i < ntiles; ++i) {
         const int vs = i % kVStages;
         if (i + 1 < ntiles && i + 1 >= kVStages) {
-          if (!mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, kWaitNs)) {
+          if (!mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, wait_ns)) {
             aborted = true;
             break;
           }
           load_v(i + 1);
           ++v_issued;
         }
-        if (!mbar_wait(bar(kPFull), (uint32_t)i & 1u, kWaitNs) ||
-            !mbar_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, kWaitNs)) {
+        if (!mbar_wait(bar(kPFull), (uint32_t)i & 1u, wait_ns) ||
+            !mbar_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -382,15 +386,15 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         mma_commit(bar(kPvDone + i % kGroups));
       }
       mma_commit(bar(kDrainPv));
-      mbar_wait(bar(kDrainPv), 0, kWaitNs);
+      mbar_wait(bar(kDrainPv), 0, wait_ns);
       for (int i = max(0, v_issued - kVStages); i < v_issued; ++i)
-        mbar_wait(bar(kVFull + i % kVStages), (uint32_t)(i / kVStages) & 1u, kWaitNs);
+        mbar_wait(bar(kVFull + i % kVStages), (uint32_t)(i / kVStages) & 1u, wait_ns);
     }
   } else {
     // ---------------- score-to-P groups (warps 2..13) ----------------
     // Group g = (w - 2) / 4 takes the tiles i with i % 3 == g; its warp w covers TMEM lane
     // quarter w % 4 (heads 32q..32q+31, one head per lane).  Per tile: own fp32 partial
-    // scores out of TMEM, a bf16 copy to the peer, the peer's bf16 partial in, the row
+    // scores out of TMEM, an fp16 copy to the peer, the peer's fp16 partial in, the row
     // maximum, the reference maximum (handed on from the group of tile i-1), P = 2^(s -
     // m_ref) into shared memory, and the running output rescaled when m_ref moves.  Each
     // group keeps its own share of the row sum; the shares are merged at the end.
@@ -435,7 +439,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     for (int i = g; i < ntiles && !aborted; i += kGroups) {
       const uint32_t ph = (uint32_t)(i / kGroups) & 1u;
       const uint32_t sb = (uint32_t)(i & 1);          // S buffer and receive buffer
-      if (!warp_wait(bar(kSFull + g), ph)) {
+      if (!warp_wait(bar(kSFull + g), ph, wait_ns)) {
         aborted = true;
         break;
       }
@@ -456,12 +460,12 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       // warps then sends a 4-byte st.async counted on our kRecvFree[i & 1] (a remote
       // mbarrier arrive is far slower under load).  The groups pass this wait in tile order
       // (kFreeSeen), so each phase of kRecvFree[i & 1] is awaited after the one before it.
-      if (i >= 1 && !warp_wait(bar(kFreeSeen + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+      if (i >= 1 && !warp_wait(bar(kFreeSeen + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u, wait_ns)) {
         aborted = true;
         break;
       }
       if (i >= 2) {
-        if (!warp_wait_cluster(bar(kRecvFree + sb), (uint32_t)((i - 2) >> 1) & 1u)) {
+        if (!warp_wait_cluster(bar(kRecvFree + sb), (uint32_t)((i - 2) >> 1) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -474,11 +478,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         const uint32_t dst = recv_peer + sb * kRecvBytes + xoff;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          st_async_v4(dst + (uint32_t)c * 512u, f2_to_bf2(x[8 * c], x[8 * c + 1]),
-                      f2_to_bf2(x[8 * c + 2], x[8 * c + 3]), f2_to_bf2(x[8 * c + 4], x[8 * c + 5]),
-                      f2_to_bf2(x[8 * c + 6], x[8 * c + 7]), recv_bar_peer);
+          st_async_v4(dst + (uint32_t)c * 512u, f2_to_h2_sat(x[8 * c], x[8 * c + 1]),
+                      f2_to_h2_sat(x[8 * c + 2], x[8 * c + 3]), f2_to_h2_sat(x[8 * c + 4], x[8 * c + 5]),
+                      f2_to_h2_sat(x[8 * c + 6], x[8 * c + 7]), recv_bar_peer);
       }
-      if (!warp_wait_cluster(bar(kRecvFull + g), ph)) {
+      if (!warp_wait_cluster(bar(kRecvFull + g), ph, wait_ns)) {
         aborted = true;
         break;
       }
@@ -500,7 +504,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         // kRecvFull of this group, only after our signal for tile i+1, hence after this
         // group's phase of tile i has completed and been read.
         asm volatile("" ::"r"(sig));
-        if (i >= 1 && !warp_wait(bar(kSigSent + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+        if (i >= 1 && !warp_wait(bar(kSigSent + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -513,8 +517,8 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            x[8 * c + 2 * u] += __uint_as_float(ww[u] << 16);
-            x[8 * c + 2 * u + 1] += __uint_as_float(ww[u] & 0xffff0000u);
+            x[8 * c + 2 * u] = add_f16_lo(ww[u], x[8 * c + 2 * u]);
+            x[8 * c + 2 * u + 1] = add_f16_hi(ww[u], x[8 * c + 2 * u + 1]);
           }
         }
       }
@@ -545,7 +549,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       // maximum exceeds it by more than 2^8.
       float m_prev = -INFINITY;
       if (i >= 1) {
-        if (!warp_wait(bar(kMref + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+        if (!warp_wait(bar(kMref + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -574,7 +578,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       l_g += ps;
       // The P buffer is free, and O stable, once PV(i-1) is done.
-      if (i >= 1 && !warp_wait(bar(kPvDone + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u)) {
+      if (i >= 1 && !warp_wait(bar(kPvDone + (i - 1) % kGroups), (uint32_t)((i - 1) / kGroups) & 1u, wait_ns)) {
         aborted = true;
         break;
       }
@@ -605,7 +609,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       // re-read V tile so that 0-weighted rows add exactly 0.
       if (valid < kN) {
         const int vs = i % kVStages;
-        if (!warp_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u)) {
+        if (!warp_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, wait_ns)) {
           aborted = true;
           break;
         }
@@ -634,7 +638,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     const bool have = !aborted && l > 0.f;
     if (!aborted) {
       const int last = ntiles - 1;
-      if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u)) aborted = true;
+      if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u, wait_ns)) aborted = true;
     }
     tc_fence_after();
     const float inv = have ? 1.f / l : 0.f;
@@ -676,7 +680,7 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode(DecodeParams p, cudaStream_t st) {
   Maps maps;
   const uint64_t kv_rows = p.block_table ? (uint64_t)p.num_pages * kPage
                                          : (uint64_t)p.B * (uint64_t)p.kv_seq_stride;
@@ -686,15 +690,16 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
       !encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode_sm103, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const WaitConfig wc = wait_config(kFaultDecode);
+  p.wait_ns = wc.wait_ns;
+  p.fault = wc.fault;
+  static SmemOptIn opt_in, opt_in_hook;
+  cudaError_t e = wc.fault ? ensure_dynamic_smem((const void*)k_decode_sm103<true>, (int)kSmemBytes, opt_in_hook)
+                           : ensure_dynamic_smem((const void*)k_decode_sm103<false>, (int)kSmemBytes, opt_in);
+  if (e != cudaSuccess) return e;
   const int units = p.B * p.S * p.num_splits;
-  cudaError_t e = launch_pdl(k_decode_sm103, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p);
+  e = wc.fault ? launch_pdl(k_decode_sm103<true>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p)
+               : launch_pdl(k_decode_sm103<false>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -12,21 +12,18 @@ namespace {
 // reads, so nothing in it has to start at zero.
 __device__ __align__(256) static unsigned char g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+void* g_scratch_ptr[mla::kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device.  The host-side name of the
 // array is only a stand-in, so the address is asked of the runtime, once per device.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const int dev = mla::current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = p;
   }
@@ -41,9 +38,12 @@ extern "C" mla_status mla_decode_latent_noalloc(
     const int32_t* block_table, int max_pages, int page_size, int num_pages, int B, int S, int H,
     int causal, float scale, int num_splits, int max_seqlen, float* o_lat, float* lse,
     int32_t* status_dev, mla_stream stream) {
-  if (!q_cat || !kv || !seqlens || !o_lat || !lse) return MLA_ERR_INVALID;
-  if (B < 1 || S < 1 || H < 1 || max_seqlen < 0) return MLA_ERR_INVALID;
-  if (num_splits < 0 || num_splits > MLA_MAX_SPLITS) return MLA_ERR_INVALID;
+  // Every host-side check of mla_decode_latent first: a rejected call makes no CUDA call
+  // (the scratch address below is what would first touch the device).
+  const mla_status bad = mla::check_decode_args(q_cat, kv, kv_seq_stride, seqlens, block_table,
+                                                max_pages, page_size, num_pages, B, S, H, scale,
+                                                num_splits, max_seqlen, o_lat, lse);
+  if (bad != MLA_OK) return bad;
   const size_t need = mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen);
   if (need > (size_t)MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
   void* scratch = nullptr;

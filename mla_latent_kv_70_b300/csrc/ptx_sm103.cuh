@@ -195,6 +195,28 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Two fp32 values rounded to fp16 (round to nearest even) and packed, lo in bits [0,16);
+// values beyond the fp16 range saturate to +-65504 instead of becoming infinite.
+__device__ __forceinline__ uint32_t f2_to_h2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// c + (the fp16 in bits [0,16) of w), or of bits [16,32) for add_f16_hi, in one fp32
+// rounding (mixed-precision add of sm_100 and later).
+__device__ __forceinline__ float add_f16_lo(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.f16 %0, l, %2;\n}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float add_f16_hi(uint32_t w, float c) {
+  float d;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n add.rn.f32.f16 %0, h, %2;\n}" : "=f"(d) : "r"(w), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -10,7 +10,11 @@ RopeFreqs make_rope_freqs(float theta) {
   // Page "Multi-Head Latent Attention (MLA)", section "구현" (_apply_rope): inverse
   // frequencies theta^(-(0, 2, 4, ..)/d_r) for the interleaved pairs.
   RopeFreqs f;
-  for (int i = 0; i < kDr / 2; ++i) f.inv_freq[i] = std::pow((double)theta, -2.0 * i / kDr);
+  for (int i = 0; i < kDr / 2; ++i) {
+    const double inv = std::pow((double)theta, -2.0 * i / kDr);
+    f.hi[i] = (float)inv;
+    f.lo[i] = (float)(inv - (double)f.hi[i]);
+  }
   return f;
 }
 
@@ -26,7 +30,7 @@ __global__ void k_rope_inplace(__nv_bfloat16* __restrict__ x, int64_t row_stride
   const int i = (int)(idx % (kDr / 2));
   uint32_t* p = reinterpret_cast<uint32_t*>(x + r * row_stride + col_offset) + i;
   const float2 v = bf2_to_f2(*p);
-  const float2 y = rope_pair(v.x, v.y, pos[r], f.inv_freq[i]);
+  const float2 y = rope_pair(v.x, v.y, pos[r], f.hi[i], f.lo[i]);
   *p = f2_to_bf2(y.x, y.y);
 }
 

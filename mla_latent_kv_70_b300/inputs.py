@@ -159,6 +159,36 @@ def weights(case: DecodeCase):
             randn_bf16((case.H, D_C, D_V), case.seed, "wuv", 0, std))
 
 
+def seq_q_cat(case: DecodeCase, b: int) -> torch.Tensor:
+    """bf16 [S, H, 576] query rows of sequence b in the layout the latent decode reads
+    ([q~ (512) | q^R (64)]), drawn directly rather than produced by the key absorption:
+    q~ ~ N(0, 1/4), the spread of q_nope W_UK^T for the draws above (128 products of
+    variance 1/512 each), and q^R ~ N(0, 1)."""
+    lat = randn_bf16((case.S, case.H, D_C), case.seed, "qlat", b, std=0.5)
+    rope = randn_bf16((case.S, case.H, D_R), case.seed, "qcr", b)
+    return torch.cat([lat, rope], dim=-1)
+
+
+def q_cat(case: DecodeCase) -> torch.Tensor:
+    """bf16 [B, S, H, 576]: seq_q_cat of every sequence."""
+    out = torch.empty(case.B, case.S, case.H, ROW, dtype=torch.bfloat16)
+    for b in range(case.B):
+        out[b] = seq_q_cat(case, b)
+    return out
+
+
+def pool_positions(case: DecodeCase) -> torch.Tensor:
+    """int32 [num_pages * page_size]: the position in its sequence of every row of a page
+    pool (row r of page block_table[b, i] is position i * page_size + r of sequence b)."""
+    pos = torch.zeros(case.num_pages * case.page_size, dtype=torch.int32)
+    r = torch.arange(case.page_size, dtype=torch.int32)
+    for b in range(case.B):
+        for i in range(case.pages_per_seq[b]):
+            page = int(case.block_table[b, i])
+            pos[page * case.page_size:(page + 1) * case.page_size] = i * case.page_size + r
+    return pos
+
+
 def queries(case: DecodeCase):
     qn = torch.empty(case.B, case.S, case.H, D_NOPE, dtype=torch.bfloat16)
     qr = torch.empty(case.B, case.S, case.H, D_R, dtype=torch.bfloat16)

@@ -137,3 +137,10 @@ def test_binding_refuses_wrong_dtypes(lib):
         mla.mla_out_proj_uv(bf(2, 1, 16, 512), bf(16, 512, 128), torch.zeros(2, 1, 16, 128))
     with pytest.raises(ValueError, match="device tensors"):   # right dtypes, host memory
         mla.mla_out_proj_uv(torch.zeros(2, 1, 16, 512), bf(16, 512, 128), torch.zeros(2, 1, 16, 128))
+
+
+def test_timeout_hook_rejects_bad_arguments(lib):
+    assert lib.mla_debug_inject_timeout(8, ctypes.c_double(1.0)) == 1        # unknown kernel bit
+    assert lib.mla_debug_inject_timeout(1, ctypes.c_double(0.0)) == 1        # no wait limit
+    assert lib.mla_debug_inject_timeout(1, ctypes.c_double(5000.0)) == 1     # beyond 2 s
+    assert lib.mla_debug_inject_timeout(0, ctypes.c_double(0.0)) == 0        # off
