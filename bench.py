@@ -34,6 +34,7 @@ from mla_latent_kv_70_b300 import inputs as I  # noqa: E402
 METRIC = "MLA decode tokens/s (one attention layer: absorb + latent attention + W_UV)"
 UNIT = "tokens/s"
 ROW_BYTES = 1152
+L2_BYTES = 126e6
 DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_sm103.cu",
                   "mla_latent_kv_70_b300/csrc/ptx_sm103.cuh",
                   "mla_latent_kv_70_b300/csrc/common.cuh"]
@@ -175,7 +176,7 @@ class ClockSampler:
                             self.reasons.add(name)
                 except Exception as e:  # noqa: BLE001
                     self.error = f"nvml sample: {e!r}"
-            time.sleep(0.001)
+            time.sleep(0.0002)
 
     def begin(self):
         self.window[0] = time.time()
@@ -346,8 +347,12 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
-    # Inputs resident in HBM before timing.
+    # Inputs resident in HBM before timing.  A cache smaller than L2 is replicated so
+    # that consecutive timed steps read different copies, more bytes in all than L2
+    # holds, and each step's cache reads come from HBM.
     kv = I.cache(case, device=dev)
+    cache_b, _, _ = algorithmic(case)
+    n_copies = 1 if cache_b > L2_BYTES else min(256, math.ceil(2 * L2_BYTES / cache_b))
     qn, qr = I.queries(case)
     w_uk, w_uv = (w.to(dev) for w in I.weights(case))
     q_nope, q_rope = qn.to(dev), qr.to(dev)
@@ -355,14 +360,16 @@ def main():
     block_table = case.block_table.to(dev) if case.paged else None
     q_pos = case.q_positions().to(dev) if case.rope else None
     if case.rope:
-        pos = torch.arange(case.t_cap, dtype=torch.int32, device=dev).repeat(case.B)
-        mla.mla_rope_inplace(kv, 576, case.B * case.t_cap, 512, pos, case.theta)
+        pos = (I.pool_positions(case).to(dev) if case.paged else
+               torch.arange(case.t_cap, dtype=torch.int32, device=dev).repeat(case.B))
+        mla.mla_rope_inplace(kv, 576, pos.numel(), 512, pos, case.theta)
+    kvs = [kv] + [kv.clone() for _ in range(n_copies - 1)]
     step = mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
                           num_splits=case.num_splits, causal=case.causal, rope_theta=case.theta,
                           total_rows=case.total_tokens)
     stream = torch.cuda.current_stream()
 
-    def run_step(st, marks=None):
+    def run_step(st, marks=None, kv=kv):
         """One step on stream `st`; `marks(i)` records the decode boundaries."""
         mla.mla_absorb_q(q_nope, q_rope, w_uk, q_pos, case.theta, step.q_cat, st)
         if marks:
@@ -403,7 +410,7 @@ def main():
                     err = cudart.cudaEventRecordWithFlags(evs[i][j], cs.cuda_stream,
                                                           cudart.cudaEventRecordExternal)[0]
                     assert err == cudart.cudaError_t.cudaSuccess, err
-                run_step(cs, marks)
+                run_step(cs, marks, kv=kvs[i % n_copies])
         graph.replay()                      # one untimed replay
         torch.cuda.synchronize()
         use_graph = True
@@ -421,7 +428,7 @@ def main():
         dec_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                       for _ in range(args.steps)]
         for i in range(args.steps):
-            run_step(stream, lambda j, i=i: dec_events[i][j].record(stream))
+            run_step(stream, lambda j, i=i: dec_events[i][j].record(stream), kv=kvs[i % n_copies])
     end.record(stream)
     barrier()
     clocks.end()
@@ -437,28 +444,53 @@ def main():
     status = int(step.status.item())
     clock_info = clocks.stop()
 
-    # End to end through the public API: queries copied in from pinned host memory,
-    # the output read back, every step.
+    # End to end through the public API, as a serving loop runs it: every step copies its
+    # queries in from pinned host memory and reads its output back.  Two sets of step
+    # buffers alternate, each step's compute replays a CUDA graph of the public
+    # DecodeStep (DecodeStep.capture), and the copies run on their own streams, so the
+    # copies of one step overlap the compute of the next.
     qn_h = qn.pin_memory()
     qr_h = qr.pin_memory()
-    o_h = torch.empty(step.o.shape, dtype=torch.float32).pin_memory()
+    steps2 = [step, mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
+                                   num_splits=case.num_splits, causal=case.causal,
+                                   rope_theta=case.theta, total_rows=case.total_tokens)]
+    qn_d, qr_d = [q_nope, q_nope.clone()], [q_rope, q_rope.clone()]
+    o_h = [torch.empty(step.o.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    replay = [steps2[k].capture(qn_d[k], qr_d[k], kv, seqlens, block_table=block_table, q_pos=q_pos)
+              for k in range(2)]
     h2d = qn_h.numel() * 2 + qr_h.numel() * 2
-    d2h = o_h.numel() * 4
+    d2h = o_h[0].numel() * 4
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "comp", "out")}
 
-    def e2e_step():
-        q_nope.copy_(qn_h, non_blocking=True)
-        q_rope.copy_(qr_h, non_blocking=True)
-        step(q_nope, q_rope, kv, seqlens, block_table=block_table, q_pos=q_pos, stream=stream)
-        o_h.copy_(step.o, non_blocking=True)
+    def e2e_step(i):
+        k = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev["comp"][k])      # step i-2 no longer reads these inputs
+            qn_d[k].copy_(qn_h, non_blocking=True)
+            qr_d[k].copy_(qr_h, non_blocking=True)
+            ev["in"][k].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev["in"][k])
+            if i >= 2:
+                s_comp.wait_event(ev["out"][k])     # step i-2's output has been read back
+            replay[k]()
+            ev["comp"][k].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"][k])
+            o_h[k].copy_(steps2[k].o, non_blocking=True)
+            ev["out"][k].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(args.steps):
+        e2e_step(i)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
@@ -468,7 +500,7 @@ def main():
     value = whole_job_rate(world, tokens_per_step, ms_per_step)
     e2e_value = whole_job_rate(world, tokens_per_step, e2e_ms / args.steps)
 
-    cache_b, alg_b, flops = algorithmic(case)
+    _, alg_b, flops = algorithmic(case)
     hbm, tf_burst, tf_sus, peak_kind = measured_peaks()
     dec_avg_s = statistics.mean(dec_ms) / 1e3
     achieved_gbs = alg_b / dec_avg_s / 1e9
@@ -500,7 +532,9 @@ def main():
                        "num_splits": step.num_splits, "paged": case.paged,
                        "causal": case.causal, "rope": case.rope,
                        "l2": f"inputs larger than L2: {cache_b / 1e6:.0f} MB cache read per step"
-                             if cache_b > 126e6 else "inputs fit in L2 (no flush)",
+                             if n_copies == 1 else
+                             f"{n_copies} copies of the {cache_b / 1e6:.2f} MB cache read in turn "
+                             f"({n_copies * cache_b / 1e6:.0f} MB > L2)",
                        "timing": timing,
                        "parallelism": f"dp{world} (independent replicas, no collective)"},
             "clocks": clock_info,

@@ -13,6 +13,8 @@
  *                      (optionally split along the cache and merged by log-sum-exp)
  *   mla_out_proj_uv    value up-projection of the aggregated latent, once per head
  *   mla_rope_inplace   RoPE on the 64-wide rope slice of cache rows or queries
+ *   mla_append_latent  the step's new latent rows into the cache (k^R rotated), before
+ *                      the decode reads it
  *
  * Conventions shared by every call
  *   - Dimensions are fixed: d_c = 512 (latent), d_r = 64 (decoupled RoPE key),
@@ -222,6 +224,33 @@ mla_status mla_combine_partials(const float* o_part, const float* lse_part, int 
  */
 mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int S, int H,
                            float* o, mla_stream stream);
+
+/*
+ * mla_append_latent -- add the latent rows of this step's S tokens per sequence to the
+ * cache, before mla_decode_latent reads it ([CALC] "계산 재배치의 효과와 한계": the current
+ * token's latent is appended first and the token then reads itself; [ANATOMY] section 2:
+ * the cached k^R carries RoPE, applied once when the row is written).
+ *
+ *   rows        bf16 [B,S,576] new rows [c^KV (512) | k^R (64), not yet rotated]
+ *   rope_theta  RoPE base; > 0 rotates k^R of the row at position t by t * theta^(-2i/64)
+ *               (interleaved pairs, as mla_rope_inplace), 0 stores k^R as given
+ *   seqlens     int32 [B] device: row s of sequence b goes to position seqlens[b] + s;
+ *               afterwards seqlens[b] += S (read and advanced by the same kernel)
+ *   kv, kv_seq_stride, block_table, max_pages, page_size, num_pages: the cache, laid out
+ *               as for mla_decode_latent (contiguous when block_table is NULL)
+ *   status_dev  int32 device word or NULL: a row whose position has no place (past
+ *               kv_seq_stride, past max_pages pages, or a page outside [0, num_pages)) is
+ *               not written and 1 << MLA_ERR_BLOCK_TABLE is OR-ed in
+ *
+ * The c^KV part is copied bit for bit; k^R is rotated in fp32 (angle reduced as in
+ * mla_rope_inplace) and stored as bf16.  The kernel does not let the next kernel on the
+ * stream start before it completes, so a mla_decode_latent issued right after it sees
+ * the appended rows and the advanced seqlens (see the convention on early starts above).
+ */
+mla_status mla_append_latent(const mla_bf16* rows, int B, int S, float rope_theta, int32_t* seqlens,
+                             mla_bf16* kv, int64_t kv_seq_stride, const int32_t* block_table,
+                             int max_pages, int page_size, int num_pages, int32_t* status_dev,
+                             mla_stream stream);
 
 /*
  * mla_rope_inplace -- rotate the 64 values x[r, col_offset : col_offset+64] of each of

@@ -40,6 +40,7 @@ SIGNATURES = {
     "mla_out_proj_uv": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "mla_rope_inplace": (_I, [_P, _I64, _I64, _I, _P, _F, _P]),
     "mla_debug_inject_timeout": (_I, [_I, ctypes.c_double]),
+    "mla_append_latent": (_I, [_P, _I, _I, _F, _P, _P, _I64, _P, _I, _I, _I, _P, _P]),
 }
 
 _LIB = None
@@ -169,6 +170,22 @@ def mla_out_proj_uv(o_lat, w_uv, o, stream=None):
     B, S, H, _ = o_lat.shape
     _check("mla_out_proj_uv", lib().mla_out_proj_uv(_ptr(o_lat, _F32), _ptr(w_uv, _BF16), B, S, H,
                                                     _ptr(o, _F32), _stream(stream)))
+
+
+def mla_append_latent(rows, seqlens, kv, *, rope_theta=0.0, block_table=None, kv_seq_stride=0,
+                      page_size=64, status=None, stream=None):
+    """Write rows [B,S,576] at positions seqlens[b] + s of the cache (k^R rotated when
+    rope_theta > 0) and advance seqlens by S."""
+    B, S, _ = rows.shape
+    if block_table is not None:
+        num_pages, max_pages = kv.shape[0], block_table.shape[1]
+    else:
+        num_pages, max_pages = 0, 0
+        kv_seq_stride = kv_seq_stride or kv.shape[1]
+    _check("mla_append_latent", lib().mla_append_latent(
+        _ptr(rows, _BF16), B, S, float(rope_theta), _ptr(seqlens, _I32), _ptr(kv, _BF16),
+        int(kv_seq_stride), _ptr(block_table, _I32), max_pages, page_size, num_pages,
+        _ptr(status, _I32), _stream(stream)))
 
 
 def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):

@@ -182,6 +182,26 @@ mla_status mla_out_proj_uv(const float* o_lat, const mla_bf16* w_uv, int B, int 
                                                B * S, H, o, static_cast<cudaStream_t>(stream)));
 }
 
+mla_status mla_append_latent(const mla_bf16* rows, int B, int S, float rope_theta, int32_t* seqlens,
+                             mla_bf16* kv, int64_t kv_seq_stride, const int32_t* block_table,
+                             int max_pages, int page_size, int num_pages, int32_t* status_dev,
+                             mla_stream stream) {
+  if (!rows || !seqlens || !kv) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || rope_theta < 0.f || !std::isfinite(rope_theta)) return MLA_ERR_INVALID;
+  if (!aligned16(rows) || !aligned16(kv)) return MLA_ERR_INVALID;
+  if (block_table) {
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID;
+  } else if (kv_seq_stride < 1) {
+    return MLA_ERR_INVALID;
+  }
+  const mla::RopeFreqs f = mla::make_rope_freqs(rope_theta > 0.f ? rope_theta : 10000.f);
+  return launch_status(mla::launch_append_latent(
+      reinterpret_cast<const __nv_bfloat16*>(rows), B, S, seqlens, reinterpret_cast<__nv_bfloat16*>(kv),
+      kv_seq_stride, block_table, max_pages, num_pages, rope_theta > 0.f ? 1 : 0, f, status_dev,
+      static_cast<cudaStream_t>(stream)));
+}
+
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream) {
   if (!x || !pos || rows < 0 || col_offset < 0 || row_stride < col_offset + mla::kDr)

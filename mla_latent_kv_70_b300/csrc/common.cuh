@@ -175,5 +175,9 @@ cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t ro
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
                            float* o, float* lse, cudaStream_t st);
 cudaError_t launch_decode(DecodeParams p, cudaStream_t st);
+cudaError_t launch_append_latent(const __nv_bfloat16* rows, int B, int S, int32_t* seqlens,
+                                 __nv_bfloat16* kv, int64_t kv_seq_stride, const int32_t* block_table,
+                                 int max_pages, int num_pages, int rotate, const RopeFreqs& f,
+                                 int32_t* status, cudaStream_t st);
 
 }  // namespace mla

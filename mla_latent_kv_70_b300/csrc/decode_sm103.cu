@@ -116,6 +116,7 @@ enum Bar {
   kQReady,
   kDrain,
   kDrainPv,
+  kVGo,                               // PV issuer -> TMA: the first V tiles are requested
   kNumBars
 };
 static_assert(kNumBars * 8 <= 384, "barrier area");
@@ -124,7 +125,14 @@ struct Maps {
   CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle
   CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle
   CUtensorMap q_rope;    // q_cat rows, box 32 cols x 128 rows, 64B swizzle
+  CUtensorMap o_store;   // output rows (o_lat or split partials) fp32, box 32 cols x H rows, 128B swizzle
 };
+
+// Epilogue staging: chunk c (32 output columns of the 128 head rows, 128 B per row,
+// 128B-swizzled) at c * 16 KB, over the score and V rings, which are idle by then.
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kStageChunk = 128 * 128;
+static_assert(kOffStage + 8 * kStageChunk <= kOffQRope, "staging stays clear of q^R and the exchange buffers");
 
 __device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int t) {
   return p.block_table[(int64_t)b * p.max_pages + t / kPage];
@@ -224,6 +232,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     mbar_init(bar(kQReady), 2 * kGroupThreads);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kDrainPv), 1);
+    mbar_init(bar(kVGo), 1);
     mbar_init(bar(kRecvFree + 0), 1);
     mbar_init(bar(kRecvFree + 1), 1);
     fence_mbar_init();
@@ -273,7 +282,16 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       for (int i = 0; i < ntiles; ++i) {
         const int qs = i % kQkStages, rs = i % kRopeStages;
         const int y = tile_row(p, b, t0 + i * kN, true);
-        if (i >= kRopeStages && !q_issued) load_q();
+        // Start-up order: tile 0, then q^R, then the other tiles, so that the first score
+        // MMAs are not queued behind the whole start-up burst of every CTA.  Tile 3 reuses
+        // the slot of tile 0, whose landing the aggregation issuer waits for (phase 0)
+        // before it requests the first V tiles: it is requested only once those requests
+        // are out (kVGo), so that wait cannot meet a later phase.
+        if (i >= 1 && !q_issued) load_q();
+        if (i == kQkStages && !mbar_wait(bar(kVGo), 0, wait_ns)) {
+          aborted = true;
+          break;
+        }
         if (i >= kQkStages && !qk_done(i - kQkStages)) {
           aborted = true;
           break;
@@ -360,8 +378,16 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
                       256 * (int)rank + 64 * j, y);
       };
       int v_issued = 0;
-      for (; v_issued < min(kVStages, ntiles); ++v_issued) load_v(v_issued);
-      for (int i = 0; i < ntiles; ++i) {
+      // The first V tiles re-read latent rows that the score ring requested first: asked
+      // for once those have landed, they are L2 hits rather than part of the start-up
+      // burst from HBM.
+      for (; v_issued < min(kVStages, ntiles); ++v_issued) {
+        if (!mbar_wait(bar(kQkFull + v_issued), 0u, wait_ns)) break;
+        load_v(v_issued);
+      }
+      mbar_arrive(bar(kVGo));
+      if (v_issued < min(kVStages, ntiles)) aborted = true;
+      for (int i = 0; i < ntiles && !aborted; ++i) {
         const int vs = i % kVStages;
         if (i + 1 < ntiles && i + 1 >= kVStages) {
           if (!mbar_wait(bar(kVEmpty + (i + 1) % kVStages), (uint32_t)((i + 1) / kVStages - 1) & 1u, wait_ns)) {
@@ -626,7 +652,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
 
     // Epilogue.  The groups' row-sum shares, each moved to the final reference maximum,
     // are summed through shared memory (the receive buffers are idle now); then each
-    // group writes its columns chunks c = g, g+3, g+6 of the O half divided by the sum.
+    // group takes the column chunks c = g, g+3, g+6 of the O half, divided by the sum,
+    // stages them in shared memory and writes each with one TMA store (full lines,
+    // where per-thread row stores would scatter 16 bytes over 32 rows each).  Once the
+    // last PV is done no copy is in flight and no MMA reads the rings, which hold the
+    // staging.  A CTA that gave up writes its rows directly.
     named_bar_sync(1, kGroups * kGroupThreads);
     const float m_fin = mref_sh[h];
     float* lsh = reinterpret_cast<float*>(smem + kOffRecv);
@@ -635,13 +665,16 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     const float l = lsh[h] + lsh[128 + h] + lsh[256 + h];
     const int64_t orow = (p.num_splits > 1) ? (int64_t)split * rows_all + qrow : qrow;
     float* out = p.o_out + orow * kDc + 256 * rank;
-    const bool have = !aborted && l > 0.f;
     if (!aborted) {
       const int last = ntiles - 1;
       if (!warp_wait(bar(kPvDone + last % kGroups), (uint32_t)(last / kGroups) & 1u, wait_ns)) aborted = true;
     }
+    const bool have = !aborted && l > 0.f;   // a row with no readable position: exact zeros
     tc_fence_after();
     const float inv = have ? 1.f / l : 0.f;
+    // The group stages only if none of its four warps gave up (then no copy is in flight
+    // into the rings); otherwise each warp writes its rows directly.
+    const bool stage = named_bar_and(2 + g, kGroupThreads, !aborted);
 #pragma unroll 1
     for (int c = g; c < 8; c += kGroups) {
       uint32_t r[32];
@@ -649,14 +682,28 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         tmem_ld32(tb + lane_off + kTmemO + 32u * c, r);
         tmem_ld_wait();
       }
-      if (head_ok) {
-        // A row that saw no readable position (l == 0) is written as exact zeros.
+      const uint32_t row = s0 + kOffStage + (uint32_t)c * kStageChunk + (uint32_t)h * 128u;
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          reinterpret_cast<float4*>(out + 32 * c)[v] =
-              have ? make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                 __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int v = 0; v < 8; ++v) {
+        const float4 o4 = have ? make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (stage)   // 128B swizzle: 16-byte chunk v of row h sits at chunk v ^ (h & 7)
+          st_shared_u4(row + (uint32_t)((v ^ (h & 7)) << 4), __float_as_uint(o4.x), __float_as_uint(o4.y),
+                       __float_as_uint(o4.z), __float_as_uint(o4.w));
+        else if (head_ok)
+          reinterpret_cast<float4*>(out + 32 * c)[v] = o4;
+      }
+    }
+    if (stage) {
+      fence_proxy_async_smem();
+      named_bar_sync(2 + g, kGroupThreads);
+      if (gtid == 0) {
+        const int y = (int)((p.num_splits > 1 ? (int64_t)split * rows_all : 0) + (int64_t)m * p.H);
+        for (int c = g; c < 8; c += kGroups)
+          tma_store_2d(&maps.o_store, 256 * (int)rank + 32 * c, y, s0 + kOffStage + (uint32_t)c * kStageChunk);
+        bulk_commit_group();
+        bulk_wait_group0();
       }
     }
     if (g == 0 && head_ok && rank == 0)
@@ -686,9 +733,12 @@ cudaError_t launch_decode(DecodeParams p, cudaStream_t st) {
                                          : (uint64_t)p.B * (uint64_t)p.kv_seq_stride;
   const uint64_t q_rows = (uint64_t)p.B * p.S * p.H;
   if (kv_rows == 0 || kv_rows > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  const uint64_t o_rows = q_rows * (uint64_t)(p.num_splits > 1 ? p.num_splits : 1);
   if (!encode_rows(&maps.kv_lat, p.kv, kv_rows, 64, kN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+      !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_tma_2d(&maps.o_store, false, p.o_out, kDc, o_rows, (uint64_t)kDc * 4, 32, (uint32_t)p.H,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const WaitConfig wc = wait_config(kFaultDecode);
   p.wait_ns = wc.wait_ns;

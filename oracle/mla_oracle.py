@@ -44,6 +44,7 @@ __all__ = [
     "combine_partials",
     "out_proj_uv",
     "gather_paged_rows",
+    "append_latent_rows",
     "cache_values_per_token",
     "cache_bytes_per_token",
     "compression_ratio",
@@ -266,6 +267,24 @@ def gather_paged_rows(pool: np.ndarray, block_row: np.ndarray, T: int) -> np.nda
     P = pool.shape[1]
     t = np.arange(T)
     return pool[np.asarray(block_row)[t // P], t % P]
+
+
+def append_latent_rows(new_rows, start: int, theta=None, d_r: int = 64):
+    """The cache rows one sequence gains in a decode step, and their positions.
+
+    [CALC] "계산 재배치의 효과와 한계": the current token's latent is added to the cache
+    before attention, so the S new rows take positions start .. start + S - 1 (start = the
+    rows already cached) and each query token then reads itself.  [ANATOMY] section 2:
+    the cached k^R carries RoPE, so the k^R part of the row at position t is rotated by t
+    when the row is written (theta None or 0: stored as given); c^KV is stored unchanged.
+    new_rows [S, d_c + d_r] (the last d_r values are k^R).
+    Returns (rows [S, d_c + d_r] as stored, positions [S]).
+    """
+    rows = np.array(new_rows, dtype=np.float64)
+    pos = start + np.arange(rows.shape[0])
+    if theta:
+        rows[:, -d_r:] = rope_interleaved(rows[:, -d_r:], pos, theta)
+    return rows, pos
 
 
 # ----------------------------------------------------------------------------

@@ -86,6 +86,14 @@ def test_other_calls_reject_bad_arguments(lib):
     assert lib.mla_rope_inplace(P, 576, 10, 512, None, 1e4, None) == 1
     assert lib.mla_rope_inplace(P, 576, 10, 520, P, 1e4, None) == 1
     assert lib.mla_rope_inplace(P, 576, 10, 511, P, 1e4, None) == 1
+    f = ctypes.c_float
+    assert lib.mla_append_latent(None, 2, 1, f(1e4), P, P, 64, None, 0, 64, 0, None, None) == 1
+    assert lib.mla_append_latent(P, 0, 1, f(1e4), P, P, 64, None, 0, 64, 0, None, None) == 1
+    assert lib.mla_append_latent(P, 2, 1, f(-1.0), P, P, 64, None, 0, 64, 0, None, None) == 1
+    assert lib.mla_append_latent(P + 8, 2, 1, f(1e4), P, P, 64, None, 0, 64, 0, None, None) == 1
+    assert lib.mla_append_latent(P, 2, 1, f(1e4), P, P, 0, None, 0, 64, 0, None, None) == 1
+    assert lib.mla_append_latent(P, 2, 1, f(1e4), P, P, 0, P, 4, 32, 10, None, None) == 2
+    assert lib.mla_append_latent(P, 2, 1, f(1e4), P, P, 0, P, 0, 64, 10, None, None) == 1
 
 
 # ----------------------------------------------------------------------------

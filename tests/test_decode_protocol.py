@@ -63,6 +63,16 @@ class Bar:
         return (self.phase & 1) != parity
 
 
+class Delay:
+    """Not a barrier: a warp that is simply late (scheduled late, or stalled) until `until`."""
+
+    def __init__(self, sim, until):
+        self.sim, self.until, self.name, self.phase = sim, until, "delay", None
+
+    def parity_done(self, parity):
+        return self.sim.step_no >= self.until
+
+
 class Slot:
     def __init__(self):
         self.tile = None
@@ -89,6 +99,7 @@ class CTA:
         self.pfull = B(f"r{rank}.PFull", 128)
         self.qfull = B(f"r{rank}.QFull", 1)
         self.qready = B(f"r{rank}.QReady", 256)
+        self.vgo = B(f"r{rank}.VGo", 1)
         # Buffers: which tile occupies them, and whether its readers are done.
         self.qk_slot = [Slot() for _ in range(3)]
         self.rope_slot = [Slot() for _ in range(2)]
@@ -146,9 +157,11 @@ class Sim:
             self.later(lambda: c.qfull.complete_tx(QROPE))
 
         for i in range(n):
-            if i >= 2 and not q_issued:
+            if i >= 1 and not q_issued:
                 load_q()
                 q_issued = True
+            if i == 3 and "no_vgo" not in self.faults:
+                yield ("wait", c.vgo, 0)
             if i >= 3:
                 yield ("wait", c.sfull[(i - 3) % 3], (i - 3) // 3)
             s = c.qk_slot[i % 3]
@@ -213,8 +226,16 @@ class Sim:
                 c.vfull[i % 2].complete_tx(VBYTES)
             self.later(land)
 
+        if self.rng.random() < 0.3:     # the issuer may start late
+            yield ("wait", Delay(self, self.step_no + self.rng.randint(1, 400)), 0)
         for i in range(min(2, n)):
+            # The first V tiles are requested once the same rows have landed in the score
+            # ring (phase 0 of its slot), so that they come from L2.
+            yield ("wait", c.qkfull[i], 0)
+            s = c.qk_slot[i]
+            check(s.tile == i and s.landed, f"r{c.rank}: first V({i}) follows a slot that no longer holds tile {i}")
             load_v(i)
+        c.vgo.arrive()
         for i in range(n):
             vs = i % 2
             if i + 1 < n and i + 1 >= 2:
@@ -319,7 +340,8 @@ class Sim:
                 if q and q[0][0] <= self.step_no:
                     choices.append(("queue", key))
             if not choices:
-                if self.events or any(self.queues.values()):
+                delayed = any(w is not None and isinstance(w[0], Delay) for g, w in states if g is not None)
+                if self.events or any(self.queues.values()) or delayed:
                     continue                     # only time passes
                 stuck = [w for g, w in states if g is not None]
                 raise ProtocolError(f"deadlock: waits {[(w[0].name, w[1]) for w in stuck if w]}")
@@ -332,7 +354,7 @@ class Sim:
                 fn()
             else:
                 gen, wait = states[which]
-                if wait is not None:
+                if wait is not None and not isinstance(wait[0], Delay):
                     bar, k = wait
                     check(bar.phase == k + 1,
                           f"{bar.name}: a wait for phase {k} returned with {bar.phase} phases complete")
@@ -353,13 +375,15 @@ def test_protocol_holds_under_random_schedules(n, partial_last):
         assert Sim(n, seed, partial_last).run()
 
 
-@pytest.mark.parametrize("fault", ["no_sfree", "no_freeseen"])
+@pytest.mark.parametrize("fault", ["no_sfree", "no_freeseen", "no_vgo"])
 def test_the_model_catches_a_broken_rule(fault):
     # Each planted mistake leaves out one rule of the protocol:
     # - no_sfree: the score issuer overwrites S buffer i & 1 before the group of tile i-2
     #   read it;
     # - no_freeseen: the groups wait for the peer's "free" signals out of tile order, so a
-    #   parity wait can meet the phase of another tile.
+    #   parity wait can meet the phase of another tile;
+    # - no_vgo: tile 3 is requested before the aggregation issuer has seen tile 0 land,
+    #   so its phase-0 wait on that slot can meet a later phase.
     # Some schedule must then trip an assertion or deadlock.
     failures = 0
     for seed in range(200):

@@ -379,3 +379,44 @@ def test_planted_mistakes_are_caught():
     expect[2], expect[3] = math.cos(ang), math.sin(ang)
     np.testing.assert_allclose(O.rope_interleaved(e, 37), expect, atol=1e-15)
     assert not np.allclose(rope_halves(e, 37), expect, atol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# Cache append ([CALC] "계산 재배치의 효과와 한계"; [ANATOMY] section 2)
+# ----------------------------------------------------------------------------
+
+def test_append_closed_form_one_pair():
+    # d_c = 3, d_r = 2: the only pair has inverse frequency theta^0 = 1, so the row written
+    # at position 1 has its k^R turned by exactly 1 radian, whatever theta is; c^KV stays.
+    rows, pos = O.append_latent_rows([[1.0, 2.0, 3.0, 1.0, 0.0]], start=1, theta=10000.0, d_r=2)
+    assert list(pos) == [1]
+    np.testing.assert_array_equal(rows[0, :3], [1.0, 2.0, 3.0])
+    np.testing.assert_allclose(rows[0, 3:], [math.cos(1.0), math.sin(1.0)], rtol=0, atol=1e-15)
+
+
+def test_append_without_rope_keeps_rows_and_counts_positions():
+    new = np.arange(3 * 576, dtype=np.float64).reshape(3, 576)
+    rows, pos = O.append_latent_rows(new, start=7)
+    np.testing.assert_array_equal(rows, new)
+    assert list(pos) == [7, 8, 9]
+
+
+def test_append_all_at_once_equals_one_by_one():
+    rng = np.random.default_rng(5)
+    new = rng.standard_normal((4, 576))
+    rows, pos = O.append_latent_rows(new, start=100, theta=10000.0)
+    for s in range(4):
+        r1, p1 = O.append_latent_rows(new[s:s + 1], start=100 + s, theta=10000.0)
+        np.testing.assert_array_equal(r1[0], rows[s])
+        assert p1[0] == pos[s]
+
+
+def test_append_planted_wrong_position_is_caught():
+    # Rotating at start - 1 (an off-by-one in the position) moves the stored k^R.
+    new = np.zeros((1, 576))
+    new[0, 512] = 1.0
+    good, _ = O.append_latent_rows(new, start=3, theta=10000.0)
+    bad = new.copy()
+    bad[:, 512:] = O.rope_interleaved(bad[:, 512:], np.array([2]), 10000.0)
+    assert not np.allclose(good, bad)
+    np.testing.assert_allclose(good[0, 512:514], [math.cos(3.0), math.sin(3.0)], atol=1e-15)
