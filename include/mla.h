@@ -15,6 +15,9 @@
  *   mla_rope_inplace   RoPE on the 64-wide rope slice of cache rows or queries
  *   mla_append_latent  the step's new latent rows into the cache (k^R rotated), before
  *                      the decode reads it
+ *   mla_fuse_weights, mla_absorb_q_fused, mla_out_proj_fused
+ *                      the projections multiplied together ahead of time, and the two
+ *                      decode-time products that use them
  *
  * Conventions shared by every call
  *   - Dimensions are fixed: d_c = 512 (latent), d_r = 64 (decoupled RoPE key),
@@ -264,6 +267,49 @@ mla_status mla_append_latent(const mla_bf16* rows, int B, int S, float rope_thet
  */
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream);
+
+/*
+ * Pre-fused weights, [CALC] "Query·출력 투영과 합치기": once the key projection is moved to
+ * the query side and the value projection behind the weighted sum, each can be multiplied
+ * ahead of time into its neighbour: the query projection (U^Q (U^K)^T, so the content
+ * query comes straight from the query latent c^Q) and the output projection (U^V W^O per
+ * head; the heads' contributions are summed).  The RoPE query path stays separate.
+ *
+ * mla_fuse_weights -- the offline products, bf16 out (fp32 accumulation):
+ *   W_UQK[h] = W_UQ[h] W_UK[h]^T   [d_cq x 512]      W_UVO[h] = W_UV[h] W_O[h]   [512 x d_model]
+ *   w_uq  bf16 [H, d_cq, 128]   (q_nope[h] = c^Q W_UQ[h])
+ *   w_uk  bf16 [H, 512, 128]    w_uv bf16 [H, 512, 128]   (as for mla_absorb_q / mla_out_proj_uv)
+ *   w_o   bf16 [H, 128, d_model] (the head-h rows of the output projection W^O)
+ *   w_uqk bf16 [H, d_cq, 512] out;   w_uvo bf16 [H, 512, d_model] out
+ *   d_cq a multiple of 64 (1536 for DeepSeek-V3), d_model a multiple of 128.
+ */
+mla_status mla_fuse_weights(const mla_bf16* w_uq, const mla_bf16* w_uk, const mla_bf16* w_uv,
+                            const mla_bf16* w_o, int H, int d_cq, int d_model, mla_bf16* w_uqk,
+                            mla_bf16* w_uvo, mla_stream stream);
+
+/*
+ * mla_absorb_q_fused -- key absorption from the query latent with the fused weights:
+ *   q_cat[b,s,h, 0:512]   = bf16( c_q[b,s,:] W_UQK[h] )                   (fp32 accumulate)
+ *   q_cat[b,s,h, 512:576] = bf16( RoPE(q_rope[b,s,h,:], q_pos[b,s]) ), or q_rope as given
+ *   c_q bf16 [B,S,d_cq]; q_rope bf16 [B,S,H,64]; w_uqk bf16 [H,d_cq,512]; q_cat as mla_absorb_q.
+ */
+mla_status mla_absorb_q_fused(const mla_bf16* c_q, const mla_bf16* q_rope, const mla_bf16* w_uqk,
+                              const int32_t* q_pos, float rope_theta, int B, int S, int H, int d_cq,
+                              mla_bf16* q_cat, mla_stream stream);
+
+/* Device scratch mla_out_proj_fused needs: a bf16 copy of o_lat, B*S*H*512*2 bytes. */
+size_t mla_out_proj_fused_workspace_bytes(int B, int S, int H);
+
+/*
+ * mla_out_proj_fused -- the attention output through the fused output weights, summed over
+ * the heads:  out[b,s,:] = sum_h bf16(o_lat[b,s,h,:]) W_UVO[h]   (fp32 accumulate)
+ *   o_lat fp32 [B,S,H,512]; w_uvo bf16 [H,512,d_model]; out fp32 [B,S,d_model]
+ *   workspace: mla_out_proj_fused_workspace_bytes(B,S,H) bytes of device scratch.
+ * The sum over the H*512 products is split into parts added with fp32 atomics, so the
+ * last bits of `out` may differ between calls.
+ */
+mla_status mla_out_proj_fused(const float* o_lat, const mla_bf16* w_uvo, int B, int S, int H, int d_model,
+                              float* out, void* workspace, size_t workspace_bytes, mla_stream stream);
 
 /*
  * mla_debug_inject_timeout -- test hook for the device-side failure path (not a step of

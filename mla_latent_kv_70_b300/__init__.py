@@ -41,6 +41,10 @@ SIGNATURES = {
     "mla_rope_inplace": (_I, [_P, _I64, _I64, _I, _P, _F, _P]),
     "mla_debug_inject_timeout": (_I, [_I, ctypes.c_double]),
     "mla_append_latent": (_I, [_P, _I, _I, _F, _P, _P, _I64, _P, _I, _I, _I, _P, _P]),
+    "mla_fuse_weights": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P, _P]),
+    "mla_absorb_q_fused": (_I, [_P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P]),
+    "mla_out_proj_fused_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "mla_out_proj_fused": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
 }
 
 _LIB = None
@@ -186,6 +190,38 @@ def mla_append_latent(rows, seqlens, kv, *, rope_theta=0.0, block_table=None, kv
         _ptr(rows, _BF16), B, S, float(rope_theta), _ptr(seqlens, _I32), _ptr(kv, _BF16),
         int(kv_seq_stride), _ptr(block_table, _I32), max_pages, page_size, num_pages,
         _ptr(status, _I32), _stream(stream)))
+
+
+def mla_fuse_weights(w_uq, w_uk, w_uv, w_o, w_uqk, w_uvo, stream=None):
+    """W_UQK[h] = W_UQ[h] W_UK[h]^T and W_UVO[h] = W_UV[h] W_O[h] (bf16 outputs)."""
+    H, d_cq, _ = w_uq.shape
+    d_model = w_o.shape[2]
+    _check("mla_fuse_weights", lib().mla_fuse_weights(
+        _ptr(w_uq, _BF16), _ptr(w_uk, _BF16), _ptr(w_uv, _BF16), _ptr(w_o, _BF16), H, d_cq, d_model,
+        _ptr(w_uqk, _BF16), _ptr(w_uvo, _BF16), _stream(stream)))
+
+
+def mla_absorb_q_fused(c_q, q_rope, w_uqk, q_pos, rope_theta, q_cat, stream=None):
+    """q_cat[b,s,h] = [c_q[b,s] . W_UQK[h] | RoPE(q_rope[b,s,h], q_pos[b,s])]."""
+    B, S, H, _ = q_rope.shape
+    d_cq = c_q.shape[2]
+    _check("mla_absorb_q_fused", lib().mla_absorb_q_fused(
+        _ptr(c_q, _BF16), _ptr(q_rope, _BF16), _ptr(w_uqk, _BF16), _ptr(q_pos, _I32), float(rope_theta),
+        B, S, H, d_cq, _ptr(q_cat, _BF16), _stream(stream)))
+
+
+def mla_out_proj_fused_workspace_bytes(B, S, H) -> int:
+    return int(lib().mla_out_proj_fused_workspace_bytes(B, S, H))
+
+
+def mla_out_proj_fused(o_lat, w_uvo, out, workspace, stream=None):
+    """out[b,s] = sum_h o_lat[b,s,h] . W_UVO[h] (fp32)."""
+    B, S, H, _ = o_lat.shape
+    d_model = w_uvo.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mla_out_proj_fused", lib().mla_out_proj_fused(
+        _ptr(o_lat, _F32), _ptr(w_uvo, _BF16), B, S, H, d_model, _ptr(out, _F32), _ptr(workspace),
+        ws_bytes, _stream(stream)))
 
 
 def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):

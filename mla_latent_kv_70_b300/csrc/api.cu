@@ -202,6 +202,99 @@ mla_status mla_append_latent(const mla_bf16* rows, int B, int S, float rope_thet
       static_cast<cudaStream_t>(stream)));
 }
 
+static inline int round16(int x) { return (x + 15) & ~15; }
+
+mla_status mla_fuse_weights(const mla_bf16* w_uq, const mla_bf16* w_uk, const mla_bf16* w_uv,
+                            const mla_bf16* w_o, int H, int d_cq, int d_model, mla_bf16* w_uqk,
+                            mla_bf16* w_uvo, mla_stream stream) {
+  if (!w_uq || !w_uk || !w_uv || !w_o || !w_uqk || !w_uvo) return MLA_ERR_INVALID;
+  if (!aligned16(w_uq) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(w_o) || !aligned16(w_uqk) ||
+      !aligned16(w_uvo))
+    return MLA_ERR_INVALID;
+  if (H < 1 || d_cq < 64 || d_model < 128) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || d_cq % 64 || d_model % 128) return MLA_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // W_UQK[h][i, c] = sum_d W_UQ[h][i, d] W_UK[h][c, d]: m = c (512), n = i (d_cq), k = d.
+  {
+    const mla::GemmOperand a{w_uk, (uint64_t)H * kDc, (uint64_t)mla::kDn, (uint64_t)mla::kDn, 0};
+    const mla::GemmOperand b{w_uq, (uint64_t)H * d_cq, (uint64_t)mla::kDn, (uint64_t)mla::kDn, 0};
+    mla::GemmShape g{};
+    g.M = kDc, g.N = d_cq, g.K = mla::kDn, g.batches = H, g.n_tile = d_cq % 256 ? 64 : 256, g.k_splits = 1;
+    g.a_batch_rows = kDc, g.b_batch_rows = d_cq;
+    g.c = w_uqk, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = kDc, g.ldc_batch = (int64_t)d_cq * kDc;
+    const mla_status r = launch_status(mla::launch_gemm(a, b, g, st));
+    if (r != MLA_OK) return r;
+  }
+  // W_UVO[h][c, j] = sum_v W_UV[h][c, v] W_O[h][v, j]: m = j (d_model), n = c (512), k = v.
+  const mla::GemmOperand a{w_o, (uint64_t)H * mla::kDv, (uint64_t)d_model, (uint64_t)d_model, 1};
+  const mla::GemmOperand b{w_uv, (uint64_t)H * kDc, (uint64_t)mla::kDv, (uint64_t)mla::kDv, 0};
+  mla::GemmShape g{};
+  g.M = d_model, g.N = kDc, g.K = mla::kDv, g.batches = H, g.n_tile = 256, g.k_splits = 1;
+  g.a_batch_rows = mla::kDv, g.b_batch_rows = kDc;
+  g.c = w_uvo, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = d_model, g.ldc_batch = (int64_t)kDc * d_model;
+  return launch_status(mla::launch_gemm(a, b, g, st));
+}
+
+mla_status mla_absorb_q_fused(const mla_bf16* c_q, const mla_bf16* q_rope, const mla_bf16* w_uqk,
+                              const int32_t* q_pos, float rope_theta, int B, int S, int H, int d_cq,
+                              mla_bf16* q_cat, mla_stream stream) {
+  if (!c_q || !q_rope || !w_uqk || !q_cat) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1 || d_cq < 64) return MLA_ERR_INVALID;
+  if (!aligned16(c_q) || !aligned16(q_rope) || !aligned16(w_uqk) || !aligned16(q_cat)) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4 || d_cq % 64) return MLA_ERR_UNSUPPORTED;
+  if (q_pos && !(rope_theta > 0.f)) return MLA_ERR_INVALID;
+  const int rows = B * S;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // q~[r, h, c] = sum_i c_q[r, i] W_UQK[h][i, c]: m = c (512), n = r, k = i (d_cq).
+  const mla::GemmOperand a{w_uqk, (uint64_t)H * d_cq, (uint64_t)kDc, (uint64_t)kDc, 1};
+  const mla::GemmOperand b{c_q, (uint64_t)rows, (uint64_t)d_cq, (uint64_t)d_cq, 0};
+  mla::GemmShape g{};
+  g.M = kDc, g.N = rows, g.K = d_cq, g.batches = H, g.n_tile = rows >= 256 ? 256 : round16(rows), g.k_splits = 1;
+  g.a_batch_rows = d_cq, g.b_batch_rows = 0;
+  g.c = q_cat, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = (int64_t)H * kRow, g.ldc_batch = kRow;
+  mla_status r = launch_status(mla::launch_gemm(a, b, g, st));
+  if (r != MLA_OK) return r;
+  const mla::RopeFreqs f = mla::make_rope_freqs(q_pos ? rope_theta : 10000.f);
+  return launch_status(mla::launch_rope_slice(reinterpret_cast<const __nv_bfloat16*>(q_rope), q_pos, f, rows, H,
+                                              reinterpret_cast<__nv_bfloat16*>(q_cat), st));
+}
+
+size_t mla_out_proj_fused_workspace_bytes(int B, int S, int H) {
+  if (B < 1 || S < 1 || H < 1) return 0;
+  return (size_t)B * S * H * kDc * 2;
+}
+
+mla_status mla_out_proj_fused(const float* o_lat, const mla_bf16* w_uvo, int B, int S, int H, int d_model,
+                              float* out, void* workspace, size_t workspace_bytes, mla_stream stream) {
+  if (!o_lat || !w_uvo || !out) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || H < 1 || d_model < 128) return MLA_ERR_INVALID;
+  if (!aligned16(o_lat) || !aligned16(w_uvo) || !aligned16(out)) return MLA_ERR_INVALID;
+  if (!heads_ok(H) || S > 4 || d_model % 128) return MLA_ERR_UNSUPPORTED;
+  const size_t need = mla_out_proj_fused_workspace_bytes(B, S, H);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
+  const int rows = B * S;
+  const int K = H * kDc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The tensor core takes o_lat in bf16 (as mla_out_proj_uv does).
+  mla_status r = launch_status(mla::launch_f32_to_bf16(o_lat, (int64_t)rows * K,
+                                                       static_cast<__nv_bfloat16*>(workspace), st));
+  if (r != MLA_OK) return r;
+  // out[r, j] = sum_(h,c) o_lat[r, h, c] W_UVO[h][c, j]: m = j (d_model), n = r, k = (h, c),
+  // split along k to fill the device, the parts added into the zeroed output.
+  const mla::GemmOperand a{w_uvo, (uint64_t)K, (uint64_t)d_model, (uint64_t)d_model, 1};
+  const mla::GemmOperand b{workspace, (uint64_t)rows, (uint64_t)K, (uint64_t)K, 0};
+  mla::GemmShape g{};
+  g.M = d_model, g.N = rows, g.K = K, g.batches = 1, g.n_tile = rows >= 256 ? 256 : round16(rows);
+  const int tiles = (d_model / 128) * ((rows + g.n_tile - 1) / g.n_tile);
+  const int sms = mla::device_sm_count() > 0 ? mla::device_sm_count() : 148;
+  g.k_splits = std::max(1, std::min(K / 64, 2 * sms / tiles));
+  g.a_batch_rows = 0, g.b_batch_rows = 0;
+  g.c = out, g.out_bf16 = 0, g.ldc_m = 1, g.ldc_n = d_model, g.ldc_batch = 0;
+  if (g.k_splits > 1 && cudaMemsetAsync(out, 0, (size_t)rows * d_model * sizeof(float), st) != cudaSuccess)
+    return launch_status(cudaErrorUnknown);
+  return launch_status(mla::launch_gemm(a, b, g, st));
+}
+
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream) {
   if (!x || !pos || rows < 0 || col_offset < 0 || row_stride < col_offset + mla::kDr)

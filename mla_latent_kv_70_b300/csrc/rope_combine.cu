@@ -34,6 +34,32 @@ __global__ void k_rope_inplace(__nv_bfloat16* __restrict__ x, int64_t row_stride
   *p = f2_to_bf2(y.x, y.y);
 }
 
+// The RoPE slice of q_cat rows, q_cat[r, h, 512:576] = RoPE(q_rope[r, h], q_pos[r]) (or a
+// copy without positions): one thread per 16-byte piece (4 pairs).
+__global__ void k_rope_slice(const __nv_bfloat16* __restrict__ q_rope, const int32_t* __restrict__ q_pos,
+                             RopeFreqs f, int M, int H, __nv_bfloat16* __restrict__ q_cat) {
+  grid_dep_launch();
+  grid_dep_wait();
+  constexpr int kPieces = kDr * 2 / 16;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)M * H * kPieces) return;
+  const int64_t mh = idx / kPieces;
+  const int piece = (int)(idx % kPieces);
+  uint4 v = reinterpret_cast<const uint4*>(q_rope + mh * kDr)[piece];
+  if (q_pos) {
+    const int pos = q_pos[mh / H];
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 x = bf2_to_f2(w[j]);
+      const float2 y = rope_pair(x.x, x.y, pos, f.hi[4 * piece + j], f.lo[4 * piece + j]);
+      w[j] = f2_to_bf2(y.x, y.y);
+    }
+    v = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  reinterpret_cast<uint4*>(q_cat + mh * kRow + kDc)[piece] = v;
+}
+
 // One CTA of 128 threads per output row: weights exp(lse_k - max) are formed once in
 // shared memory, then each thread merges one float4 of the 512-wide latent row.
 __global__ void __launch_bounds__(128)
@@ -87,6 +113,15 @@ cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t ro
   k_rope_inplace<<<(unsigned)((n + threads - 1) / threads), threads, 0, st>>>(
       x, row_stride, rows, col_offset, pos, f);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rope_slice(const __nv_bfloat16* q_rope, const int32_t* q_pos, const RopeFreqs& f, int M,
+                              int H, __nv_bfloat16* q_cat, cudaStream_t st) {
+  const int64_t n = (int64_t)M * H * (kDr * 2 / 16);
+  if (n == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(k_rope_slice, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, q_rope, q_pos, f,
+                             M, H, q_cat);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,

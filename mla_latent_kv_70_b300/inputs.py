@@ -25,6 +25,8 @@ D_R = 64
 D_NOPE = 128
 D_V = 128
 ROW = D_C + D_R
+D_CQ = 1536      # query latent width of DeepSeek-V3 (the pages' module: d_c' = 1536)
+D_MODEL = 4096   # model width of the pages' module
 
 
 def _gen(seed: int, stream: str, index: int = 0) -> torch.Generator:
@@ -187,6 +189,26 @@ def pool_positions(case: DecodeCase) -> torch.Tensor:
             page = int(case.block_table[b, i])
             pos[page * case.page_size:(page + 1) * case.page_size] = i * case.page_size + r
     return pos
+
+
+def query_side_weights(case: DecodeCase, d_cq: int = D_CQ):
+    """W_UQ bf16 [H, d_cq, 128], std 1/sqrt(d_cq) (q_nope[h] = c^Q W_UQ[h])."""
+    return randn_bf16((case.H, d_cq, D_NOPE), case.seed, "wuq", 0, 1.0 / math.sqrt(d_cq))
+
+
+def output_weights(case: DecodeCase, d_model: int = D_MODEL):
+    """W_O bf16 [H, 128, d_model], std 1/sqrt(H*128): head h's rows of the output projection."""
+    return randn_bf16((case.H, D_V, d_model), case.seed, "wo", 0, 1.0 / math.sqrt(case.H * D_V))
+
+
+def seq_c_q(case: DecodeCase, b: int, d_cq: int = D_CQ) -> torch.Tensor:
+    """bf16 [S, d_cq] query latents c^Q of sequence b, N(0, 1)."""
+    return randn_bf16((case.S, d_cq), case.seed, "cq", b)
+
+
+def c_q(case: DecodeCase, d_cq: int = D_CQ) -> torch.Tensor:
+    """bf16 [B, S, d_cq]: seq_c_q of every sequence."""
+    return torch.stack([seq_c_q(case, b, d_cq) for b in range(case.B)])
 
 
 def queries(case: DecodeCase):

@@ -45,6 +45,11 @@ __all__ = [
     "out_proj_uv",
     "gather_paged_rows",
     "append_latent_rows",
+    "fuse_query_weights",
+    "fuse_output_weights",
+    "absorb_q_from_latent",
+    "out_proj_fused",
+    "out_proj_heads",
     "cache_values_per_token",
     "cache_bytes_per_token",
     "compression_ratio",
@@ -250,6 +255,45 @@ def out_proj_uv(o_lat: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
     """
     return np.einsum("...hc,hcv->...hv", np.asarray(o_lat, np.float64),
                      np.asarray(w_uv, np.float64))
+
+
+# ----------------------------------------------------------------------------
+# Pre-fused weights ([CALC] "Query·출력 투영과 합치기")
+# ----------------------------------------------------------------------------
+
+def fuse_query_weights(w_uq, w_uk):
+    """W_UQK[h] = W_UQ[h] W_UK[h]^T, the query projection and the transposed key
+    projection multiplied ahead of time ([CALC] "Query·출력 투영과 합치기": U^Q is 3x2 and
+    (U^K)^T 2x3 in the toy, so their product is a 3x3 matrix that takes c^Q straight to
+    q~).  w_uq [H, d_cq, d_k]; w_uk [H, d_c, d_k] -> [H, d_cq, d_c]."""
+    return np.einsum("hik,hck->hic", np.asarray(w_uq, np.float64), np.asarray(w_uk, np.float64))
+
+
+def fuse_output_weights(w_uv, w_o):
+    """W_UVO[h] = W_UV[h] W_O[h], the value projection multiplied into head h's rows of
+    the output projection ([CALC] "Query·출력 투영과 합치기": U^V 3x2 times W^O_1 2x8 gives
+    the 3x8 matrix that takes z to head 1's contribution to the model dimension).
+    w_uv [H, d_c, d_v]; w_o [H, d_v, d_model] -> [H, d_c, d_model]."""
+    return np.einsum("hcv,hvj->hcj", np.asarray(w_uv, np.float64), np.asarray(w_o, np.float64))
+
+
+def absorb_q_from_latent(c_q, w_uqk):
+    """q~[..., h, :] = c^Q[..., :] W_UQK[h]: the content query of every head taken from the
+    query latent in one product.  c_q [..., d_cq]; w_uqk [H, d_cq, d_c] -> [..., H, d_c]."""
+    return np.einsum("...i,hic->...hc", np.asarray(c_q, np.float64), np.asarray(w_uqk, np.float64))
+
+
+def out_proj_fused(o_lat, w_uvo):
+    """out[..., :] = sum_h z_h W_UVO[h]: every head's contribution to the model dimension,
+    summed ([CALC] "Query·출력 투영과 합치기": the heads' contributions add up to the whole
+    output projection).  o_lat [..., H, d_c]; w_uvo [H, d_c, d_model] -> [..., d_model]."""
+    return np.einsum("...hc,hcj->...j", np.asarray(o_lat, np.float64), np.asarray(w_uvo, np.float64))
+
+
+def out_proj_heads(o, w_o):
+    """The output projection of per-head outputs: out = sum_h o_h W_O[h] (the unfused
+    order).  o [..., H, d_v]; w_o [H, d_v, d_model] -> [..., d_model]."""
+    return np.einsum("...hv,hvj->...j", np.asarray(o, np.float64), np.asarray(w_o, np.float64))
 
 
 # ----------------------------------------------------------------------------

@@ -420,3 +420,71 @@ def test_append_planted_wrong_position_is_caught():
     bad[:, 512:] = O.rope_interleaved(bad[:, 512:], np.array([2]), 10000.0)
     assert not np.allclose(good, bad)
     np.testing.assert_allclose(good[0, 512:514], [math.cos(3.0), math.sin(3.0)], atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# Pre-fused weights ([CALC] "Query·출력 투영과 합치기")
+# ----------------------------------------------------------------------------
+
+def _toy_projections():
+    # The pages' toy head 1: d_c = 3, d_k = d_v = 2.  U^K picks the first two latent
+    # components ([CALC] "Key 투영을 Query 쪽으로 옮기기"); U^V makes [c0 + c2, c1] ([CALC]
+    # "Value 투영을 가중합 뒤로 옮기기").  U^Q (3x2) is not printed; this one takes
+    # c^Q = [2, 1, 0] to the pages' content query q = [2, 1].
+    u_k = np.array([[[1.0, 0.0], [0.0, 1.0], [0.0, 0.0]]])
+    u_v = np.array([[[1.0, 0.0], [0.0, 1.0], [1.0, 0.0]]])
+    u_q = np.array([[[1.0, 0.0], [0.0, 1.0], [0.0, 0.0]]])
+    return u_q, u_k, u_v
+
+
+def test_fused_query_weights_reproduce_the_toy_q_tilde():
+    u_q, u_k, _ = _toy_projections()
+    w = O.fuse_query_weights(u_q, u_k)
+    assert w.shape == (1, 3, 3)                       # 3x2 times 2x3
+    q_tilde = O.absorb_q_from_latent(np.array([2.0, 1.0, 0.0]), w)
+    np.testing.assert_array_equal(q_tilde[0], [2.0, 1.0, 0.0])     # the pages' q~
+    assert q_tilde[0] @ np.array([1.0, 2.0, 3.0]) == 4.0           # q~ . c_3 = 4
+
+
+def test_fused_output_weights_on_the_value_toy():
+    # z = [0.8, 1.3, 1.5] ([CALC] value-absorption table) through U^V gives [2.3, 1.3];
+    # with a W^O_1 of 2x8 that copies the two head outputs into model columns 0 and 5
+    # and their sum into column 7, the fused 3x8 matrix gives head 1's 1x8 contribution.
+    _, _, u_v = _toy_projections()
+    w_o = np.zeros((1, 2, 8))
+    w_o[0, 0, 0] = w_o[0, 1, 5] = w_o[0, 0, 7] = w_o[0, 1, 7] = 1.0
+    w = O.fuse_output_weights(u_v, w_o)
+    assert w.shape == (1, 3, 8)
+    out = O.out_proj_fused(np.array([[0.8, 1.3, 1.5]]), w)
+    expect = np.zeros(8)
+    expect[0], expect[5], expect[7] = 2.3, 1.3, 3.6
+    np.testing.assert_allclose(out, expect, rtol=0, atol=1e-15)
+
+
+def test_fused_forms_equal_the_two_step_products_brute_force():
+    rng = np.random.default_rng(9)
+    H, d_cq, d_c, d_k, d_model = 3, 5, 4, 2, 6
+    w_uq, w_uk = rng.standard_normal((H, d_cq, d_k)), rng.standard_normal((H, d_c, d_k))
+    w_uv, w_o = rng.standard_normal((H, d_c, d_k)), rng.standard_normal((H, d_k, d_model))
+    c_q, z = rng.standard_normal(d_cq), rng.standard_normal((H, d_c))
+    wq, wo = O.fuse_query_weights(w_uq, w_uk), O.fuse_output_weights(w_uv, w_o)
+    for h in range(H):                    # scalar loops: q~ = (c_q W_UQ[h]) W_UK[h]^T
+        q = [sum(c_q[i] * w_uq[h, i, k] for i in range(d_cq)) for k in range(d_k)]
+        qt = [sum(q[k] * w_uk[h, c, k] for k in range(d_k)) for c in range(d_c)]
+        np.testing.assert_allclose(O.absorb_q_from_latent(c_q, wq)[h], qt, rtol=1e-12)
+    out = np.zeros(d_model)
+    for h in range(H):                    # out = sum_h (z_h W_UV[h]) W_O[h]
+        v = [sum(z[h, c] * w_uv[h, c, k] for c in range(d_c)) for k in range(d_k)]
+        out += [sum(v[k] * w_o[h, k, j] for k in range(d_k)) for j in range(d_model)]
+    np.testing.assert_allclose(O.out_proj_fused(z, wo), out, rtol=1e-12)
+    np.testing.assert_allclose(O.out_proj_heads(O.out_proj_uv(z, w_uv), w_o), out, rtol=1e-12)
+
+
+def test_fused_planted_transpose_is_caught():
+    # Multiplying W_UQ by W_UK without the transpose (a wrong index) changes q~.
+    rng = np.random.default_rng(3)
+    w_uq, w_uk = rng.standard_normal((1, 4, 4)), rng.standard_normal((1, 4, 4))
+    c_q = rng.standard_normal(4)
+    good = O.absorb_q_from_latent(c_q, O.fuse_query_weights(w_uq, w_uk))
+    bad = np.einsum("i,hic->hc", c_q, np.einsum("hik,hkc->hic", w_uq, w_uk))
+    assert not np.allclose(good, bad)
