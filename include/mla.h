@@ -18,6 +18,7 @@
  *   mla_fuse_weights, mla_absorb_q_fused, mla_out_proj_fused
  *                      the projections multiplied together ahead of time, and the two
  *                      decode-time products that use them
+ *   mla_prefill        prefill / chunked prefill in the expanded order (per-head K, V built)
  *
  * Conventions shared by every call
  *   - Dimensions are fixed: d_c = 512 (latent), d_r = 64 (decoupled RoPE key),
@@ -310,6 +311,30 @@ size_t mla_out_proj_fused_workspace_bytes(int B, int S, int H);
  */
 mla_status mla_out_proj_fused(const float* o_lat, const mla_bf16* w_uvo, int B, int S, int H, int d_model,
                               float* out, void* workspace, size_t workspace_bytes, mla_stream stream);
+
+/*
+ * mla_prefill -- attention of T_q query tokens per sequence (a whole prompt, or a chunk
+ * of one) in the expanded order: [MLA] (prefill vs. decode) and [CALC]
+ * "계산 재배치의 효과와 한계": when many queries share the keys, building the per-head keys
+ * and values once costs less than d_c-wide absorbed dot products, so prefill may keep
+ * that order.  For each sequence b and head h:
+ *   K_h[t] = c_t W_UK[h],  V_h[t] = c_t W_UV[h]          (bf16, fp32 accumulation)
+ *   x_ij = scale * (q_nope[b,i,h] . K_h[j] + q_rope[b,i,h] . k^R_j)
+ *   query i is the row at position T_kv - T_q + i and reads rows j <= T_kv - T_q + i
+ *   o[b,i,h,:] = sum_j softmax_j(x_ij) V_h[j],  lse[b,i,h] = ln sum_j exp(x_ij)
+ *
+ *   q_nope bf16 [B,T_q,H,128]; q_rope bf16 [B,T_q,H,64], already rotated at the query
+ *   positions (mla_rope_inplace); kv the contiguous cache [B, kv_seq_stride, 576] whose
+ *   first T_kv rows per sequence are read (k^R already rotated); w_uk, w_uv [H,512,128];
+ *   o fp32 [B,T_q,H,128]; lse fp32 [B,T_q,H]; 1 <= T_q <= T_kv <= kv_seq_stride.
+ *   workspace: mla_prefill_workspace_bytes(B, kv_seq_stride, H) bytes, which hold K_h and
+ *   V_h of every cache row of the B sequences.
+ */
+size_t mla_prefill_workspace_bytes(int B, int64_t kv_seq_stride, int H);
+mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* kv, int64_t kv_seq_stride,
+                       int T_kv, const mla_bf16* w_uk, const mla_bf16* w_uv, int B, int T_q, int H, float scale,
+                       float* o, float* lse, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                       mla_stream stream);
 
 /*
  * mla_debug_inject_timeout -- test hook for the device-side failure path (not a step of

@@ -45,6 +45,8 @@ SIGNATURES = {
     "mla_absorb_q_fused": (_I, [_P, _P, _P, _P, _F, _I, _I, _I, _I, _P, _P]),
     "mla_out_proj_fused_workspace_bytes": (_SZ, [_I, _I, _I]),
     "mla_out_proj_fused": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mla_prefill_workspace_bytes": (_SZ, [_I, _I64, _I]),
+    "mla_prefill": (_I, [_P, _P, _P, _I64, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P, _P]),
 }
 
 _LIB = None
@@ -222,6 +224,23 @@ def mla_out_proj_fused(o_lat, w_uvo, out, workspace, stream=None):
     _check("mla_out_proj_fused", lib().mla_out_proj_fused(
         _ptr(o_lat, _F32), _ptr(w_uvo, _BF16), B, S, H, d_model, _ptr(out, _F32), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def mla_prefill_workspace_bytes(B, kv_seq_stride, H) -> int:
+    return int(lib().mla_prefill_workspace_bytes(B, int(kv_seq_stride), H))
+
+
+def mla_prefill(q_nope, q_rope, kv, T_kv, w_uk, w_uv, o, lse, *, scale, workspace, status=None,
+                stream=None):
+    """Causal attention of the T_q query tokens (the last T_q of T_kv positions) of each
+    sequence over expanded per-head keys/values; writes o [B,T_q,H,128] and lse [B,T_q,H]."""
+    B, T_q, H, _ = q_nope.shape
+    stride = kv.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("mla_prefill", lib().mla_prefill(
+        _ptr(q_nope, _BF16), _ptr(q_rope, _BF16), _ptr(kv, _BF16), int(stride), int(T_kv), _ptr(w_uk, _BF16),
+        _ptr(w_uv, _BF16), B, T_q, H, float(scale), _ptr(o, _F32), _ptr(lse, _F32), _ptr(workspace), ws_bytes,
+        _ptr(status, _I32), _stream(stream)))
 
 
 def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):

@@ -295,6 +295,48 @@ mla_status mla_out_proj_fused(const float* o_lat, const mla_bf16* w_uvo, int B, 
   return launch_status(mla::launch_gemm(a, b, g, st));
 }
 
+size_t mla_prefill_workspace_bytes(int B, int64_t kv_seq_stride, int H) {
+  if (B < 1 || kv_seq_stride < 1 || H < 1) return 0;
+  return 2 * (size_t)B * (size_t)kv_seq_stride * (size_t)H * mla::kDn * 2;
+}
+
+mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* kv, int64_t kv_seq_stride,
+                       int T_kv, const mla_bf16* w_uk, const mla_bf16* w_uv, int B, int T_q, int H, float scale,
+                       float* o, float* lse, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                       mla_stream stream) {
+  if (!q_nope || !q_rope || !kv || !w_uk || !w_uv || !o || !lse) return MLA_ERR_INVALID;
+  if (B < 1 || H < 1 || T_q < 1 || T_kv < T_q || kv_seq_stride < T_kv) return MLA_ERR_INVALID;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(kv) || !aligned16(w_uk) || !aligned16(w_uv) ||
+      !aligned16(o))
+    return MLA_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MLA_ERR_INVALID;
+  if (!heads_ok(H)) return MLA_ERR_UNSUPPORTED;
+  if ((uint64_t)B * (uint64_t)kv_seq_stride > 0x7FFFFFFFull || (int64_t)B * T_q > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
+  const size_t need = mla_prefill_workspace_bytes(B, kv_seq_stride, H);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint64_t rows = (uint64_t)B * (uint64_t)kv_seq_stride;
+  __nv_bfloat16* k_exp = static_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* v_exp = k_exp + rows * (uint64_t)H * mla::kDn;
+  // K_h[t] = c_t W_UK[h], V_h[t] = c_t W_UV[h]: m = output column (128), n = cache row t,
+  // k = latent column (512); the weights are read MN-major, the cache rows K-major.
+  for (int which = 0; which < 2; ++which) {
+    const mla::GemmOperand a{which ? w_uv : w_uk, (uint64_t)H * kDc, (uint64_t)mla::kDn, (uint64_t)mla::kDn, 1};
+    const mla::GemmOperand b{kv, rows, (uint64_t)kRow, (uint64_t)kRow, 0};
+    mla::GemmShape g{};
+    g.M = mla::kDn, g.N = (int)rows, g.K = kDc, g.batches = H, g.n_tile = 256, g.k_splits = 1;
+    g.a_batch_rows = kDc, g.b_batch_rows = 0;
+    g.c = which ? v_exp : k_exp, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = (int64_t)H * mla::kDn, g.ldc_batch = mla::kDn;
+    g.status = status_dev;
+    const mla_status r = launch_status(mla::launch_gemm(a, b, g, st));
+    if (r != MLA_OK) return r;
+  }
+  return launch_status(mla::launch_prefill_attn(
+      reinterpret_cast<const __nv_bfloat16*>(q_nope), reinterpret_cast<const __nv_bfloat16*>(q_rope),
+      reinterpret_cast<const __nv_bfloat16*>(kv), kv_seq_stride, k_exp, v_exp, B, T_q, T_kv, H, scale, o, lse,
+      status_dev, st));
+}
+
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream) {
   if (!x || !pos || rows < 0 || col_offset < 0 || row_stride < col_offset + mla::kDr)

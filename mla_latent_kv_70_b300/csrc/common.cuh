@@ -185,6 +185,11 @@ cudaError_t launch_f32_to_bf16(const float* x, int64_t n, __nv_bfloat16* y, cuda
 cudaError_t launch_rope_slice(const __nv_bfloat16* q_rope, const int32_t* q_pos, const RopeFreqs& f, int M,
                               int H, __nv_bfloat16* q_cat, cudaStream_t st);
 
+cudaError_t launch_prefill_attn(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_rope,
+                                const __nv_bfloat16* kv, int64_t kv_seq_stride, const __nv_bfloat16* k_exp,
+                                const __nv_bfloat16* v_exp, int B, int T_q, int T_kv, int H, float scale,
+                                float* o, float* lse, int32_t* status, cudaStream_t st);
+
 // Launchers (defined next to their kernels).
 cudaError_t launch_absorb_q(const __nv_bfloat16* q_nope, const __nv_bfloat16* q_rope,
                             const __nv_bfloat16* w_uk, const int32_t* q_pos, const RopeFreqs& f,

@@ -152,3 +152,22 @@ def test_timeout_hook_rejects_bad_arguments(lib):
     assert lib.mla_debug_inject_timeout(1, ctypes.c_double(0.0)) == 1        # no wait limit
     assert lib.mla_debug_inject_timeout(1, ctypes.c_double(5000.0)) == 1     # beyond 2 s
     assert lib.mla_debug_inject_timeout(0, ctypes.c_double(0.0)) == 0        # off
+
+
+def test_prefill_and_fused_calls_reject_bad_shapes(lib):
+    f = ctypes.c_float
+
+    def prefill(**kw):
+        a = dict(qn=P, qr=P, kv=P, stride=128, T_kv=100, wuk=P, wuv=P, B=1, T_q=10, H=16, scale=f(0.07),
+                 o=P, lse=P, ws=P, ws_bytes=1 << 30, status=None, stream=None)
+        a.update(kw)
+        return lib.mla_prefill(*a.values())
+    assert prefill(T_q=200) == 1            # more query tokens than cached rows
+    assert prefill(stride=50) == 1          # rows past the sequence stride
+    assert prefill(H=24) == 2
+    assert prefill(ws_bytes=16) == 4
+    assert prefill(qn=P + 2) == 1
+    assert lib.mla_fuse_weights(P, P, P, P, 16, 100, 4096, P, P, None) == 2          # d_cq % 64
+    assert lib.mla_fuse_weights(P, P, P, P, 16, 1536, 1000, P, P, None) == 2         # d_model % 128
+    assert lib.mla_absorb_q_fused(P, P, P, None, f(1e4), 2, 5, 16, 1536, P, None) == 2   # S > 4
+    assert lib.mla_out_proj_fused(P, P, 2, 1, 16, 4096, P, P, 16, None) == 4          # workspace

@@ -1,0 +1,76 @@
+"""GPU parity of prefill / chunked prefill (mla_prefill through the C ABI) against the
+oracle's expanded definition: per-head K_h = C W_UK[h], V_h = C W_UV[h], causal softmax
+attention of the last T_q positions over the first T_kv cached rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mla_latent_kv_70_b300 import inputs as I
+from tests.mla_cases import (K_HOEFFDING, LSE_ABS_TOL, ROW_REL_TOL, SHORT_T, U_BF16, check_lse,
+                             row_rel_err)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mla_latent_kv_70_b300 import build
+    build.build()
+
+
+def prefill_lse_tolerance(qn, qr, C, KR, w_uk, scale, heads):
+    """[S, len(heads)] bound on |lse_gpu - lse_exact|: LSE_ABS_TOL for query tokens that read
+    at least SHORT_T rows; below that, plus the effect of storing K_h = C W_UK[h] in bf16
+    (each element moves by at most 2^-8 of itself), bounded as for the decode path by
+    Hoeffding's inequality over those independent roundings: first order
+    sum_j a_j scale sum_d q_d e_jd, second order max_j d_j^2 / 2."""
+    S, T = qn.shape[0], C.shape[0]
+    tol = np.full((S, len(heads)), LSE_ABS_TOL)
+    k, u = K_HOEFFDING, U_BF16
+    for hi, h in enumerate(heads):
+        K = C @ w_uk[h]                                     # [T, 128]
+        for s in range(S):
+            n = O.visible_length(T, S, s, True)
+            if n >= SHORT_T:
+                continue
+            x = (K[:n] @ qn[s, h] + KR[:n] @ qr[s, h]) * scale
+            a = np.exp(x - x.max())
+            a /= a.sum()
+            per = (qn[s, h] ** 2) @ (K[:n] ** 2).T            # [n]: sum_d q_d^2 K_jd^2
+            first = k * scale * u * np.sqrt((a ** 2) @ per)
+            second = 0.5 * (k * scale * u) ** 2 * per.max()
+            tol[s, hi] = LSE_ABS_TOL + first + second
+    return tol
+
+
+@pytest.mark.parametrize("B,T_q,T_kv,H", [(2, 300, 300, 16), (1, 130, 700, 16), (1, 64, 64, 32),
+                                          (1, 200, 1000, 128)])
+def test_prefill_matches_oracle(B, T_q, T_kv, H):
+    import mla_latent_kv_70_b300 as mla
+    case = I.make_case("prefill", B, T_q, H, [T_kv] * B, causal=True, seed=91, t_cap=T_kv + 40)
+    kv = I.cache(case, device="cuda")
+    kv[:, T_kv:] = float("nan")                 # rows past the sequence must never be used
+    qn, qr = I.queries(case)
+    w_uk, w_uv = I.weights(case)
+    o = torch.empty(B, T_q, H, 128, device="cuda")
+    lse = torch.empty(B, T_q, H, device="cuda")
+    ws = torch.empty(mla.mla_prefill_workspace_bytes(B, case.t_cap, H), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_prefill(qn.cuda(), qr.cuda(), kv, T_kv, w_uk.cuda(), w_uv.cuda(), o, lse, scale=case.scale,
+                    workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    heads = list(range(H)) if H <= 32 else [0, 61, 127]
+    wk, wv = w_uk.double().numpy(), w_uv.double().numpy()
+    for b in range(B):
+        rows = I.seq_rows(case, b)[:T_kv].double().numpy()
+        C, KR = rows[:, :512], rows[:, 512:]
+        q_n, q_r = (t.double().numpy() for t in I.seq_queries(case, b))
+        r_o, r_lse = O.decode_expanded_seq(q_n[:, heads], q_r[:, heads], C, KR, wk[heads], wv[heads],
+                                           case.scale, causal=True)
+        assert row_rel_err(o[b][:, heads].cpu().numpy(), r_o) <= ROW_REL_TOL, b
+        tol = prefill_lse_tolerance(q_n, q_r, C, KR, wk, case.scale, heads)
+        check_lse(lse[b][:, heads].cpu().numpy(), r_lse, tol, where=b)
