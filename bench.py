@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dsv3_decode", choices=sorted(I.WORKLOADS))
+    ap.add_argument("--workload", default="dsv3_decode", choices=sorted(I.WORKLOADS) + sorted(EXTRA))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -331,8 +331,236 @@ def run_reference(args, case):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# The two paths beside the decode step: prefill of a 4096-token prompt in the expanded
+# order, and the DeepSeek-V3 decode step on pre-fused weights (W_UQ W_UK^T, W_UV W_O).
+# ----------------------------------------------------------------------------
+EXTRA = {
+    "prefill_4k": "prefill of one 4096-token prompt, H=128 (mla_prefill: K_h, V_h built, causal attention)",
+    "dsv3_fused": "DeepSeek-V3 decode step on pre-fused weights: c^Q W_UQK -> latent attention -> "
+                  "sum_h z_h W_UVO[h] (d_cq=1536, d_model=4096)",
+}
+
+
+def prefill_flops(B, T_q, T_kv, H):
+    pairs = B * sum(min(T_kv, T_kv - T_q + i + 1) for i in range(T_q))
+    return 2.0 * H * pairs * (192 + 128) + 2.0 * B * T_kv * 512 * 256 * H
+
+
+def cpu_baseline_extra(name, case, min_seconds=10.0):
+    """The oracle on a bounded sample of the extra workloads (a few heads of the prompt,
+    or whole sequences of the fused decode), scaled to the workload's unit."""
+    import numpy as np
+    import oracle as O
+    cores = blas_threads()
+    t0 = time.perf_counter()
+    d = lambda t: t.double().numpy()
+    if name == "prefill_4k":
+        T = case.seqlens[0]
+        rows = d(I.seq_rows(case, 0)[:T])
+        qn, qr = (d(t) for t in I.seq_queries(case, 0))
+        w_uk, w_uv = (d(w) for w in I.weights(case))
+        heads = 0
+        while heads == 0 or (time.perf_counter() - t0 < min_seconds and heads < case.H):
+            h = [heads]
+            O.decode_expanded_seq(qn[:, h], qr[:, h], rows[:, :512], rows[:, 512:], w_uk[h], w_uv[h],
+                                  case.scale, causal=True)
+            heads += 1
+        dt = time.perf_counter() - t0
+        value = case.S / (dt * case.H / heads)
+        sample = f"{heads} of {case.H} heads of the {T}-token prompt (fp64 expanded attention), {dt:.1f} s, scaled to all heads"
+    else:
+        w_uk, w_uv = (d(w) for w in I.weights(case))
+        w_uq, w_o = d(I.query_side_weights(case)), d(I.output_weights(case))
+        seqs = 0
+        while seqs == 0 or (time.perf_counter() - t0 < min_seconds and seqs < case.B):
+            T = case.seqlens[seqs]
+            rows = d(I.seq_rows(case, seqs)[:T])
+            q_nope = np.einsum("si,hik->shk", d(I.seq_c_q(case, seqs)), w_uq)
+            q_lat = O.absorb_q(q_nope, w_uk)
+            o_lat, _ = O.decode_absorbed_seq(q_lat, d(I.seq_queries(case, seqs)[1]), rows[:, :512], rows[:, 512:],
+                                             case.scale)
+            O.out_proj_heads(O.out_proj_uv(o_lat, w_uv), w_o)
+            seqs += 1
+        dt = time.perf_counter() - t0
+        value = seqs * case.S / dt
+        sample = f"{seqs} whole sequences (c^Q W_UQ, absorbed fp64 attention, W_UV, W_O), {dt:.1f} s"
+    return {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+
+def run_extra(args):
+    name = args.workload
+    rank, world, local = dist_env()
+    if name == "prefill_4k":
+        case = I.make_case("prefill_4k", 1, 4096, 128, [4096], causal=True)
+    else:
+        case = I.dsv3()
+    if args.impl == "reference":
+        if rank == 0:
+            r = cpu_baseline_extra(name, case, min_seconds=2.0)
+            print(json.dumps({"impl": "reference", "metric": METRIC_EXTRA[name], "value": r["value"], "unit": UNIT,
+                              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": case.B * case.S / r["value"] * 1e3, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                              "config": {"workload": name, "description": EXTRA[name]}, "cpu_baseline": r,
+                              "e2e": {"value": r["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    import mla_latent_kv_70_b300 as mla
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    B, S, H = case.B, case.S, case.H
+    w_uk, w_uv = (w.to(dev) for w in I.weights(case))
+    qn_h, qr_h = I.queries(case)
+    q_nope, q_rope = qn_h.to(dev), qr_h.to(dev)
+    kv = I.cache(case, device=dev)
+    if name == "prefill_4k":
+        T = case.seqlens[0]
+        o = torch.empty(B, S, H, 128, device=dev)
+        lse = torch.empty(B, S, H, device=dev)
+        ws = torch.empty(mla.mla_prefill_workspace_bytes(B, case.t_cap, H), dtype=torch.uint8, device=dev)
+        inputs_h, inputs_d, result = [qn_h, qr_h], [q_nope, q_rope], o
+
+        def step(st, marks=None):
+            if marks:
+                marks(0)
+            mla.mla_prefill(q_nope, q_rope, kv, T, w_uk, w_uv, o, lse, scale=case.scale, workspace=ws, stream=st)
+            if marks:
+                marks(1)
+        flops = prefill_flops(B, S, T, H)
+        alg_bytes = B * T * 1152 + B * S * H * (192 * 2 + 128 * 4 + 4) + 2 * H * 512 * 128 * 2
+        kernel = "mla_prefill (K_h, V_h expansion GEMMs + causal attention)"
+    else:
+        w_uq, w_o = I.query_side_weights(case).to(dev), I.output_weights(case).to(dev)
+        d_cq, d_model = w_uq.shape[1], w_o.shape[2]
+        w_uqk = torch.empty(H, d_cq, 512, dtype=torch.bfloat16, device=dev)
+        w_uvo = torch.empty(H, 512, d_model, dtype=torch.bfloat16, device=dev)
+        mla.mla_fuse_weights(w_uq, w_uk, w_uv, w_o, w_uqk, w_uvo)
+        c_q_h = I.c_q(case)
+        c_q = c_q_h.to(dev)
+        seqlens = torch.tensor(case.seqlens, dtype=torch.int32, device=dev)
+        q_cat = torch.empty(B, S, H, 576, dtype=torch.bfloat16, device=dev)
+        o_lat = torch.empty(B, S, H, 512, device=dev)
+        lse = torch.empty(B, S, H, device=dev)
+        out = torch.empty(B, S, d_model, device=dev)
+        ws = torch.empty(mla.mla_out_proj_fused_workspace_bytes(B, S, H), dtype=torch.uint8, device=dev)
+        splits = mla.mla_decode_num_splits(B, S, H, max(case.seqlens))
+        dws = mla.mla_decode_workspace_bytes(B, S, H, splits, max(case.seqlens))
+        dws = torch.empty(max(dws, 16), dtype=torch.uint8, device=dev)
+        inputs_h, inputs_d, result = [c_q_h, qr_h], [c_q, q_rope], out
+
+        def step(st, marks=None):
+            mla.mla_absorb_q_fused(c_q, q_rope, w_uqk, None, case.theta, q_cat, st)
+            mla.mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, scale=case.scale, max_seqlen=max(case.seqlens),
+                                  num_splits=splits, workspace=dws, stream=st)
+            if marks:
+                marks(0)
+            mla.mla_out_proj_fused(o_lat, w_uvo, out, ws, st)
+            if marks:
+                marks(1)
+        flops = 2.0 * B * S * H * 512 * d_model
+        alg_bytes = H * 512 * d_model * 2 + B * S * H * 512 * (4 + 2 + 2) + B * S * d_model * 4
+        kernel = "mla_out_proj_fused (sum_h z_h W_UVO[h], the dominant call)"
+
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(dev)
+    clocks.start_smi()
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize()
+    from cuda.bindings import runtime as cudart
+    evs = [(cudart.cudaEventCreate()[1], cudart.cudaEventCreate()[1]) for _ in range(args.steps)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+        cs = torch.cuda.current_stream()
+        for i in range(args.steps):
+            def marks(j, i=i):
+                cudart.cudaEventRecordWithFlags(evs[i][j], cs.cuda_stream, cudart.cudaEventRecordExternal)
+            step(cs, marks)
+    graph.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.begin()
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks.end()
+    total_ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    part_s = statistics.mean(cudart.cudaEventElapsedTime(a, b)[1] for a, b in evs) / 1e3
+    clock_info = clocks.stop()
+
+    # End to end through the public API: the step's inputs copied in from pinned host
+    # memory and its output read back, every step (eager launches).
+    pinned = [t.pin_memory() for t in inputs_h]
+    res_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = res_h.numel() * res_h.element_size()
+
+    def e2e_step():
+        for src, dst in zip(pinned, inputs_d):
+            dst.copy_(src, non_blocking=True)
+        step(stream)
+        res_h.copy_(result, non_blocking=True)
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+    hbm, tf_burst, _, peak_kind = measured_peaks()
+    t_hbm, t_tc = alg_bytes / (hbm * 1e9), flops / (tf_burst * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flops / part_s / 1e12, "peak": tf_burst, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": alg_bytes / part_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": kernel,
+                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)", "kernel_us": part_s * 1e6,
+                 "algorithmic_bytes": alg_bytes, "flops": flops, "roofline_us": max(t_hbm, t_tc) * 1e6})
+    tokens = B * S
+    line = {"metric": METRIC_EXTRA[name], "value": whole_job_rate(world, tokens, total_ms / args.steps),
+            "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "description": EXTRA[name], "B": B, "S": S, "H": H,
+                       "T": case.seqlens[0], "l2": "inputs larger than L2",
+                       "timing": "cuda graph of the timed steps",
+                       "parallelism": f"dp{world} (independent replicas, no collective)"},
+            "clocks": clock_info,
+            "e2e": {"value": whole_job_rate(world, tokens, e2e_ms / args.steps), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * (3 if name == "prefill_4k" else 6),
+            "roofline": roof}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_extra(name, case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+METRIC_EXTRA = {"prefill_4k": "MLA prefill tokens/s (one attention layer, expanded order)",
+                "dsv3_fused": "MLA decode tokens/s on pre-fused weights (one attention layer: "
+                              "c^Q W_UQK + latent attention + sum_h z_h W_UVO[h])"}
+
+
 def main():
     args = parse()
+    if args.workload in EXTRA:
+        run_extra(args)
+        return
     case = I.WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, case)

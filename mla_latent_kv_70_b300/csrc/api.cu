@@ -3,6 +3,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "gemm.cuh"
 
 using mla::kDc;
 using mla::kPage;
@@ -324,7 +325,8 @@ mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla
     const mla::GemmOperand a{which ? w_uv : w_uk, (uint64_t)H * kDc, (uint64_t)mla::kDn, (uint64_t)mla::kDn, 1};
     const mla::GemmOperand b{kv, rows, (uint64_t)kRow, (uint64_t)kRow, 0};
     mla::GemmShape g{};
-    g.M = mla::kDn, g.N = (int)rows, g.K = kDc, g.batches = H, g.n_tile = 256, g.k_splits = 1;
+    // Eight k blocks per tile: two stages are enough, and let two CTAs share an SM.
+    g.M = mla::kDn, g.N = (int)rows, g.K = kDc, g.batches = H, g.n_tile = 256, g.k_splits = 1, g.stages = 2;
     g.a_batch_rows = kDc, g.b_batch_rows = 0;
     g.c = which ? v_exp : k_exp, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = (int64_t)H * mla::kDn, g.ldc_batch = mla::kDn;
     g.status = status_dev;

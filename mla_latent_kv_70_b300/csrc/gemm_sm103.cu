@@ -20,6 +20,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "gemm.cuh"
 #include "ptx_sm103.cuh"
 
 namespace mla {
@@ -29,7 +30,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kGemmThreads = 128;
-constexpr int kGemmStages = 4;
+constexpr int kGemmStages = 4;                // the most stages of the k ring
 constexpr uint32_t kGemmABytes = 128 * 128;   // 128 m x 64 k, bf16
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
@@ -42,8 +43,8 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t n) {
 
 __host__ __device__ constexpr uint32_t gemm_b_bytes(int n_tile) { return (uint32_t)n_tile * 128u; }
 
-__host__ __device__ constexpr uint32_t gemm_smem_bytes(int n_tile) {
-  return kGemmStages * (kGemmABytes + gemm_b_bytes(n_tile)) + 128 + 1024;
+__host__ __device__ constexpr uint32_t gemm_smem_bytes(int n_tile, int stages) {
+  return (uint32_t)stages * (kGemmABytes + gemm_b_bytes(n_tile)) + 128 + 1024;
 }
 
 struct GemmMaps {
@@ -58,11 +59,12 @@ k_gemm(const __grid_constant__ GemmMaps maps, GemmShape g, WaitConfig wc) {
   const uint32_t s0 = smem_addr(smem);
   const uint32_t b_bytes = gemm_b_bytes(g.n_tile);
   const uint32_t stage_bytes = kGemmABytes + b_bytes;
-  const uint32_t bars = s0 + kGemmStages * stage_bytes;
+  const int nst = g.stages;   // stages of the ring (barrier slots exist for kGemmStages)
+  const uint32_t bars = s0 + (uint32_t)nst * stage_bytes;
   auto full = [&](int s) { return bars + 8u * (uint32_t)s; };
   auto empty = [&](int s) { return bars + 8u * (uint32_t)(kGemmStages + s); };
   const uint32_t bar_done = bars + 8u * (2 * kGemmStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kGemmStages * stage_bytes + 8 * (2 * kGemmStages + 1));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + nst * stage_bytes + 8 * (2 * kGemmStages + 1));
   const uint64_t wait_ns = wc.wait_ns;
   const uint32_t ncols = tmem_cols_for((uint32_t)g.n_tile);
 
@@ -73,7 +75,7 @@ k_gemm(const __grid_constant__ GemmMaps maps, GemmShape g, WaitConfig wc) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
@@ -99,8 +101,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, GemmShape g, WaitConfig wc) {
     prefetch_tmap(&maps.b);
     const int ya = z * g.a_batch_rows, yb = z * g.b_batch_rows;
     for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
-      const int it = kb - kb0, s = it % kGemmStages;
-      if (it >= kGemmStages && !mbar_wait(empty(s), (uint32_t)(it / kGemmStages - 1) & 1u, wait_ns)) {
+      const int it = kb - kb0, s = it % nst;
+      if (it >= nst && !mbar_wait(empty(s), (uint32_t)(it / nst - 1) & 1u, wait_ns)) {
         ok = false;
         break;
       }
@@ -123,8 +125,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, GemmShape g, WaitConfig wc) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = idesc_bf16(128, g.n_tile, g.a_mn != 0, g.b_mn != 0);
     for (int kb = kb0; kb < kb1; ++kb) {
-      const int it = kb - kb0, s = it % kGemmStages;
-      if (!mbar_wait(full(s), (uint32_t)(it / kGemmStages) & 1u, wait_ns)) {
+      const int it = kb - kb0, s = it % nst;
+      if (!mbar_wait(full(s), (uint32_t)(it / nst) & 1u, wait_ns)) {
         ok = false;
         break;
       }
@@ -177,8 +179,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, GemmShape g, WaitConfig wc) {
   }
   if (!ok && g.status && tid == 0) raise_flag(g.status, kFlagTimeout);
   if (tid == 0) {   // no copy may land after exit
-    for (int i = max(0, loaded - kGemmStages); i < loaded; ++i)
-      mbar_wait(full(i % kGemmStages), (uint32_t)(i / kGemmStages) & 1u, wait_ns);
+    for (int i = max(0, loaded - nst); i < loaded; ++i)
+      mbar_wait(full(i % nst), (uint32_t)(i / nst) & 1u, wait_ns);
   }
   tc_fence_before();
   __syncthreads();
@@ -205,6 +207,8 @@ __global__ void k_f32_to_bf16(const float* __restrict__ x, int64_t n8, __nv_bflo
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, GemmShape g, cudaStream_t st) {
   if (g.K % 64 || g.n_tile % 16 || g.n_tile < 16 || g.n_tile > 256) return cudaErrorInvalidValue;
   if ((b.mn && g.n_tile % 64) || g.k_splits < 1) return cudaErrorInvalidValue;
+  if (g.stages == 0) g.stages = kGemmStages;
+  if (g.stages < 2 || g.stages > kGemmStages) return cudaErrorInvalidValue;
   GemmMaps maps;
   // A: K-major rows of K (box 64 x 128); MN-major rows of M (box 64 x 64).
   if (!encode_tma_2d(&maps.a, true, a.ptr, a.cols, a.rows, a.row_stride * 2, 64, a.mn ? 64 : 128,
@@ -215,10 +219,11 @@ cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, GemmShape g,
   g.a_mn = a.mn;
   g.b_mn = b.mn;
   static SmemOptIn opt_in;
-  cudaError_t e = ensure_dynamic_smem((const void*)k_gemm, (int)gemm_smem_bytes(256), opt_in);
+  cudaError_t e = ensure_dynamic_smem((const void*)k_gemm, (int)gemm_smem_bytes(256, kGemmStages), opt_in);
   if (e != cudaSuccess) return e;
   dim3 grid((g.M + 127) / 128, (g.N + g.n_tile - 1) / g.n_tile, g.batches * g.k_splits);
-  e = launch_pdl(k_gemm, grid, dim3(kGemmThreads), gemm_smem_bytes(g.n_tile), st, maps, g, wait_config(0));
+  e = launch_pdl(k_gemm, grid, dim3(kGemmThreads), gemm_smem_bytes(g.n_tile, g.stages), st, maps, g,
+                 wait_config(0));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "gemm.cuh"
 #include "ptx_sm103.cuh"
 
 namespace mla {
