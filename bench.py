@@ -34,6 +34,8 @@ from mla_latent_kv_70_b300 import inputs as I  # noqa: E402
 METRIC = "MLA decode tokens/s (one attention layer: absorb + latent attention + W_UV)"
 UNIT = "tokens/s"
 ROW_BYTES = 1152
+EVENT_EVERY = 4
+E2E_SETS = 4
 L2_BYTES = 126e6
 DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_sm103.cu",
                   "mla_latent_kv_70_b300/csrc/ptx_sm103.cuh",
@@ -121,11 +123,50 @@ def recorded_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
+class CtypesNvml:
+    """The few read-only NVML queries the clock sampler needs, called straight from the
+    driver's libnvidia-ml through ctypes (for hosts where the pynvml module is missing).
+    Mirrors the pynvml names ClockSampler uses; raises if the library or device is absent."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, pci_bus_id: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.handle = ctypes.c_void_p()
+        rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.handle))
+        if rc != 0:
+            raise RuntimeError(f"nvmlDeviceGetHandleByPciBusId_v2: {rc}")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _uint(self, fn, *args):
+        v = self.ct.c_uint()
+        if fn(self.handle, *args, self.ct.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def nvmlDeviceGetClockInfo(self, h, clock):
+        return self._uint(self.lib.nvmlDeviceGetClockInfo, self.ct.c_int(clock))
+
+    def nvmlDeviceGetMaxClockInfo(self, h, clock):
+        return self._uint(self.lib.nvmlDeviceGetMaxClockInfo, self.ct.c_int(clock))
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.ct.c_ulonglong()
+        if self.reasons_fn(self.handle, self.ct.byref(v)) != 0:
+            raise RuntimeError("clock event reasons")
+        return v.value
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled while `active` is set.
 
-    NVML (handle found by the device's UUID, so CUDA_VISIBLE_DEVICES remapping is
-    harmless); if NVML is unusable, `nvidia-smi -lms` on the device's PCI bus id, started
+    NVML through pynvml (handle found by the device's UUID, so CUDA_VISIBLE_DEVICES
+    remapping is harmless), else through ctypes on libnvidia-ml (handle found by the
+    device's PCI bus id); if NVML is unusable, `nvidia-smi -lms` on that bus id, started
     before the warm-up and filtered to the samples stamped inside the timed region (or the
     two that bracket it, when the region is shorter than the sampling period)."""
     REASONS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
@@ -162,6 +203,16 @@ class ClockSampler:
         except Exception as e:  # noqa: BLE001
             self.error = f"nvml: {e!r}"
         self.bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        if self.nv is None:
+            try:
+                nv = CtypesNvml(self.bus)
+                self.h = None
+                self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(None, nv.NVML_CLOCK_SM)
+                self.nv = nv
+                self.NVML_CLOCK_SM = nv.NVML_CLOCK_SM
+                self.error = None
+            except Exception as e:  # noqa: BLE001
+                self.error = (self.error + "; " if self.error else "") + f"libnvidia-ml: {e!r}"
         self.t = threading.Thread(target=self._run, daemon=True)
         self.t.start()
 
@@ -171,9 +222,9 @@ class ClockSampler:
                 try:
                     self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
                     r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                    for bit, name in self.REASONS.items():
-                        if r & bit:
-                            self.reasons.add(name)
+                    for bit in range(1, 64):       # bit 0 is gpu_idle
+                        if r >> bit & 1:
+                            self.reasons.add(self.REASONS.get(1 << bit, f"0x{1 << bit:x}"))
                 except Exception as e:  # noqa: BLE001
                     self.error = f"nvml sample: {e!r}"
             time.sleep(0.0002)
@@ -498,7 +549,8 @@ def run_extra(args):
     clock_info = clocks.stop()
 
     # End to end through the public API: the step's inputs copied in from pinned host
-    # memory and its output read back, every step (eager launches).
+    # memory (mla_copy_from_host: SM loads of the mapped buffer) and its output read back
+    # by the copy engine, every step (eager launches).
     pinned = [t.pin_memory() for t in inputs_h]
     res_h = torch.empty(result.shape, dtype=result.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned)
@@ -506,7 +558,7 @@ def run_extra(args):
 
     def e2e_step():
         for src, dst in zip(pinned, inputs_d):
-            dst.copy_(src, non_blocking=True)
+            mla.mla_copy_from_host(dst, src, stream)
         step(stream)
         res_h.copy_(result, non_blocking=True)
     for _ in range(args.warmup):
@@ -624,11 +676,16 @@ def main():
     # The K timed steps are captured once into a CUDA graph (the library makes no host
     # synchronisation, so a decode step is capturable, as serving engines run it) and
     # replayed as one launch: no host launch gaps between the kernels.  Event-record
-    # nodes around every decode give the decode kernel's duration inside the same run.
-    timing = "cuda graph of the timed steps"
+    # nodes around the decode of every fourth step give the decode kernel's duration
+    # inside the same run.  An event node between two kernels stops the next kernel from
+    # starting early under programmatic dependent launch (about 12 us per step here), so
+    # the other steps carry none and keep the overlap a serving loop gets.
+    timing = (f"cuda graph of the timed steps; decode timed by event nodes on every "
+              f"{EVENT_EVERY}th step")
     try:
         from cuda.bindings import runtime as cudart
-        evs = [(cudart.cudaEventCreate()[1], cudart.cudaEventCreate()[1]) for _ in range(args.steps)]
+        sampled = list(range(0, args.steps, EVENT_EVERY))
+        evs = {i: (cudart.cudaEventCreate()[1], cudart.cudaEventCreate()[1]) for i in sampled}
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         with torch.cuda.graph(graph, stream=cap):
@@ -638,7 +695,7 @@ def main():
                     err = cudart.cudaEventRecordWithFlags(evs[i][j], cs.cuda_stream,
                                                           cudart.cudaEventRecordExternal)[0]
                     assert err == cudart.cudaError_t.cudaSuccess, err
-                run_step(cs, marks, kv=kvs[i % n_copies])
+                run_step(cs, marks if i in evs else None, kv=kvs[i % n_copies])
         graph.replay()                      # one untimed replay
         torch.cuda.synchronize()
         use_graph = True
@@ -662,8 +719,8 @@ def main():
     clocks.end()
     total_ms = start.elapsed_time(end)
     if use_graph:
-        dec_ms = [cudart.cudaEventElapsedTime(a, b)[1] for a, b in evs]
-        for a, b in evs:
+        dec_ms = [cudart.cudaEventElapsedTime(a, b)[1] for a, b in evs.values()]
+        for a, b in evs.values():
             cudart.cudaEventDestroy(a)
             cudart.cudaEventDestroy(b)
     else:
@@ -673,52 +730,54 @@ def main():
     clock_info = clocks.stop()
 
     # End to end through the public API, as a serving loop runs it: every step copies its
-    # queries in from pinned host memory and reads its output back.  Two sets of step
-    # buffers alternate, each step's compute replays a CUDA graph of the public
-    # DecodeStep (DecodeStep.capture), and the copies run on their own streams, so the
-    # copies of one step overlap the compute of the next.
+    # queries in from pinned host memory, runs the public DecodeStep and reads its output
+    # back.  Each of E2E_SETS buffer sets has that whole step (copy in, compute, copy out)
+    # captured as one CUDA graph, and consecutive steps take the E2E_SETS sets in turn, each
+    # on its own stream, so the copies of one step overlap the compute of the others; a step
+    # costs one graph launch on the host.  The queries come in through mla_copy_from_host (SM
+    # loads of the mapped pinned buffer): on this host the copy engine moves a 3 MB
+    # host-to-device copy at about 14 GB/s, the SMs at about 48 GB/s.  The output goes
+    # out by the copy engine (57 GB/s), beside the compute.
     qn_h = qn.pin_memory()
     qr_h = qr.pin_memory()
-    steps2 = [step, mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
-                                   num_splits=case.num_splits, causal=case.causal,
-                                   rope_theta=case.theta, total_rows=case.total_tokens)]
-    qn_d, qr_d = [q_nope, q_nope.clone()], [q_rope, q_rope.clone()]
-    o_h = [torch.empty(step.o.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
-    replay = [steps2[k].capture(qn_d[k], qr_d[k], kv, seqlens, block_table=block_table, q_pos=q_pos)
-              for k in range(2)]
+    sets = [step] + [mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
+                                    num_splits=case.num_splits, causal=case.causal,
+                                    rope_theta=case.theta, total_rows=case.total_tokens)
+                     for _ in range(E2E_SETS - 1)]
+    qn_d = [q_nope] + [q_nope.clone() for _ in range(E2E_SETS - 1)]
+    qr_d = [q_rope] + [q_rope.clone() for _ in range(E2E_SETS - 1)]
+    o_h = [torch.empty(step.o.shape, dtype=torch.float32).pin_memory() for _ in range(E2E_SETS)]
     h2d = qn_h.numel() * 2 + qr_h.numel() * 2
     d2h = o_h[0].numel() * 4
-    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "comp", "out")}
+    streams = [torch.cuda.Stream() for _ in range(E2E_SETS)]
+    graphs = []
+    for k in range(E2E_SETS):
+        sets[k](qn_d[k], qr_d[k], kv, seqlens, block_table=block_table, q_pos=q_pos)   # one-time set-up
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=streams[k]):
+            mla.mla_copy_from_host(qn_d[k], qn_h, streams[k])
+            mla.mla_copy_from_host(qr_d[k], qr_h, streams[k])
+            sets[k](qn_d[k], qr_d[k], kv, seqlens, block_table=block_table, q_pos=q_pos)
+            o_h[k].copy_(sets[k].o, non_blocking=True)
+        graphs.append(g)
 
     def e2e_step(i):
-        k = i % 2
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev["comp"][k])      # step i-2 no longer reads these inputs
-            qn_d[k].copy_(qn_h, non_blocking=True)
-            qr_d[k].copy_(qr_h, non_blocking=True)
-            ev["in"][k].record(s_in)
-        with torch.cuda.stream(s_comp):
-            s_comp.wait_event(ev["in"][k])
-            if i >= 2:
-                s_comp.wait_event(ev["out"][k])     # step i-2's output has been read back
-            replay[k]()
-            ev["comp"][k].record(s_comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev["comp"][k])
-            o_h[k].copy_(steps2[k].o, non_blocking=True)
-            ev["out"][k].record(s_out)
+        with torch.cuda.stream(streams[i % E2E_SETS]):
+            graphs[i % E2E_SETS].replay()
 
     for i in range(args.warmup):
         e2e_step(i)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    e0.record(stream)
+    for st in streams:
+        st.wait_stream(stream)
     for i in range(args.steps):
         e2e_step(i)
-    s_in.wait_stream(s_out)
-    e1.record(s_in)
+    for st in streams:
+        stream.wait_stream(st)
+    e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
@@ -769,6 +828,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * step.kernels_per_step,
+            "decode_steps_timed": len(dec_ms),
             "device_status": status,
             "roofline": roof}
     if rank == 0 and not args.no_cpu_baseline:

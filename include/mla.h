@@ -337,6 +337,16 @@ mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla
                        mla_stream stream);
 
 /*
+ * mla_copy_from_host -- copy `bytes` (a multiple of 16; both pointers 16-byte aligned) from
+ * pinned (page-locked) host memory `src_host` to device memory `dst`, asynchronously on
+ * `stream`, by a kernel whose threads read the host buffer through its device-mapped
+ * address.  Not a step of the method: the host-to-device leg of a serving loop, for hosts
+ * whose copy engines move host-to-device data slowly.  Returns MLA_ERR_INVALID if src_host
+ * is not pinned memory.  The host buffer must stay unchanged until the copy has run.
+ */
+mla_status mla_copy_from_host(void* dst, const void* src_host, size_t bytes, mla_stream stream);
+
+/*
  * mla_debug_inject_timeout -- test hook for the device-side failure path (not a step of
  * the method).  For the kernels named in `kernels` (bit 0: the latent decode, bit 1: the
  * key absorption, bit 2: the W_UV projection; 0 turns the hook off) every later launch

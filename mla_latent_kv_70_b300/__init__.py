@@ -46,6 +46,7 @@ SIGNATURES = {
     "mla_out_proj_fused_workspace_bytes": (_SZ, [_I, _I, _I]),
     "mla_out_proj_fused": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mla_prefill_workspace_bytes": (_SZ, [_I, _I64, _I]),
+    "mla_copy_from_host": (_I, [_P, _P, _SZ, _P]),
     "mla_prefill": (_I, [_P, _P, _P, _I64, _I, _P, _P, _I, _I, _I, _F, _P, _P, _P, _SZ, _P, _P]),
 }
 
@@ -241,6 +242,17 @@ def mla_prefill(q_nope, q_rope, kv, T_kv, w_uk, w_uv, o, lse, *, scale, workspac
         _ptr(q_nope, _BF16), _ptr(q_rope, _BF16), _ptr(kv, _BF16), int(stride), int(T_kv), _ptr(w_uk, _BF16),
         _ptr(w_uv, _BF16), B, T_q, H, float(scale), _ptr(o, _F32), _ptr(lse, _F32), _ptr(workspace), ws_bytes,
         _ptr(status, _I32), _stream(stream)))
+
+
+def mla_copy_from_host(dst, src_pinned, stream=None):
+    """dst (device) <- src_pinned (pinned host tensor of the same size), copied by the SMs."""
+    if src_pinned.is_cuda or not src_pinned.is_pinned():
+        raise ValueError("mla_copy_from_host takes a pinned host tensor")
+    nbytes = src_pinned.numel() * src_pinned.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("size mismatch")
+    _check("mla_copy_from_host", lib().mla_copy_from_host(_ptr(dst), src_pinned.data_ptr(), nbytes,
+                                                          _stream(stream)))
 
 
 def mla_rope_inplace(x, row_stride, rows, col_offset, pos, theta, stream=None):

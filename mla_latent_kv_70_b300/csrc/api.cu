@@ -339,6 +339,17 @@ mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla
       status_dev, st));
 }
 
+mla_status mla_copy_from_host(void* dst, const void* src_host, size_t bytes, mla_stream stream) {
+  if (!dst || !src_host || bytes % 16 || !aligned16(dst) || !aligned16(src_host)) return MLA_ERR_INVALID;
+  if (bytes == 0) return MLA_OK;
+  void* alias = nullptr;
+  if (cudaHostGetDevicePointer(&alias, const_cast<void*>(src_host), 0) != cudaSuccess || !alias) {
+    cudaGetLastError();
+    return MLA_ERR_INVALID;   // not pinned (page-locked) host memory
+  }
+  return launch_status(mla::launch_copy_from_host(alias, dst, (int64_t)bytes, static_cast<cudaStream_t>(stream)));
+}
+
 mla_status mla_rope_inplace(mla_bf16* x, int64_t row_stride, int64_t rows, int col_offset,
                             const int32_t* pos, float theta, mla_stream stream) {
   if (!x || !pos || rows < 0 || col_offset < 0 || row_stride < col_offset + mla::kDr)

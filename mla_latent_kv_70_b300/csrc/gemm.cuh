@@ -26,6 +26,7 @@ struct GemmShape {
 };
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, GemmShape g, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* x, int64_t n, __nv_bfloat16* y, cudaStream_t st);
+cudaError_t launch_copy_from_host(const void* src_dev_alias, void* dst, int64_t bytes, cudaStream_t st);
 cudaError_t launch_rope_slice(const __nv_bfloat16* q_rope, const int32_t* q_pos, const RopeFreqs& f, int M,
                               int H, __nv_bfloat16* q_cat, cudaStream_t st);
 

@@ -42,3 +42,12 @@ def test_garbage_and_empty_output():
     assert bench.smi_window([], 0.0, 1.0)[0] == []
     mhz, _, _, note = bench.smi_window(["", "[N/A], x", "Failed to initialize NVML"], 0.0, 1.0)
     assert mhz == [] and note
+
+
+def test_ctypes_nvml_fails_cleanly_without_a_driver():
+    # On a host without the driver's libnvidia-ml (or without the device), the ctypes
+    # fallback raises, and the sampler then uses nvidia-smi or reports no samples.
+    try:
+        bench.CtypesNvml("00000000:00:00.0")
+    except Exception as e:  # noqa: BLE001
+        assert isinstance(e, (OSError, RuntimeError, AttributeError))

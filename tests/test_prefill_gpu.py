@@ -46,8 +46,12 @@ def prefill_lse_tolerance(qn, qr, C, KR, w_uk, scale, heads):
     return tol
 
 
+# Query tiles of 128 rows go two to a CTA: 300 leaves a second CTA whose upper tile holds no
+# query; 200/200 ends the sequence inside a key tile that only the upper tile reads (it
+# clears the rows past the end); 512/600 fills both tiles of two CTAs with the key tiles
+# offset from the query tiles (chunked prefill).
 @pytest.mark.parametrize("B,T_q,T_kv,H", [(2, 300, 300, 16), (1, 130, 700, 16), (1, 64, 64, 32),
-                                          (1, 200, 1000, 128)])
+                                          (1, 200, 1000, 128), (1, 200, 200, 16), (1, 512, 600, 16)])
 def test_prefill_matches_oracle(B, T_q, T_kv, H):
     import mla_latent_kv_70_b300 as mla
     case = I.make_case("prefill", B, T_q, H, [T_kv] * B, causal=True, seed=91, t_cap=T_kv + 40)
