@@ -9,21 +9,23 @@
 //   head, causal attention of the T_q query tokens (the last T_q of T_kv positions) over
 //   [K_h | k^R] with [q_nope | q^R], one scale, and V_h mixed by the weights.
 //
-// k_prefill_attn: one CTA per (sequence, head, 256 query tokens), as two tiles A and B of
-// 128 queries that share every key tile.  Warps 0-3 run the online softmax of tile A and
-// warps 4-7 that of tile B, one query row per thread (TMEM lane = row); warp 8 streams the
-// key tiles of 64 positions by TMA, [K_h | k^R] (24 KB) into a ring of two stages and V_h
-// (16 KB) into a ring of three; warp 9 issues the MMAs, per key tile j:
-//   S_A(j), S_B(j) [128 x 64] = Q_t [128 x 192] . K(j)^T   (12 MMAs each, S double-buffered)
-//   O_A, O_B [128 x 128]   += P_t(j-1) [128 x 64] . V(j-1)  (4 MMAs each)
-// so the tensor core works on one tile's products while the other tile's softmax runs
-// (two query tiles in flight hide the softmax; one tile left the tensor core idle while
-// its own softmax ran).  The key half of a stage is released as soon as both score
-// products are done, the value half once both aggregations are.  The running maximum is
-// raised lazily (O is rescaled only when a row's maximum grows by more than 2^8), as in
-// the latent decode.  Key tiles past a tile's last query position are neither loaded nor
-// multiplied.  Every wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT, drains
-// and exits.
+// k_prefill_attn: one CTA per (sequence, head, 128 query tokens), key tiles of 128
+// positions.  TMEM holds O (128 columns), two score buffers (128 each), q_nope as the A
+// operand of the score products (64 columns of bf16 pairs) and P as the A operand of the
+// aggregation (64 columns); shared memory holds the key tiles [K_h | k^R] (48 KB, a ring
+// of three), the value tiles V_h (32 KB, a ring of two) and q^R.  Per key tile j:
+//   S(j) [128 x 128] = q_nope . K_h(j)^T (8 MMAs, A from TMEM) + q^R . k^R(j)^T (4 MMAs)
+//   O [128 x 128]   += P(j-1) [128 x 128] . V(j-1)  (8 MMAs, A from TMEM)
+// Both score products and the aggregation read only the key or value tile from shared
+// memory (with N = 64 and both operands in shared memory the products were bound by
+// their operand reads).  Warps 0-7 run the online softmax, two threads per query row
+// (TMEM lane = row; warp w takes key columns [64 (w / 4), 64 (w / 4) + 64)), the pair
+// agreeing on the row maximum through shared memory; warps 8 and 10 stream the key and
+// value tiles by TMA; warp 9 issues the MMAs, S(j+1) running while the softmax of tile j does.  The running
+// maximum is raised lazily (O is rescaled only when a row's maximum grows by more than
+// 2^8), as in the latent decode.  Key tiles past the last query's position are not
+// loaded.  Every wait is bounded; on expiry the CTA records MLA_ERR_TIMEOUT, drains and
+// exits.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -35,58 +37,60 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kPQ = 128;                  // query rows per tile (TMEM lanes)
-constexpr int kPTiles = 2;                // query tiles per CTA
-constexpr int kPKeys = 64;                // keys per tile
-constexpr int kPKStages = 2;              // [K_h | k^R] ring
-constexpr int kPVStages = 3;              // V_h ring
-constexpr int kPMmaWarp = 9, kPTmaWarp = 8;
-constexpr int kPThreads = 320;
-constexpr uint32_t kPBox = 64 * 128;      // 64 rows x 64 bf16
-constexpr uint32_t kPQBox = 128 * 128;    // 128 rows x 64 bf16
-constexpr uint32_t kPQBytes = 3 * kPQBox; // q_nope (2 boxes) + q^R (1 box)
+constexpr int kPQ = 128;                  // query rows per CTA (TMEM lanes)
+constexpr int kPKeys = 128;               // keys per tile
+constexpr int kPKStages = 3;              // [K_h | k^R] ring
+constexpr int kPVStages = 2;              // V_h ring
+constexpr int kPSoftWarps = 8;
+constexpr int kPTmaWarp = 8, kPMmaWarp = 9, kPVWarp = 10;
+constexpr int kPThreads = 352;
+constexpr uint32_t kPBox = 128 * 128;     // 128 rows x 64 bf16 (128B swizzle)
 constexpr uint32_t kPKBytes = 3 * kPBox;  // K_h (2 boxes) + k^R (1 box)
 constexpr uint32_t kPVBytes = 2 * kPBox;
-constexpr uint32_t kPOffQ = 0;
-constexpr uint32_t kPOffK = kPOffQ + kPTiles * kPQBytes;
+constexpr uint32_t kPOffK = 0;
 constexpr uint32_t kPOffV = kPOffK + kPKStages * kPKBytes;
-constexpr uint32_t kPOffP = kPOffV + kPVStages * kPVBytes;
-constexpr uint32_t kPOffBars = kPOffP + kPTiles * kPQ * 128;
-constexpr uint32_t kPSmem = kPOffBars + 256 + 1024;
+constexpr uint32_t kPOffQR = kPOffV + kPVStages * kPVBytes;
+constexpr uint32_t kPOffRed = kPOffQR + kPBox;   // [2 halves][128 rows] fp32
+constexpr uint32_t kPOffBars = kPOffRed + 2 * 128 * 4;
+constexpr uint32_t kPSmem = kPOffBars + 192 + 1024;
 static_assert(kPSmem <= 232448, "shared memory per CTA");
-static_assert(kPOffK % 1024 == 0 && kPOffV % 1024 == 0 && kPOffP % 1024 == 0, "128B-swizzled tiles");
+static_assert(kPOffV % 1024 == 0 && kPOffQR % 1024 == 0, "128B-swizzled tiles");
 
-// TMEM: O of tile t at 128 t; S of tile t at 256 + 128 t (two buffers of 64 columns).
-constexpr uint32_t kPTmemO = 0, kPTmemS = 256;
+// TMEM columns.
+constexpr uint32_t kPTmemO = 0;      // [0,128)   O, fp32
+constexpr uint32_t kPTmemS = 128;    // [128,384) two score buffers of 128 fp32
+constexpr uint32_t kPTmemQ = 384;    // [384,448) q_nope, bf16 pairs
+constexpr uint32_t kPTmemP = 448;    // [448,512) P, bf16 pairs
 constexpr float kPRescale = 8.0f;
 
 enum PBar {
-  kPQFullB = 0,
-  kPKFullB,                             // [2] key half of a stage landed
-  kPKEmptyB = kPKFullB + kPKStages,     // [2] both score products of the stage done
-  kPVFullB = kPKEmptyB + kPKStages,     // [3] value half landed
-  kPVEmptyB = kPVFullB + kPVStages,     // [3] both aggregations of the stage done
-  kPSFullB = kPVEmptyB + kPVStages,     // [tile][2] S buffer ready
-  kPSFreeB = kPSFullB + 2 * kPTiles,    // [tile][2] S buffer read (4 warps)
-  kPPFullB = kPSFreeB + 2 * kPTiles,    // [tile] P written (128 threads)
-  kPPvDoneB = kPPFullB + kPTiles,       // [tile] PV(j) done: P free, O stable
-  kPDrainB = kPPvDoneB + kPTiles,
+  kPQFullB = 0,                         // q^R landed
+  kPQReadyB,                            // q_nope in TMEM (256 threads)
+  kPKFullB,                             // [3] key tile landed
+  kPKEmptyB = kPKFullB + kPKStages,     // [3] score products of the stage done
+  kPVFullB = kPKEmptyB + kPKStages,     // [2] value tile landed
+  kPVEmptyB = kPVFullB + kPVStages,     // [2] aggregation of the stage done
+  kPSFullB = kPVEmptyB + kPVStages,     // [2] S buffer ready
+  kPSFreeB = kPSFullB + 2,              // [2] S buffer read (8 warps)
+  kPPFullB = kPSFreeB + 2,              // P in TMEM (256 threads)
+  kPPvDoneB,                            // PV(j) done: P free, O stable
+  kPDrainB,
   kPNumBars
 };
-static_assert(kPNumBars * 8 + 16 <= 256, "barrier area");
+static_assert(kPNumBars * 8 + 16 <= 192, "barrier area");
 
 struct PrefillMaps {
-  CUtensorMap q_nope;   // [B*T_q, H*128], box 64 x 128
   CUtensorMap q_rope;   // [B*T_q, H*64], box 64 x 128
-  CUtensorMap k_exp;    // [rows, H*128], box 64 x 64
-  CUtensorMap k_rope;   // cache rows [rows, 576], box 64 x 64 (columns 512..575)
-  CUtensorMap v_exp;    // [rows, H*128], box 64 x 64
+  CUtensorMap k_exp;    // [rows, H*128], box 64 x 128
+  CUtensorMap k_rope;   // cache rows [rows, 576], box 64 x 128 (columns 512..575)
+  CUtensorMap v_exp;    // [rows, H*128], box 64 x 128
 };
 
 struct PrefillParams {
   int B, T_q, T_kv, H;
   int64_t kv_seq_stride;
   float scale_log2;
+  const __nv_bfloat16* q_nope;   // [B, T_q, H, 128]
   float* o;      // [B, T_q, H, 128]
   float* lse;    // [B, T_q, H]
   int32_t* status;
@@ -94,15 +98,6 @@ struct PrefillParams {
 
 __device__ __forceinline__ bool pwarp_wait(uint32_t bar, uint32_t parity) {
   return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, kDefaultWaitNs));
-}
-
-// Key tiles that query tile t of the CTA starting at query q0 reads (0 if it holds no query).
-__device__ __forceinline__ int tile_keys(const PrefillParams& p, int q0, int t) {
-  const int first = q0 + kPQ * t;
-  if (first >= p.T_q) return 0;
-  const int last_q = min(first + kPQ - 1, p.T_q - 1);
-  const int last_pos = min(p.T_kv - 1, p.T_kv - p.T_q + last_q);
-  return last_pos < 0 ? 0 : last_pos / kPKeys + 1;
 }
 
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -114,19 +109,19 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
   const uint32_t bars = s0 + kPOffBars;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPOffBars + 8 * kPNumBars);
+  float* red = reinterpret_cast<float*>(smem + kPOffRed);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.x * (kPTiles * kPQ), h = blockIdx.y, b = blockIdx.z;
+  // The query blocks of a head run from the last (the most key tiles) to the first.
+  const int q0 = (gridDim.x - 1 - blockIdx.x) * kPQ, h = blockIdx.y, b = blockIdx.z;
   const int offset = p.T_kv - p.T_q;                 // query i sits at position offset + i
-  int ntt[kPTiles];
-#pragma unroll
-  for (int t = 0; t < kPTiles; ++t) ntt[t] = tile_keys(p, q0, t);
-  const int nt = max(ntt[0], ntt[1]);                // key tiles the CTA reads
-  const int ntiles_q = ntt[1] > 0 ? 2 : 1;           // query tiles holding a query
+  const int last_pos = min(p.T_kv - 1, offset + min(q0 + kPQ - 1, p.T_q - 1));
+  const int nt = last_pos < 0 ? 0 : last_pos / kPKeys + 1;   // key tiles any row reads
   const int64_t krow0 = (int64_t)b * p.kv_seq_stride;
 
   if (tid == 0) {
     mbar_init(bar(kPQFullB), 1);
+    mbar_init(bar(kPQReadyB), 32 * kPSoftWarps);
     for (int i = 0; i < kPKStages; ++i) {
       mbar_init(bar(kPKFullB + i), 1);
       mbar_init(bar(kPKEmptyB + i), 1);
@@ -135,14 +130,12 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       mbar_init(bar(kPVFullB + i), 1);
       mbar_init(bar(kPVEmptyB + i), 1);
     }
-    for (int t = 0; t < kPTiles; ++t) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(bar(kPSFullB + 2 * t + i), 1);
-        mbar_init(bar(kPSFreeB + 2 * t + i), 4);
-      }
-      mbar_init(bar(kPPFullB + t), 128);
-      mbar_init(bar(kPPvDoneB + t), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kPSFullB + i), 1);
+      mbar_init(bar(kPSFreeB + i), kPSoftWarps);
     }
+    mbar_init(bar(kPPFullB), 32 * kPSoftWarps);
+    mbar_init(bar(kPPvDoneB), 1);
     mbar_init(bar(kPDrainB), 1);
     fence_mbar_init();
   }
@@ -159,24 +152,20 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
 
   bool aborted = false;
   if (warp == kPTmaWarp) {
-    // ---------------- TMA producer ----------------
-    // Per key tile j: the key half into K stage j % 2 (free once S_A(j-2), S_B(j-2) are
-    // done) and the value half into V stage j % 3 (free once PV_A(j-3), PV_B(j-3) are).
+    // ---------------- TMA producer: q^R and the key tiles ----------------
+    // Key tile j into K stage j % 3, free once S(j-3) is done.  The value tiles have a
+    // producer of their own, so that a key tile is never queued behind a value tile
+    // waiting for an aggregation.
     if (lane == 0) {
-      prefetch_tmap(&maps.q_nope);
+      prefetch_tmap(&maps.q_rope);
       prefetch_tmap(&maps.k_exp);
+      prefetch_tmap(&maps.k_rope);
       prefetch_tmap(&maps.v_exp);
-      mbar_arrive_expect_tx(bar(kPQFullB), (uint32_t)ntiles_q * kPQBytes);
-      for (int t = 0; t < ntiles_q; ++t) {
-        const int qy = b * p.T_q + q0 + kPQ * t;
-        const uint32_t qs = s0 + kPOffQ + (uint32_t)t * kPQBytes;
-        tma_load_2d(qs, &maps.q_nope, bar(kPQFullB), h * 128, qy);
-        tma_load_2d(qs + kPQBox, &maps.q_nope, bar(kPQFullB), h * 128 + 64, qy);
-        tma_load_2d(qs + 2 * kPQBox, &maps.q_rope, bar(kPQFullB), h * 64, qy);
-      }
-      int k_issued = 0, v_issued = 0;
+      mbar_arrive_expect_tx(bar(kPQFullB), kPBox);
+      tma_load_2d(s0 + kPOffQR, &maps.q_rope, bar(kPQFullB), h * 64, b * p.T_q + q0);
+      int k_issued = 0;
       for (int j = 0; j < nt; ++j) {
-        const int ks = j % kPKStages, vs = j % kPVStages;
+        const int ks = j % kPKStages;
         const int y = (int)(krow0 + (int64_t)j * kPKeys);
         if (j >= kPKStages &&
             !mbar_wait(bar(kPKEmptyB + ks), (uint32_t)(j / kPKStages - 1) & 1u, kDefaultWaitNs)) {
@@ -189,75 +178,77 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
         tma_load_2d(kst + kPBox, &maps.k_exp, bar(kPKFullB + ks), h * 128 + 64, y);
         tma_load_2d(kst + 2 * kPBox, &maps.k_rope, bar(kPKFullB + ks), kDc, y);
         ++k_issued;
+      }
+      // No copy may land after exit.
+      for (int j = max(0, k_issued - kPKStages); j < k_issued; ++j)
+        mbar_wait(bar(kPKFullB + j % kPKStages), (uint32_t)(j / kPKStages) & 1u, kDefaultWaitNs);
+      mbar_wait(bar(kPQFullB), 0, kDefaultWaitNs);
+    }
+  } else if (warp == kPVWarp) {
+    // ---------------- TMA producer: the value tiles ----------------
+    // Value tile j into V stage j % 2, free once PV(j-2) is done.
+    if (lane == 0) {
+      int v_issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int vs = j % kPVStages;
         if (j >= kPVStages &&
             !mbar_wait(bar(kPVEmptyB + vs), (uint32_t)(j / kPVStages - 1) & 1u, kDefaultWaitNs)) {
           aborted = true;
           break;
         }
+        const int y = (int)(krow0 + (int64_t)j * kPKeys);
         const uint32_t vst = s0 + kPOffV + (uint32_t)vs * kPVBytes;
         mbar_arrive_expect_tx(bar(kPVFullB + vs), kPVBytes);
         tma_load_2d(vst, &maps.v_exp, bar(kPVFullB + vs), h * 128, y);
         tma_load_2d(vst + kPBox, &maps.v_exp, bar(kPVFullB + vs), h * 128 + 64, y);
         ++v_issued;
       }
-      // No copy may land after exit.
-      for (int j = max(0, k_issued - kPKStages); j < k_issued; ++j)
-        mbar_wait(bar(kPKFullB + j % kPKStages), (uint32_t)(j / kPKStages) & 1u, kDefaultWaitNs);
-      for (int j = max(0, v_issued - kPVStages); j < v_issued; ++j)
+      for (int j = max(0, v_issued - kPVStages); j < v_issued; ++j)   // no copy may land after exit
         mbar_wait(bar(kPVFullB + j % kPVStages), (uint32_t)(j / kPVStages) & 1u, kDefaultWaitNs);
-      mbar_wait(bar(kPQFullB), 0, kDefaultWaitNs);
     }
   } else if (warp == kPMmaWarp) {
     // ---------------- MMA issuer ----------------
-    // Round j: S_A(j), S_B(j) (each once its tile's softmax has read buffer j & 1 at tile
-    // j-2), the key stage released, then PV_A(j-1), PV_B(j-1) (each once that tile's P is
-    // written) and the value stage released.  A tile past its last key tile sits out.
+    // Round j: S(j) once the softmax has read buffer j & 1 at tile j-2 (8 MMAs with
+    // q_nope from TMEM against the two K_h boxes, 4 with q^R from shared memory against
+    // k^R), then PV(j-1) once P(j-1) is in TMEM (8 MMAs, A = P from TMEM, B = the value
+    // tile read MN-major).
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, kPKeys, false, false);
       const uint32_t id_o = idesc_bf16(128, 128, false, true);
-      auto pv = [&](int i) {   // O_t += P_t(i) V(i) for the tiles that read key tile i
-        if (!mbar_wait(bar(kPVFullB + i % kPVStages), (uint32_t)(i / kPVStages) & 1u, kDefaultWaitNs)) return false;
-        const uint64_t vd = smem_desc(s0 + kPOffV + (uint32_t)(i % kPVStages) * kPVBytes, kPBox, 1024, kSwizzle128B);
-        for (int t = 0; t < kPTiles; ++t) {
-          if (i >= ntt[t]) continue;
-          if (!mbar_wait(bar(kPPFullB + t), (uint32_t)i & 1u, kDefaultWaitNs)) return false;
-          tc_fence_after();
-          const uint64_t pd = smem_desc(s0 + kPOffP + (uint32_t)t * (kPQ * 128), 16, 1024, kSwizzle128B);
+      const uint64_t qr_desc = smem_desc(s0 + kPOffQR, 16, 1024, kSwizzle128B);
+      auto pv = [&](int i) {   // O += P(i) V(i)
+        const int vs = i % kPVStages;
+        if (!mbar_wait(bar(kPPFullB), (uint32_t)i & 1u, kDefaultWaitNs) ||
+            !mbar_wait(bar(kPVFullB + vs), (uint32_t)(i / kPVStages) & 1u, kDefaultWaitNs))
+          return false;
+        tc_fence_after();
+        const uint64_t vd = smem_desc(s0 + kPOffV + (uint32_t)vs * kPVBytes, kPBox, 1024, kSwizzle128B);
 #pragma unroll
-          for (int k = 0; k < kPKeys / 16; ++k)
-            mma_ss(tb + kPTmemO + 128u * t, pd + 2u * k, vd + 128u * k, id_o, (i > 0 || k > 0) ? 1u : 0u);
-          mma_commit(bar(kPPvDoneB + t));
-        }
-        mma_commit(bar(kPVEmptyB + i % kPVStages));
+        for (int k = 0; k < kPKeys / 16; ++k)
+          mma_ts(tb + kPTmemO, tb + kPTmemP + 8u * k, vd + 128u * k, id_o, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar(kPVEmptyB + vs));
+        mma_commit(bar(kPPvDoneB));
         return true;
       };
-      if (!mbar_wait(bar(kPQFullB), 0, kDefaultWaitNs)) aborted = true;
+      if (!mbar_wait(bar(kPQFullB), 0, kDefaultWaitNs) || !mbar_wait(bar(kPQReadyB), 0, kDefaultWaitNs))
+        aborted = true;
       for (int j = 0; j < nt && !aborted; ++j) {
         const int ks = j % kPKStages;
-        if (!mbar_wait(bar(kPKFullB + ks), (uint32_t)(j / kPKStages) & 1u, kDefaultWaitNs)) {
+        if ((j >= 2 && !mbar_wait(bar(kPSFreeB + (j & 1)), (uint32_t)((j - 2) >> 1) & 1u, kDefaultWaitNs)) ||
+            !mbar_wait(bar(kPKFullB + ks), (uint32_t)(j / kPKStages) & 1u, kDefaultWaitNs)) {
           aborted = true;
           break;
         }
+        tc_fence_after();
         const uint32_t kst = s0 + kPOffK + (uint32_t)ks * kPKBytes;
-        for (int t = 0; t < kPTiles && !aborted; ++t) {
-          if (j >= ntt[t]) continue;
-          if (j >= 2 && !mbar_wait(bar(kPSFreeB + 2 * t + (j & 1)), (uint32_t)((j - 2) >> 1) & 1u, kDefaultWaitNs)) {
-            aborted = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tb + kPTmemS + 128u * t + 64u * (uint32_t)(j & 1);
-          const uint32_t qs = s0 + kPOffQ + (uint32_t)t * kPQBytes;
+        const uint32_t d = tb + kPTmemS + 128u * (uint32_t)(j & 1);
+        const uint64_t kd = smem_desc(kst, 16, 1024, kSwizzle128B);
 #pragma unroll
-          for (int bx = 0; bx < 3; ++bx) {
-            const uint64_t qd = smem_desc(qs + (uint32_t)bx * kPQBox, 16, 1024, kSwizzle128B);
-            const uint64_t kd = smem_desc(kst + (uint32_t)bx * kPBox, 16, 1024, kSwizzle128B);
+        for (int k = 0; k < 8; ++k)   // 16 dims per MMA: 32 bytes along a 128-byte row, box k / 4
+          mma_ts(d, tb + kPTmemQ + 8u * k, kd + (((k >> 2) * kPBox + (k & 3) * 32u) >> 4), id_s, k > 0 ? 1u : 0u);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_ss(d, qd + 2u * k, kd + 2u * k, id_s, (bx > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(kPSFullB + 2 * t + (j & 1)));
-        }
-        if (aborted) break;
+        for (int k = 0; k < 4; ++k) mma_ss(d, qr_desc + 2u * k, kd + ((2 * kPBox) >> 4) + 2u * k, id_s, 1u);
+        mma_commit(bar(kPSFullB + (j & 1)));
         mma_commit(bar(kPKEmptyB + ks));
         if (j >= 1 && !pv(j - 1)) {
           aborted = true;
@@ -269,43 +260,75 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       mbar_wait(bar(kPDrainB), 0, kDefaultWaitNs);
     }
   } else {
-    // ---------------- softmax warps: one query row per thread ----------------
-    const int t = warp >> 2;                      // query tile of this warp
-    const int r = 32 * (warp & 3) + lane;         // TMEM lane == query row of the tile
-    const int qi = q0 + kPQ * t + r;              // query index in the sequence
+    // ---------------- softmax warps: two threads per query row ----------------
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int r = 32 * quarter + lane;            // TMEM lane == query row of the tile
+    const int qi = q0 + r;                        // query index in the sequence
     const int qpos = offset + qi;                 // its position
-    const int my_nt = ntt[t];
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t s_tm = tb + kPTmemS + 128u * t, o_tm = tb + kPTmemO + 128u * t;
-    // The rows of a key tile past the sequence end are cleared by the first tile to read it.
-    const int clear_tile = (t == 0 || ntt[0] == 0) ? 0 : ntt[0];
-    float m_ref = -INFINITY, l = 0.f;
-    for (int j = 0; j < my_nt; ++j) {
-      if (!pwarp_wait(bar(kPSFullB + 2 * t + (j & 1)), (uint32_t)(j >> 1) & 1u)) {
-        aborted = true;
-        break;
+    const bool row_ok = qi < p.T_q;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const uint32_t pair_bar = 1u + (uint32_t)quarter;   // the two warps of this lane quarter
+    // This thread's half of q_nope (64 dims) into TMEM: the A operand of the score MMAs.
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (((int64_t)b * p.T_q + qi) * p.H + h) * kDn + 64 * hf);
+      uint32_t v[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = row_ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * c] = w.x;
+        v[4 * c + 1] = w.y;
+        v[4 * c + 2] = w.z;
+        v[4 * c + 3] = w.w;
       }
-      tc_fence_after();
+      tmem_st32(tb + lane_off + kPTmemQ + 32u * (uint32_t)hf, v);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kPQReadyB));
+    }
+    // The two threads of a row meet at named barriers, so they leave the loop together:
+    // a failed wait is carried to the next meeting, where the pair agrees to give up.
+    float m_ref = -INFINITY, l = 0.f;
+    bool failed = false;   // a wait of this thread gave up since the last meeting
+    for (int j = 0; j < nt; ++j) {
       float x[64];
-      {
-        const uint32_t ts = s_tm + lane_off + 64u * (uint32_t)(j & 1);
+      if (pwarp_wait(bar(kPSFullB + (j & 1)), (uint32_t)(j >> 1) & 1u)) {
+        tc_fence_after();
+        const uint32_t ts = tb + lane_off + kPTmemS + 128u * (uint32_t)(j & 1) + 64u * (uint32_t)hf;
         tmem_ld32f<0>(ts, x);
         tmem_ld32f<32>(ts + 32u, x);
         tmem_ld_wait();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kPSFreeB + 2 * t + (j & 1)));
-      // Causal mask and the sequence end (rows of later positions may hold anything).
-      const int k0 = j * kPKeys;
-      const int vis = min(kPKeys, min(qpos, p.T_kv - 1) - k0 + 1);   // readable keys of this row
-      float mx = -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPSFreeB + (j & 1)));
+      } else {
+        failed = true;
 #pragma unroll
-      for (int c = 0; c < kPKeys; ++c) {
-        if (c >= vis) x[c] = -INFINITY;
-        mx = fmaxf(mx, x[c]);
+        for (int c = 0; c < 64; ++c) x[c] = -INFINITY;
       }
-      mx *= p.scale_log2;
+      // Causal mask and the sequence end (rows of later positions may hold anything).
+      const int k0 = j * kPKeys + 64 * hf;
+      const int vis = min(64, min(qpos, p.T_kv - 1) - k0 + 1);   // readable keys of this half-row
+      float t16[16];
+      if (vis < 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= vis) x[c] = -INFINITY;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) t16[c] = fmaxf(fmaxf(x[c], x[c + 16]), fmaxf(x[c + 32], x[c + 48]));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) t16[c] = fmaxf(t16[c], t16[c + w]);
+      // The row maximum of the two halves, through shared memory: write, meet (agreeing to
+      // go on), read, meet (the next tile's write stays behind the partner's read).
+      red[hf * 128 + r] = t16[0];
+      if (!named_bar_and(pair_bar, 64, !failed)) {
+        aborted = true;
+        break;
+      }
+      const float mx = fmaxf(t16[0], red[(hf ^ 1) * 128 + r]) * p.scale_log2;
+      named_bar_sync(pair_bar, 64);
       const bool grow = mx > m_ref + kPRescale;
       const float m_new = grow ? mx : m_ref;
       if (grow) l *= ex2_approx(m_ref - m_new);   // 0 when m_ref = -inf (l is 0 then)
@@ -313,72 +336,67 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       m_ref = m_new;
       const float bias = (m_new == -INFINITY) ? 0.f : -m_new;
       uint32_t pw[32];
-      float ps = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums: short dependency chains
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float a = ex2_approx(fmaf(x[2 * c], p.scale_log2, bias));
         const float e = ex2_approx(fmaf(x[2 * c + 1], p.scale_log2, bias));
-        ps += a + e;
+        ps[c & 3] += a + e;
         pw[c] = f2_to_bf2(a, e);
       }
-      l += ps;
-      // This tile's P buffer is free, and its O stable, once its PV(j-1) is done.
-      if (j >= 1 && !pwarp_wait(bar(kPPvDoneB + t), (uint32_t)(j - 1) & 1u)) {
-        aborted = true;
-        break;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // The P columns are free, and O stable, once PV(j-1) is done.
+      if (j >= 1 && !pwarp_wait(bar(kPPvDoneB), (uint32_t)(j - 1) & 1u)) {
+        failed = true;
+        continue;
       }
-      {
-        const uint32_t prow = s0 + kPOffP + (uint32_t)t * (kPQ * 128) + (uint32_t)r * 128u;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_u4(prow + (uint32_t)((c ^ (r & 7)) << 4), pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      }
-      if (__any_sync(0xffffffffu, grow && j > 0)) {   // rescale this warp's rows of O
-        tc_fence_after();
+      tc_fence_after();
+      tmem_st32(tb + lane_off + kPTmemP + 32u * (uint32_t)hf, pw);
+      if (__any_sync(0xffffffffu, grow && j > 0)) {   // rescale this thread's half of its O row
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          const uint32_t ta = o_tm + lane_off + 32u * c;
+          const uint32_t ta = tb + lane_off + kPTmemO + 64u * (uint32_t)hf + 32u * c;
           tmem_ld32(ta, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(ta, o);
         }
-        tmem_st_wait();
-        tc_fence_before();
       }
+      tmem_st_wait();
       // Rows of the key tile past the sequence end may hold anything (even NaN): clear
-      // them in the V tile so that their zero weights add exactly zero.  Tile A clears the
-      // key tiles it reads; tile B those past tile A's range (its aggregation of a tile
-      // is issued after tile A's).
-      const int rows_valid = min(kPKeys, p.T_kv - k0);
-      if (rows_valid < kPKeys && j >= clear_tile) {
+      // them in the value tile so that their zero weights add exactly zero.
+      const int rows_valid = min(kPKeys, p.T_kv - j * kPKeys);
+      if (rows_valid < kPKeys) {
         if (!pwarp_wait(bar(kPVFullB + j % kPVStages), (uint32_t)(j / kPVStages) & 1u)) {
-          aborted = true;
-          break;
+          failed = true;
+          continue;
         }
         const uint32_t vt = s0 + kPOffV + (uint32_t)(j % kPVStages) * kPVBytes;
-        for (int idx = tid - 128 * t; idx < (kPKeys - rows_valid) * 16; idx += 128) {
+        for (int idx = tid; idx < (kPKeys - rows_valid) * 16; idx += 32 * kPSoftWarps) {
           const int row = rows_valid + idx / 16, c = idx % 16;   // 2 boxes x 8 chunks per row
           st_shared_v4_zero(vt + (uint32_t)(c >> 3) * kPBox + (uint32_t)row * 128u + (uint32_t)(c & 7) * 16u);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kPPFullB + t));
+      tc_fence_before();
+      mbar_arrive(bar(kPPFullB));
     }
-    // Epilogue: O / l and the LSE of each query row.
-    if (!aborted && my_nt > 0 && !pwarp_wait(bar(kPPvDoneB + t), (uint32_t)(my_nt - 1) & 1u)) aborted = true;
+    // Epilogue: the row sum of both halves, then this thread's half of O / l, and the LSE.
+    if (!aborted && !failed && nt > 0 && !pwarp_wait(bar(kPPvDoneB), (uint32_t)(nt - 1) & 1u)) failed = true;
     tc_fence_after();
-    const bool have = !aborted && l > 0.f;
-    const float inv = have ? 1.f / l : 0.f;
-    const bool row_ok = qi < p.T_q;
-    float* out = p.o + (((int64_t)b * p.T_q + qi) * p.H + h) * 128;
+    red[hf * 128 + r] = l;
+    if (!named_bar_and(pair_bar, 64, !aborted && !failed)) aborted = true;
+    const float l_row = l + red[(hf ^ 1) * 128 + r];
+    const bool have = !aborted && l_row > 0.f;
+    const float inv = have ? 1.f / l_row : 0.f;
+    float* out = p.o + (((int64_t)b * p.T_q + qi) * p.H + h) * 128 + 64 * hf;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t o[32];
-      if (!aborted && my_nt > 0) {
-        tmem_ld32(o_tm + lane_off + 32u * c, o);
+      if (!aborted && nt > 0) {
+        tmem_ld32(tb + lane_off + kPTmemO + 64u * (uint32_t)hf + 32u * c, o);
         tmem_ld_wait();
       }
       if (row_ok) {
@@ -390,7 +408,8 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    if (row_ok) p.lse[((int64_t)b * p.T_q + qi) * p.H + h] = have ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    if (row_ok && hf == 0)
+      p.lse[((int64_t)b * p.T_q + qi) * p.H + h] = have ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
   }
 
   if (aborted) raise_flag(p.status, kFlagTimeout);
@@ -410,9 +429,7 @@ cudaError_t launch_prefill_attn(const __nv_bfloat16* q_nope, const __nv_bfloat16
                                 float* o, float* lse, int32_t* status, cudaStream_t st) {
   PrefillMaps maps;
   const uint64_t qrows = (uint64_t)B * T_q, krows = (uint64_t)B * kv_seq_stride;
-  if (!encode_tma_2d(&maps.q_nope, true, q_nope, (uint64_t)H * kDn, qrows, (uint64_t)H * kDn * 2, 64, kPQ,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tma_2d(&maps.q_rope, true, q_rope, (uint64_t)H * kDr, qrows, (uint64_t)H * kDr * 2, 64, kPQ,
+  if (!encode_tma_2d(&maps.q_rope, true, q_rope, (uint64_t)H * kDr, qrows, (uint64_t)H * kDr * 2, 64, kPQ,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tma_2d(&maps.k_exp, true, k_exp, (uint64_t)H * kDn, krows, (uint64_t)H * kDn * 2, 64, kPKeys,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -421,11 +438,11 @@ cudaError_t launch_prefill_attn(const __nv_bfloat16* q_nope, const __nv_bfloat16
       !encode_tma_2d(&maps.v_exp, true, v_exp, (uint64_t)H * kDv, krows, (uint64_t)H * kDv * 2, 64, kPKeys,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  PrefillParams p{B, T_q, T_kv, H, kv_seq_stride, scale * kLog2e, o, lse, status};
+  PrefillParams p{B, T_q, T_kv, H, kv_seq_stride, scale * kLog2e, q_nope, o, lse, status};
   static SmemOptIn opt_in;
   cudaError_t e = ensure_dynamic_smem((const void*)k_prefill_attn, (int)kPSmem, opt_in);
   if (e != cudaSuccess) return e;
-  dim3 grid((T_q + kPTiles * kPQ - 1) / (kPTiles * kPQ), H, B);
+  dim3 grid((T_q + kPQ - 1) / kPQ, H, B);
   e = launch_pdl(k_prefill_attn, grid, dim3(kPThreads), kPSmem, st, maps, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
