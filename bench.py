@@ -107,9 +107,9 @@ def source_sha():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, num_splits=None):
     """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+    current kernel source with the same split count (else None)."""
     p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
@@ -119,6 +119,8 @@ def recorded_traffic(workload):
         return None
     e = d.get(workload)
     if not e or e.get("source_sha") != source_sha():
+        return None
+    if num_splits is not None and e.get("num_splits") not in (None, num_splits):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -646,7 +648,7 @@ def main():
     kvs = [kv] + [kv.clone() for _ in range(n_copies - 1)]
     step = mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
                           num_splits=case.num_splits, causal=case.causal, rope_theta=case.theta,
-                          total_rows=case.total_tokens)
+                          total_rows=case.total_tokens, seqlens=case.seqlens)
     stream = torch.cuda.current_stream()
 
     def run_step(st, marks=None, kv=kv):
@@ -742,7 +744,7 @@ def main():
     qr_h = qr.pin_memory()
     sets = [step] + [mla.DecodeStep(case.B, case.S, case.H, w_uk, w_uv, max_seqlen=max(case.seqlens),
                                     num_splits=case.num_splits, causal=case.causal,
-                                    rope_theta=case.theta, total_rows=case.total_tokens)
+                                    rope_theta=case.theta, total_rows=case.total_tokens, seqlens=case.seqlens)
                      for _ in range(E2E_SETS - 1)]
     qn_d = [q_nope] + [q_nope.clone() for _ in range(E2E_SETS - 1)]
     qr_d = [q_rope] + [q_rope.clone() for _ in range(E2E_SETS - 1)]
@@ -795,7 +797,7 @@ def main():
     t_hbm = alg_b / (hbm * 1e9)
     t_tc = flops / (tf_burst * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    traffic = recorded_traffic(case.name)
+    traffic = recorded_traffic(case.name, step.num_splits)
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": achieved_gbs / hbm}

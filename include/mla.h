@@ -135,6 +135,25 @@ size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_s
 int mla_decode_num_splits(int B, int S, int H, int max_seqlen, int64_t total_rows);
 
 /*
+ * A split count for mla_decode_latent from the batch's own lengths, for callers that
+ * know them on the host (a serving scheduler does).  For each candidate count s (1 ..
+ * MLA_MAX_SPLITS, at most the 64-row tiles of max_seqlen) it lays out the (query token,
+ * split) units exactly as mla_decode_latent will (C = ceil(max_seqlen / s) rounded up to
+ * 64, causal visibility per query token), hands them in launch order to the device's
+ * CTA-pair slots (each to the slot that frees first, as the hardware starts a cluster
+ * where one finishes), with each unit's time from measured costs (a fixed part plus one
+ * per 64-row tile; near nothing for an empty unit), adds the merge of the partials for
+ * s > 1, and returns the s with the least estimated time (a larger s must win by 2%).
+ *   seqlens    HOST int32 [B]; entries are clamped to [0, max_seqlen] as the decode does
+ *   B, S, H    as for mla_decode_latent (S <= 4, H a multiple of 16 in [16,128])
+ *   causal     as for mla_decode_latent
+ *   max_seqlen the bound that will be passed to mla_decode_latent
+ * Returns 0 on invalid arguments (null seqlens, bad sizes), 1 when no row is readable.
+ * Host work grows with B*S*s; candidates past B*S*s = 2^22 units are not tried.
+ */
+int mla_decode_plan_splits(const int32_t* seqlens, int B, int S, int H, int causal, int max_seqlen);
+
+/*
  * mla_decode_latent -- attention of the absorbed queries straight over the latent
  * cache, [CALC] "Content 점수와 위치 점수 합치기" (eq. s_j, Fig. 2) and
  * "Value 투영을 가중합 뒤로 옮기기" (Fig. 4):

@@ -32,6 +32,7 @@ SIGNATURES = {
     "mla_absorb_q": (_I, [_P, _P, _P, _P, _F, _I, _I, _I, _P, _P]),
     "mla_decode_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "mla_decode_num_splits": (_I, [_I, _I, _I, _I, _I64]),
+    "mla_decode_plan_splits": (_I, [_P, _I, _I, _I, _I, _I]),
     "mla_decode_latent": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _P, _P, _P, _SZ, _P, _P]),
     "mla_decode_latent_noalloc": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -127,6 +128,20 @@ def mla_decode_workspace_bytes(B, S, H, num_splits, max_seqlen) -> int:
 
 def mla_decode_num_splits(B, S, H, max_seqlen, total_rows=0) -> int:
     return int(lib().mla_decode_num_splits(B, S, H, max_seqlen, int(total_rows)))
+
+
+def mla_decode_plan_splits(seqlens, S, H, *, causal=False, max_seqlen=None) -> int:
+    """Split count from the batch's host-side lengths (a list or CPU int tensor)."""
+    import ctypes
+    lens = [int(x) for x in (seqlens.tolist() if hasattr(seqlens, "tolist") else seqlens)]
+    if not lens:
+        raise ValueError("empty batch")
+    arr = (ctypes.c_int32 * len(lens))(*lens)
+    T = max(lens) if max_seqlen is None else int(max_seqlen)
+    r = int(lib().mla_decode_plan_splits(ctypes.addressof(arr), len(lens), int(S), int(H), 1 if causal else 0, T))
+    if r < 1:
+        raise ValueError("mla_decode_plan_splits rejected its arguments")
+    return r
 
 
 def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, block_table=None,

@@ -1,4 +1,6 @@
 // The C ABI of include/mla.h: argument checks, split planning, launches.
+#include <algorithm>
+#include <vector>
 #include <cmath>
 #include <cstdint>
 
@@ -46,6 +48,42 @@ int auto_splits(int B, int S, int H, int max_seqlen, int64_t total_rows, int sms
     }
   }
   return best;
+}
+
+// Times of the CTA-pair decode on a B300, measured on the DeepSeek-V3 shape (H = 128): a
+// unit's fixed cost (set-up, first tiles, drain, epilogue; less for a unit that starts
+// after the launch, whose first requests do not queue behind every other pair's) and each
+// 64-row tile after it; an empty unit only writes its empty partial; the merge is a launch
+// plus one pass over the fp32 partials.
+constexpr double kUnitFixedUs = 17.0, kLaterUnitFixedUs = 11.0, kTileUs = 1.036, kEmptyUnitUs = 1.5;
+constexpr double kMergeFixedUs = 3.0, kMergeBytesPerUs = 6.0e6;
+
+// Estimated decode time with `s` splits: units are handed to the pair slots in launch
+// order ((query token, split), token-major), each to the slot that frees first, as the
+// hardware starts a cluster wherever one finishes.
+double simulate_splits(const int32_t* seqlens, int B, int S, int H, int causal, int max_seqlen, int s,
+                       int slots, std::vector<double>& heap) {
+  int chunk = (max_seqlen + s - 1) / s;
+  chunk = (chunk + 63) & ~63;
+  heap.assign((size_t)slots, 0.0);   // a min-heap of the times the slots free up
+  auto cmp = [](double x, double y) { return x > y; };
+  for (int b = 0; b < B; ++b) {
+    const int T = std::min(std::max(0, seqlens[b]), max_seqlen);
+    for (int q = 0; q < S; ++q) {
+      const int n_vis = causal ? std::min(T, std::max(0, T - S + q + 1)) : T;
+      for (int k = 0; k < s; ++k) {
+        const int t0 = std::min(k * chunk, n_vis), t1 = std::min(t0 + chunk, n_vis);
+        const int tiles = (t1 - t0 + 63) / 64;
+        std::pop_heap(heap.begin(), heap.end(), cmp);
+        const double fixed = heap.back() < 3.0 ? kUnitFixedUs : kLaterUnitFixedUs;
+        heap.back() += tiles > 0 ? fixed + tiles * kTileUs : kEmptyUnitUs;
+        std::push_heap(heap.begin(), heap.end(), cmp);
+      }
+    }
+  }
+  double t = *std::max_element(heap.begin(), heap.end());
+  if (s > 1) t += kMergeFixedUs + (double)s * B * S * H * (kDc + 1) * 4.0 * 2.0 / kMergeBytesPerUs;
+  return t;
 }
 
 mla_status launch_status(cudaError_t e) {
@@ -112,6 +150,28 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope, const ml
 int mla_decode_num_splits(int B, int S, int H, int max_seqlen, int64_t total_rows) {
   if (B < 1 || S < 1 || max_seqlen < 0) return 1;
   return auto_splits(B, S, H, max_seqlen, total_rows, mla::device_sm_count());
+}
+
+int mla_decode_plan_splits(const int32_t* seqlens, int B, int S, int H, int causal, int max_seqlen) {
+  if (!seqlens || B < 1 || S < 1 || S > 4 || !heads_ok(H) || max_seqlen < 0) return 0;
+  int longest = 0;
+  for (int b = 0; b < B; ++b) longest = std::max(longest, std::min(std::max(0, seqlens[b]), max_seqlen));
+  if (longest == 0) return 1;
+  const int sms = mla::device_sm_count() > 0 ? mla::device_sm_count() : 148;
+  const int slots = std::max(1, sms / 2);
+  const int tiles = (max_seqlen + 63) / 64;
+  std::vector<double> heap;
+  int best = 1;
+  double best_t = 0.0;
+  for (int s = 1; s <= MLA_MAX_SPLITS && s <= tiles; ++s) {
+    if ((int64_t)B * S * s > (1 << 22)) break;   // bounds the host work
+    const double t = simulate_splits(seqlens, B, S, H, causal, max_seqlen, s, slots, heap);
+    if (s == 1 || t < best_t * 0.98) {
+      best = s;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_seqlen) {

@@ -12,12 +12,14 @@ import math
 import torch
 
 from . import (D_C, D_V, ROW, mla_absorb_q, mla_append_latent, mla_decode_latent,
-               mla_decode_num_splits, mla_decode_workspace_bytes, mla_out_proj_uv)
+               mla_decode_num_splits, mla_decode_plan_splits, mla_decode_workspace_bytes, mla_out_proj_uv)
 
 
 class DecodeStep:
     def __init__(self, B, S, H, w_uk, w_uv, *, max_seqlen, num_splits=0, causal=False,
-                 rope_theta=10000.0, scale=None, total_rows=0, rope=False, device="cuda"):
+                 rope_theta=10000.0, scale=None, total_rows=0, seqlens=None, rope=False, device="cuda"):
+        """num_splits = 0 plans the split count: from the host-side `seqlens` when given
+        (mla_decode_plan_splits), else from max_seqlen and total_rows."""
         self.B, self.S, self.H = B, S, H
         self.w_uk, self.w_uv = w_uk, w_uv
         self.max_seqlen = int(max_seqlen)
@@ -25,7 +27,12 @@ class DecodeStep:
         self.rope_theta = rope_theta
         self.rope = rope             # rotate appended k^R rows (append only)
         self.scale = scale if scale is not None else 1.0 / math.sqrt(128 + 64)
-        self.num_splits = num_splits or mla_decode_num_splits(B, S, H, self.max_seqlen, total_rows)
+        if num_splits:
+            self.num_splits = num_splits
+        elif seqlens is not None:
+            self.num_splits = mla_decode_plan_splits(seqlens, S, H, causal=causal, max_seqlen=self.max_seqlen)
+        else:
+            self.num_splits = mla_decode_num_splits(B, S, H, self.max_seqlen, total_rows)
         ws = mla_decode_workspace_bytes(B, S, H, self.num_splits, self.max_seqlen)
         self.workspace = torch.empty(ws // 4, dtype=torch.float32, device=device) if ws else None
         self.q_cat = torch.empty(B, S, H, ROW, dtype=torch.bfloat16, device=device)

@@ -40,13 +40,16 @@ class DeviceCase:
                 pos = torch.arange(case.t_cap, dtype=torch.int32, device=device).repeat(case.B)
             mla.mla_rope_inplace(self.kv, I.ROW, pos.numel(), I.D_C, pos, case.theta)
 
-    def step(self, num_splits=None, max_seqlen=None):
+    def step(self, num_splits=None, max_seqlen=None, planned=False):
+        """One DecodeStep; `planned` lets mla_decode_plan_splits pick the split count from
+        the host-side lengths (as the bench does)."""
         import mla_latent_kv_70_b300 as mla
         c = self.case
         st = mla.DecodeStep(c.B, c.S, c.H, self.w_uk, self.w_uv,
                             max_seqlen=max_seqlen or max(c.seqlens),
-                            num_splits=c.num_splits if num_splits is None else num_splits,
-                            causal=c.causal, rope_theta=c.theta, total_rows=c.total_tokens)
+                            num_splits=0 if planned else (c.num_splits if num_splits is None else num_splits),
+                            causal=c.causal, rope_theta=c.theta, total_rows=c.total_tokens,
+                            seqlens=c.seqlens if planned else None)
         st(self.q_nope, self.q_rope, self.kv, self.seqlens, block_table=self.block_table,
            q_pos=self.q_pos)
         torch.cuda.synchronize()

@@ -128,6 +128,72 @@ def test_planner_uses_the_total_row_hint(lib):
     assert mla.mla_decode_num_splits(c.B, 1, 128, T, c.total_tokens) > mla.mla_decode_num_splits(c.B, 1, 128, T)
 
 
+@pytest.mark.parametrize("name,expected", [("tiny", 1), ("dsv3", 1), ("ragged_paged", 8),
+                                           ("long_splitkv", 36), ("mtp", 1)])
+def test_length_planner_choices_for_the_workloads(lib, name, expected):
+    # The counts that measured fastest on a B300 among those tried (ragged: 2-16, long
+    # context: 24-48, multi-token: 1-3, DeepSeek-V3: 1-2; tiny: all equal).
+    from mla_latent_kv_70_b300 import inputs as I
+    c = getattr(I, name)()
+    assert mla.mla_decode_plan_splits(c.seqlens, c.S, c.H, causal=c.causal) == expected
+
+
+def _schedule_time(lens, S, H, causal, s, slots=74):
+    """The planner's schedule estimate, restated: units in launch order, each to the pair
+    slot that frees first; 17 us + 1.036 us per 64-row tile (11 us fixed for a unit
+    starting after 3 us), 1.5 us for an empty unit, plus the merge for s > 1."""
+    import heapq
+    T = max(lens)
+    chunk = ((T + s - 1) // s + 63) // 64 * 64
+    free = [0.0] * slots
+    for Tb in lens:
+        for q in range(S):
+            n_vis = min(Tb, max(0, Tb - S + q + 1)) if causal else Tb
+            for k in range(s):
+                t0 = min(k * chunk, n_vis)
+                tiles = (min(t0 + chunk, n_vis) - t0 + 63) // 64
+                t = heapq.heappop(free)
+                heapq.heappush(free, t + ((17.0 if t < 3.0 else 11.0) + tiles * 1.036 if tiles else 1.5))
+    t = max(free)
+    if s > 1:
+        t += 3.0 + s * len(lens) * S * H * 513 * 8 / 6.0e6
+    return t
+
+
+def test_length_planner_follows_its_schedule_model(lib):
+    import random
+    rng = random.Random(5)
+    for trial in range(12):
+        B = rng.choice([1, 3, 17, 64, 150])
+        S = rng.choice([1, 2, 4])
+        causal = S > 1 and rng.random() < 0.5
+        lens = [rng.randint(0, 20000) for _ in range(B)]
+        lens[0] = max(lens[0], 1)
+        T = max(lens)
+        times = {s: _schedule_time(lens, S, 128, causal, s) for s in range(1, min(128, (T + 63) // 64) + 1)}
+        best, best_t = 1, times[1]
+        for s in sorted(times)[1:]:
+            if times[s] < best_t * 0.98:
+                best, best_t = s, times[s]
+        assert mla.mla_decode_plan_splits(lens, S, 128, causal=causal) == best, (B, S, causal)
+
+
+def test_length_planner_edge_cases(lib):
+    assert mla.mla_decode_plan_splits([0, 0, 0], 1, 128) == 1        # nothing readable
+    assert mla.mla_decode_plan_splits([64] * 300, 1, 128) == 1       # one tile each
+    for lens in ([1], [10 ** 6], [5, 10 ** 5, 7]):
+        s = mla.mla_decode_plan_splits(lens, 1, 128)
+        assert 1 <= s <= min(128, -(-max(lens) // 64))
+    import ctypes
+    arr = (ctypes.c_int32 * 2)(100, 200)
+    f = lib.mla_decode_plan_splits
+    assert f(None, 2, 1, 128, 0, 200) == 0                               # null lengths
+    assert f(ctypes.addressof(arr), 0, 1, 128, 0, 200) == 0              # B < 1
+    assert f(ctypes.addressof(arr), 2, 5, 128, 0, 200) == 0              # S > 4
+    assert f(ctypes.addressof(arr), 2, 1, 24, 0, 200) == 0               # H not a multiple of 16
+    assert f(ctypes.addressof(arr), 2, 1, 128, 0, 150) >= 1              # lengths clamped to max_seqlen
+
+
 def test_binding_refuses_wrong_dtypes(lib):
     # The binding checks each tensor's element type (the library would misread it) before
     # its device; these CPU tensors stop at the first check that applies.

@@ -234,6 +234,9 @@ def test_ragged_paged_full_size():
     lens = case.seqlens
     seqs = [int(np.argmin(lens)), int(np.argmax(lens)), 7]
     check_case(dc, st, seqs, expanded_heads=[5])
+    st_plan = dc.step(planned=True)              # the count planned from the lengths (8)
+    assert st_plan.num_splits != st.num_splits
+    check_case(dc, st_plan, seqs)
 
 
 def test_long_context_splitkv_full_size():
@@ -250,6 +253,9 @@ def test_mtp_causal_full_size():
     dc = DeviceCase(case)
     st = dc.step()
     check_case(dc, st, [0, 64, 127], expanded_heads=[3])
+    st_plan = dc.step(planned=True)              # planned from the lengths: one split
+    assert st_plan.num_splits == 1
+    check_case(dc, st_plan, [0, 127])
 
 
 # ----------------------------------------------------------------------------
