@@ -50,6 +50,11 @@ __all__ = [
     "absorb_q_from_latent",
     "out_proj_fused",
     "out_proj_heads",
+    "e4m3_decode",
+    "e4m3_encode",
+    "fp8_row_scale",
+    "quantize_fp8_rows",
+    "dequantize_fp8_rows",
     "cache_values_per_token",
     "cache_bytes_per_token",
     "compression_ratio",
@@ -334,6 +339,81 @@ def append_latent_rows(new_rows, start: int, theta=None, d_r: int = 64):
 # ----------------------------------------------------------------------------
 # Cache-size identities
 # ----------------------------------------------------------------------------
+
+# ----------------------------------------------------------------------------
+# FP8 latent cache ([ANATOMY] section 5, the checklist item on FP8 mixed precision:
+# E4M3 applied to the 512-wide latent space with a per-token or per-tensor scale).
+# The pages fix neither the E4M3 encoding nor the scale rule; the readings here:
+#   * E4M3 is the OCP 8-bit floating point format "E4M3": sign, 4 exponent bits with
+#     bias 7, 3 mantissa bits, subnormals at exponent field 0 (value m/8 * 2^-6), no
+#     infinities, S.1111.111 the only NaN, largest finite 448;
+#   * one scale per cached token over its 512 latent values, a power of two: the
+#     smallest 2^e with amax/2^e <= 448 (e clamped to [-126, 127]; an all-zero row
+#     takes 2^0), so that dividing by it and multiplying back are exact;
+#   * codes are the round-to-nearest-even E4M3 value of c/scale, saturating at +-448;
+#   * the 64-wide RoPE key k^R stays as it is (bf16): the checklist speaks of the
+#     latent space only.
+# ----------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of E4M3 codes (uint8) as float64; NaN for S.1111.111."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F))          # the 127 finite non-negative values, increasing
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round-to-nearest-even E4M3 codes of finite float64 values, saturating at +-448.
+
+    Nearest by brute force over the 127 non-negative values; a tie goes to the code
+    with an even mantissa (its lowest bit 0).  The sign bit is the sign of x (so a
+    negative value that rounds to zero gives 0x80)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x).reshape(-1)
+    d = np.abs(a[:, None] - _E4M3_POS[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    n_cand = cand.sum(axis=1)
+    first = cand.argmax(axis=1)
+    last = _E4M3_POS.size - 1 - cand[:, ::-1].argmax(axis=1)
+    code = np.where((n_cand > 1) & (first % 2 == 1), last, first)   # ties: the even code
+    code = np.where(a >= 448.0, 0x7E, code)
+    code = code | np.where(np.signbit(x.reshape(-1)), 0x80, 0)
+    return code.astype(np.uint8).reshape(x.shape)
+
+
+def fp8_row_scale(c_row) -> float:
+    """Per-token scale: the smallest power of two 2^e with max|c|/2^e <= 448."""
+    amax = float(np.max(np.abs(np.asarray(c_row, dtype=np.float64))))
+    if amax == 0.0:
+        return 1.0
+    mant, e = math.frexp(amax / 448.0)          # amax/448 = mant * 2^e, 0.5 <= mant < 1
+    if mant == 0.5:                             # an exact power of two
+        e -= 1
+    return math.ldexp(1.0, min(127, max(-126, e)))
+
+
+def quantize_fp8_rows(rows, d_c: int = 512):
+    """Cache rows [n, d_c + d_r] -> (codes uint8 [n, d_c], k^R [n, d_r] unchanged,
+    scales [n]): codes = E4M3(c / scale) per row."""
+    rows = np.asarray(rows, dtype=np.float64)
+    scales = np.array([fp8_row_scale(r[:d_c]) for r in rows], dtype=np.float64)
+    codes = e4m3_encode(rows[:, :d_c] / scales[:, None])
+    return codes, rows[:, d_c:].copy(), scales
+
+
+def dequantize_fp8_rows(codes, k_rope, scales) -> np.ndarray:
+    """Cache rows [n, d_c + d_r] read back from the FP8 form: scale * E4M3 value, then k^R."""
+    c = e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[:, None]
+    return np.concatenate([c, np.asarray(k_rope, dtype=np.float64)], axis=1)
+
 
 def cache_values_per_token(kind: str, n_h=128, d_k=128, d_c=512, d_r=64, n_kv_heads=8) -> int:
     """Cached values per token per layer.

@@ -488,3 +488,94 @@ def test_fused_planted_transpose_is_caught():
     good = O.absorb_q_from_latent(c_q, O.fuse_query_weights(w_uq, w_uk))
     bad = np.einsum("i,hic->hc", c_q, np.einsum("hik,hkc->hic", w_uq, w_uk))
     assert not np.allclose(good, bad)
+
+
+# ----------------------------------------------------------------------------
+# FP8 latent cache: the E4M3 format of the OCP 8-bit floating point specification
+# (bias 7, subnormals at exponent 0, no infinities, S.1111.111 NaN, largest 448), a
+# power-of-two scale per token over the 512 latent values
+# ----------------------------------------------------------------------------
+
+def test_e4m3_closed_forms():
+    v = O.e4m3_decode
+    assert v(0x7E) == 448.0                       # S.1111.110: (1 + 6/8) * 2^8
+    assert v(0x01) == 2.0 ** -9                   # smallest subnormal: 1/8 * 2^-6
+    assert v(0x07) == 7 * 2.0 ** -9               # largest subnormal
+    assert v(0x08) == 2.0 ** -6                   # smallest normal
+    assert v(0x38) == 1.0                         # exponent field 7 = bias
+    assert v(0x3C) == 1.5 and v(0xBC) == -1.5
+    assert np.isnan(v(0x7F)) and np.isnan(v(0xFF))
+    assert v(0x00) == 0.0 and np.signbit(v(0x80))
+    pos = v(np.arange(0x7F))
+    assert pos.size == 127 and np.all(np.diff(pos) > 0)       # 127 distinct, increasing
+    # every normal binade holds 8 values spaced 2^(e-10)
+    for e in range(1, 16):
+        b = v(np.arange(8 * e, 8 * e + 8)) if 8 * e + 8 <= 0x7F else None
+        if b is not None:
+            assert np.allclose(np.diff(b), 2.0 ** (e - 10))
+
+
+def test_e4m3_encode_round_trip_and_ties():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)     # -0.0 <-> 0x80 included
+    e = O.e4m3_encode
+    assert e(1.0625) == 0x38 and e(1.1875) == 0x3A          # ties to the even mantissa
+    assert e(2.0 ** -10) == 0x00 and e(1.5 * 2.0 ** -10) == 0x01   # below the smallest subnormal
+    assert e(464.0) == 0x7E and e(500.0) == 0x7E and e(1e30) == 0x7E and e(-1e30) == 0xFE   # saturation
+    assert e(-2.0 ** -11) == 0x80
+
+
+def test_e4m3_encode_matches_the_torch_float8_type():
+    # torch.float8_e4m3fn rounds to nearest even (it does not saturate, so the
+    # comparison stays within +-448).
+    import torch
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.normal(0, 30, 20000), rng.normal(0, 0.01, 5000), rng.uniform(-448, 448, 5000)])
+    x = np.clip(x, -448, 448)
+    ref = torch.tensor(x, dtype=torch.float64).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x), ref)
+
+
+def test_fp8_row_scale_is_the_least_power_of_two():
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        row = rng.normal(0, 10 ** rng.uniform(-6, 4), 512)
+        s = O.fp8_row_scale(row)
+        assert math.frexp(s)[0] == 0.5                        # a power of two
+        amax = np.abs(row).max()
+        assert amax / s <= 448.0 < amax / (s / 2)
+    assert O.fp8_row_scale(np.zeros(512)) == 1.0
+    assert O.fp8_row_scale([448.0]) == 1.0 and O.fp8_row_scale([449.0]) == 2.0
+    assert O.fp8_row_scale([224.0]) == 0.5
+
+
+def test_fp8_quantize_error_bound_and_rope_untouched():
+    rng = np.random.default_rng(5)
+    rows = rng.normal(0, 1, (40, 576))
+    rows[3, :512] = 0.0
+    codes, kr, scales = O.quantize_fp8_rows(rows)
+    assert codes.dtype == np.uint8 and codes.shape == (40, 512)
+    assert np.array_equal(kr, rows[:, 512:])
+    back = O.dequantize_fp8_rows(codes, kr, scales)
+    err = np.abs(back[:, :512] - rows[:, :512])
+    # nearest rounding: half a step of the binade (2^(e-4) relative) for normals, half
+    # the subnormal step (2^-10 * scale) below 2^-6 * scale
+    bound = np.maximum(np.abs(rows[:, :512]) * 2.0 ** -4, 2.0 ** -10 * scales[:, None])
+    assert np.all(err <= bound)
+    assert np.all(back[3, :512] == 0.0) and scales[3] == 1.0
+    # values already on the grid come back exactly (the scale may halve when the row's
+    # maximum rounded down onto 224 * scale)
+    codes2, kr2, scales2 = O.quantize_fp8_rows(back)
+    assert np.array_equal(O.dequantize_fp8_rows(codes2, kr2, scales2), back)
+    assert np.all((scales2 == scales) | (scales2 == scales / 2))
+
+
+def test_fp8_planted_mistakes_are_caught():
+    # A plain truncation instead of nearest rounding, and a scale that is not the least
+    # power of two, both break the pins above.
+    pos = O.e4m3_decode(np.arange(0x7F))
+    trunc = lambda a: np.searchsorted(pos, a, side="right") - 1
+    assert trunc(1.0625 + 0.06) != O.e4m3_encode(1.0625 + 0.06)
+    loose = lambda row: 2.0 * O.fp8_row_scale(row)
+    row = np.array([300.0])
+    assert not (np.abs(row).max() / loose(row) > 224.0)
