@@ -348,8 +348,10 @@ def append_latent_rows(new_rows, start: int, theta=None, d_r: int = 64):
 #     bias 7, 3 mantissa bits, subnormals at exponent field 0 (value m/8 * 2^-6), no
 #     infinities, S.1111.111 the only NaN, largest finite 448;
 #   * one scale per cached token over its 512 latent values, a power of two: the
-#     smallest 2^e with amax/2^e <= 448 (e clamped to [-126, 127]; an all-zero row
-#     takes 2^0), so that dividing by it and multiplying back are exact;
+#     smallest 2^e with amax/2^e <= 448 (e clamped to [-126, 15]; an all-zero row
+#     takes 2^0), so that dividing by it and multiplying back are exact, and 2^112 * 2^e
+#     stays a finite bf16 (the factor the GPU path widens E4M3 values to bf16 with);
+#     a row whose amax exceeds 448 * 2^15 saturates;
 #   * codes are the round-to-nearest-even E4M3 value of c/scale, saturating at +-448;
 #   * the 64-wide RoPE key k^R stays as it is (bf16): the checklist speaks of the
 #     latent space only.
@@ -397,7 +399,7 @@ def fp8_row_scale(c_row) -> float:
     mant, e = math.frexp(amax / 448.0)          # amax/448 = mant * 2^e, 0.5 <= mant < 1
     if mant == 0.5:                             # an exact power of two
         e -= 1
-    return math.ldexp(1.0, min(127, max(-126, e)))
+    return math.ldexp(1.0, min(15, max(-126, e)))
 
 
 def quantize_fp8_rows(rows, d_c: int = 512):

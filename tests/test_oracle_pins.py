@@ -547,6 +547,8 @@ def test_fp8_row_scale_is_the_least_power_of_two():
     assert O.fp8_row_scale(np.zeros(512)) == 1.0
     assert O.fp8_row_scale([448.0]) == 1.0 and O.fp8_row_scale([449.0]) == 2.0
     assert O.fp8_row_scale([224.0]) == 0.5
+    assert O.fp8_row_scale([1e9]) == 2.0 ** 15                 # the exponent's upper clamp
+    assert O.e4m3_encode(1e9 / 2.0 ** 15) == 0x7E              # ... and the row saturates
 
 
 def test_fp8_quantize_error_bound_and_rope_untouched():
