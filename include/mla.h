@@ -197,6 +197,41 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
                              int32_t* status_dev, mla_stream stream);
 
 /*
+ * FP8 latent cache ("DeepSeek Multi-Head Latent Attention(MLA) 아키텍처 해부", section 5,
+ * the checklist item on FP8 mixed precision: E4M3 over the 512-wide latent space with a
+ * per-token scale).  A row is 640 bytes: the 512 latent values as E4M3 codes (OCP 8-bit
+ * floating point, E4M3: bias 7, largest 448, no infinities) of c / s, then k^R as 64
+ * bf16, unchanged; s, the row's scale, is a separate fp32.  Rows sit like bf16 rows:
+ * contiguous (row t of sequence b at kv8 + (b*kv_seq_stride + t)*640) or a page pool
+ * [num_pages, 64, 640] with the same block table; scale i belongs to row i of the same
+ * layout.
+ *
+ * mla_quantize_fp8 -- bf16 cache rows of 576 (n_rows of them, row_stride bf16 apart, a
+ * multiple of 8) to that form: s = the least power of two 2^e with max|c| / s <= 448,
+ * e clamped to [-126, 15] (an all-zero row takes 1); codes = E4M3 of c / s rounded to
+ * nearest even, saturating at +-448.  Latent values must be finite.  Writes kv8
+ * [n_rows, 640] and kv_scale [n_rows] (both device, 16- and 4-byte aligned).
+ */
+mla_status mla_quantize_fp8(const mla_bf16* rows, int64_t row_stride, int64_t n_rows, uint8_t* kv8,
+                            float* kv_scale, mla_stream stream);
+
+/*
+ * mla_decode_latent_fp8 -- mla_decode_latent over the FP8 form of the cache: the same
+ * result as mla_decode_latent on rows whose latent part is s * E4M3(code) (exact in
+ * bf16 for the power-of-two scales mla_quantize_fp8 writes; other scales are rounded
+ * once to bf16 after the product) and whose k^R is the stored one.  Arguments as for
+ * mla_decode_latent, with kv8 (640-byte rows, 16-byte aligned) and kv_scale (fp32, one
+ * per row) in place of kv; scales must lie in [2^-126, 2^15].  Same workspace, split
+ * planning, status flags and early-start contract.
+ */
+mla_status mla_decode_latent_fp8(const mla_bf16* q_cat, const uint8_t* kv8, const float* kv_scale,
+                                 int64_t kv_seq_stride, const int32_t* seqlens, const int32_t* block_table,
+                                 int max_pages, int page_size, int num_pages, int B, int S, int H,
+                                 int causal, float scale, int num_splits, int max_seqlen, float* o_lat,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, mla_stream stream);
+
+/*
  * mla_decode_latent_noalloc -- mla_decode_latent without a caller-provided workspace.
  * The pages have no counterpart: this is a convenience for callers that cannot allocate
  * device memory themselves, such as plugins that are handed only their input and output

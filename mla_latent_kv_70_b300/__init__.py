@@ -35,6 +35,9 @@ SIGNATURES = {
     "mla_decode_plan_splits": (_I, [_P, _I, _I, _I, _I, _I]),
     "mla_decode_latent": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                _P, _P, _P, _SZ, _P, _P]),
+    "mla_decode_latent_fp8": (_I, [_P, _P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                                   _P, _P, _P, _SZ, _P, _P]),
+    "mla_quantize_fp8": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "mla_decode_latent_noalloc": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                        _I, _P, _P, _P, _P]),
     "mla_combine_partials": (_I, [_P, _P, _I, _I64, _P, _P, _P]),
@@ -75,7 +78,7 @@ def lib() -> ctypes.CDLL:
     return _LIB
 
 
-_BF16, _F32, _I32 = torch.bfloat16, torch.float32, torch.int32
+_BF16, _F32, _I32, _U8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
 
 
 def _ptr(t, dtype=None):
@@ -157,6 +160,36 @@ def mla_decode_latent(q_cat, kv, seqlens, o_lat, lse, *, scale, max_seqlen, bloc
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("mla_decode_latent", lib().mla_decode_latent(
         _ptr(q_cat, _BF16), _ptr(kv, _BF16), int(kv_seq_stride), _ptr(seqlens, _I32),
+        _ptr(block_table, _I32), max_pages, page_size, num_pages, B, S, H, int(bool(causal)),
+        float(scale), int(num_splits), int(max_seqlen), _ptr(o_lat, _F32), _ptr(lse, _F32),
+        _ptr(workspace), ws_bytes, _ptr(status, _I32), _stream(stream)))
+
+
+def mla_quantize_fp8(rows, kv8, kv_scale, *, stream=None):
+    """bf16 cache rows [n, 576] (rows may be a view with a larger row stride) -> the FP8
+    form: kv8 uint8 [n, 640], kv_scale fp32 [n]."""
+    if rows.dtype != _BF16 or not rows.is_cuda or rows.dim() != 2 or rows.shape[1] != 576 or rows.stride(1) != 1:
+        raise ValueError("rows: a CUDA bf16 [n, 576] tensor with unit column stride")
+    n = rows.shape[0]
+    if kv8.numel() < n * 640 or kv_scale.numel() < n:
+        raise ValueError("output too small")
+    _check("mla_quantize_fp8", lib().mla_quantize_fp8(rows.data_ptr(), int(rows.stride(0)), n, _ptr(kv8, _U8),
+                                                      _ptr(kv_scale, _F32), _stream(stream)))
+
+
+def mla_decode_latent_fp8(q_cat, kv8, kv_scale, seqlens, o_lat, lse, *, scale, max_seqlen,
+                          block_table=None, kv_seq_stride=0, page_size=64, causal=False,
+                          num_splits=0, workspace=None, status=None, stream=None):
+    """mla_decode_latent over the FP8 form of the cache (kv8 uint8 [..., 640], kv_scale fp32)."""
+    B, S, H, _ = q_cat.shape
+    if block_table is not None:
+        num_pages, max_pages = kv8.shape[0], block_table.shape[1]
+    else:
+        num_pages, max_pages = 0, 0
+        kv_seq_stride = kv_seq_stride or kv8.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("mla_decode_latent_fp8", lib().mla_decode_latent_fp8(
+        _ptr(q_cat, _BF16), _ptr(kv8, _U8), _ptr(kv_scale, _F32), int(kv_seq_stride), _ptr(seqlens, _I32),
         _ptr(block_table, _I32), max_pages, page_size, num_pages, B, S, H, int(bool(causal)),
         float(scale), int(num_splits), int(max_seqlen), _ptr(o_lat, _F32), _ptr(lse, _F32),
         _ptr(workspace), ws_bytes, _ptr(status, _I32), _stream(stream)))

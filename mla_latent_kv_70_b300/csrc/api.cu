@@ -182,16 +182,20 @@ size_t mla_decode_workspace_bytes(int B, int S, int H, int num_splits, int max_s
   return (size_t)splits * rows * (kDc + 1) * sizeof(float);
 }
 
-mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t kv_seq_stride,
-                             const int32_t* seqlens, const int32_t* block_table, int max_pages,
-                             int page_size, int num_pages, int B, int S, int H, int causal,
-                             float scale, int num_splits, int max_seqlen, float* o_lat,
-                             float* lse, void* workspace, size_t workspace_bytes,
-                             int32_t* status_dev, mla_stream stream) {
+namespace {
+
+// The decode over either form of the cache (fp8: kv is the 640-byte-row form, kv_scale
+// its scales).
+mla_status decode_any(const mla_bf16* q_cat, const void* kv, const float* kv_scale, bool fp8,
+                      int64_t kv_seq_stride, const int32_t* seqlens, const int32_t* block_table,
+                      int max_pages, int page_size, int num_pages, int B, int S, int H, int causal,
+                      float scale, int num_splits, int max_seqlen, float* o_lat, float* lse,
+                      void* workspace, size_t workspace_bytes, int32_t* status_dev, mla_stream stream) {
   const mla_status bad = mla::check_decode_args(q_cat, kv, kv_seq_stride, seqlens, block_table,
                                                 max_pages, page_size, num_pages, B, S, H, scale,
                                                 num_splits, max_seqlen, o_lat, lse);
   if (bad != MLA_OK) return bad;
+  if (fp8 && (!kv_scale || (reinterpret_cast<uintptr_t>(kv_scale) & 3u))) return MLA_ERR_INVALID;
   const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen, 0);
   const size_t need = mla_decode_workspace_bytes(B, S, H, splits, max_seqlen);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -201,6 +205,7 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
   mla::DecodeParams p{};
   p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
   p.kv = reinterpret_cast<const __nv_bfloat16*>(kv);
+  p.kv_scale = kv_scale;
   p.kv_seq_stride = kv_seq_stride;
   p.seqlens = seqlens;
   p.block_table = block_table;
@@ -219,9 +224,42 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
   p.o_out = splits > 1 ? part_o : o_lat;
   p.lse_out = splits > 1 ? part_lse : lse;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  mla_status r = launch_status(mla::launch_decode(p, st));
+  mla_status r = launch_status(fp8 ? mla::launch_decode_fp8(p, st) : mla::launch_decode(p, st));
   if (r != MLA_OK || splits <= 1) return r;
   return launch_status(mla::launch_combine(part_o, part_lse, splits, rows, o_lat, lse, st));
+}
+
+}  // namespace
+
+mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t kv_seq_stride,
+                             const int32_t* seqlens, const int32_t* block_table, int max_pages,
+                             int page_size, int num_pages, int B, int S, int H, int causal,
+                             float scale, int num_splits, int max_seqlen, float* o_lat,
+                             float* lse, void* workspace, size_t workspace_bytes,
+                             int32_t* status_dev, mla_stream stream) {
+  return decode_any(q_cat, kv, nullptr, false, kv_seq_stride, seqlens, block_table, max_pages, page_size,
+                    num_pages, B, S, H, causal, scale, num_splits, max_seqlen, o_lat, lse, workspace,
+                    workspace_bytes, status_dev, stream);
+}
+
+mla_status mla_decode_latent_fp8(const mla_bf16* q_cat, const uint8_t* kv8, const float* kv_scale,
+                                 int64_t kv_seq_stride, const int32_t* seqlens, const int32_t* block_table,
+                                 int max_pages, int page_size, int num_pages, int B, int S, int H,
+                                 int causal, float scale, int num_splits, int max_seqlen, float* o_lat,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, mla_stream stream) {
+  return decode_any(q_cat, kv8, kv_scale, true, kv_seq_stride, seqlens, block_table, max_pages, page_size,
+                    num_pages, B, S, H, causal, scale, num_splits, max_seqlen, o_lat, lse, workspace,
+                    workspace_bytes, status_dev, stream);
+}
+
+mla_status mla_quantize_fp8(const mla_bf16* rows, int64_t row_stride, int64_t n_rows, uint8_t* kv8,
+                            float* kv_scale, mla_stream stream) {
+  if (!rows || !kv8 || !kv_scale || n_rows < 0 || row_stride < kRow || row_stride % 8) return MLA_ERR_INVALID;
+  if (!aligned16(rows) || !aligned16(kv8) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)) return MLA_ERR_INVALID;
+  if (n_rows == 0) return MLA_OK;
+  return launch_status(mla::launch_quantize_fp8(reinterpret_cast<const __nv_bfloat16*>(rows), row_stride, n_rows,
+                                                kv8, kv_scale, static_cast<cudaStream_t>(stream)));
 }
 
 mla_status mla_combine_partials(const float* o_part, const float* lse_part, int num_splits,

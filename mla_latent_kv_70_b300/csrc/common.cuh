@@ -103,6 +103,7 @@ struct DecodeParams {
   int32_t* status;
   uint64_t wait_ns;            // limit of every mbarrier wait
   int fault;                   // 1: the score issuer withholds the completion of tile 0
+  const float* kv_scale;       // FP8 cache only: per-row scale of the E4M3 latent values
 };
 
 // Rows [t0, t1) of sequence b that split `split` covers for query token s.  Splits are
@@ -125,6 +126,10 @@ __device__ __forceinline__ void split_range(const DecodeParams& p, int T, int s,
 bool encode_tma_2d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                    uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// The same over bytes (uint8 elements).
+bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                      CUtensorMapSwizzle swizzle);
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel on the stream finishes, running its independent prologue (barriers, TMEM,
@@ -180,6 +185,10 @@ cudaError_t launch_rope_inplace(__nv_bfloat16* x, int64_t row_stride, int64_t ro
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int splits, int64_t rows,
                            float* o, float* lse, cudaStream_t st);
 cudaError_t launch_decode(DecodeParams p, cudaStream_t st);
+// The decode over the FP8 cache (640-byte rows at p.kv, scales at p.kv_scale).
+cudaError_t launch_decode_fp8(DecodeParams p, cudaStream_t st);
+cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t row_stride, int64_t n, uint8_t* out,
+                                float* scales, cudaStream_t st);
 cudaError_t launch_append_latent(const __nv_bfloat16* rows, int B, int S, int32_t* seqlens,
                                  __nv_bfloat16* kv, int64_t kv_seq_stride, const int32_t* block_table,
                                  int max_pages, int num_pages, int rotate, const RopeFreqs& f,

@@ -80,13 +80,30 @@ constexpr uint32_t kOffRecv = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffP = kOffRecv + 2 * kRecvBytes;
 constexpr uint32_t kOffMref = kOffP + kPBytes;    // [128] reference maximum per head, log2 units
 constexpr uint32_t kOffBars = kOffMref + 128 * 4;
-constexpr uint32_t kOffSlot = kOffBars + 384;
+constexpr uint32_t kOffSlot = kOffBars + 512;
 constexpr uint32_t kOffSig = kOffSlot + 16;       // [4] landing words of the peer's "buffer free" signals
 constexpr uint32_t kSmemBytes = kOffSig + 16 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 static_assert(kOffV % 1024 == 0 && kOffP % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
 static_assert(kOffRope % 512 == 0 && kOffQRope % 512 == 0, "64B-swizzled tiles need 512-byte alignment");
 static_assert(kGroups * kGroupThreads * 4 <= 2 * kRecvBytes, "row sums reuse the receive buffers");
+
+// FP8 cache: a ring of kSlots8 bf16 tiles serves both products; a tile's E4M3 bytes (64
+// rows x this CTA's 256 latent columns) land by TMA in staging buffer i % 2, from which
+// the group that owns the tile (i % 3) widens them into slot i % 4.  Four slots let that
+// group widen tile i right after finishing tile i-3 (PV(i-4), which held the slot, is
+// done by then).  The staging buffers are shared by the groups, so before waiting for
+// tile i's bytes the group waits for tile i-2 to be widened: the buffer's previous phase
+// has then completed, and its parity wait cannot take the phase of tile i-2.
+constexpr int kSlots8 = 4;
+constexpr int kStages8 = 2;
+constexpr uint32_t kLat8Bytes = kN * 256;          // 64 rows x 256 E4M3 bytes
+constexpr uint32_t kOffStage8 = kOffQk + kSlots8 * kLatBytes;
+constexpr uint32_t kOffRope8 = kOffQk + 5 * kLatBytes;   // q^R stays where the bf16 layout has it
+constexpr int kRow8 = 640;                         // bytes of an FP8 cache row
+static_assert(kOffStage8 + kStages8 * kLat8Bytes <= kOffRope8, "FP8 staging below the rope ring");
+static_assert(kOffRope8 + kRopeStages * kRopeBoxBytes == kOffQRope, "the FP8 layout keeps q^R in place");
+static_assert(kOffRope8 % 512 == 0 && kOffStage8 % 1024 == 0, "alignment");
 
 // TMEM columns.
 constexpr uint32_t kTmemO = 0;      // [0,256)   O half, fp32
@@ -117,13 +134,18 @@ enum Bar {
   kDrain,
   kDrainPv,
   kVGo,                               // PV issuer -> TMA: the first V tiles are requested
-  kNumBars
+  // FP8 cache only:
+  kStageLoaded,                         // [kStages8] a tile's E4M3 bytes landed (TMA)
+  kStageFree = kStageLoaded + kStages8, // [kStages8] the converting group has read them (4 warps)
+  kSlotFull = kStageFree + kStages8,    // [kSlots8] bf16 tile in its slot (128 threads)
+  kSlotEmpty = kSlotFull + kSlots8,     // [kSlots8] PV of the slot's tile done
+  kNumBars = kSlotEmpty + kSlots8
 };
-static_assert(kNumBars * 8 <= 384, "barrier area");
+static_assert(kNumBars * 8 <= 512, "barrier area");
 
 struct Maps {
-  CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle
-  CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle
+  CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle; FP8: bytes, box 256 x 64
+  CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle (FP8: rows as 320 bf16)
   CUtensorMap q_rope;    // q_cat rows, box 32 cols x 128 rows, 64B swizzle
   CUtensorMap o_store;   // output rows (o_lat or split partials) fp32, box 32 cols x H rows, 128B swizzle
 };
@@ -152,6 +174,22 @@ __device__ __forceinline__ int tile_row(const DecodeParams& p, int b, int t, boo
   return (int)((int64_t)b * p.kv_seq_stride + t);
 }
 
+// Four E4M3 values (bytes of w, lowest first) to four bf16 (lo: the first two), times
+// the bf16x2 multiplier mul2.  The hardware conversion to f16 is exact (every E4M3 value
+// is an f16 normal or zero); moving the f16 exponent and mantissa bits down by 3 puts
+// them in bf16 positions, which reads as the value times 2^-112; the multiplication by
+// 2^112 * scale then gives scale * value, exactly when the scale is a power of two.
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t mul2, uint32_t& lo, uint32_t& hi) {
+  uint32_t h0, h1;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(h0), "=r"(h1)
+      : "r"(w));
+  const uint32_t r0 = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
+  const uint32_t r1 = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(lo) : "r"(r0), "r"(mul2));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(hi) : "r"(r1), "r"(mul2));
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   return !__any_sync(0xffffffffu, !mbar_wait(bar, parity, limit_ns));
 }
@@ -163,10 +201,13 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 // kTestHook: the instance launched only while the test hook mla_debug_inject_timeout is
 // on, whose wait limit comes from the launch and whose score issuer may withhold a
 // completion; the ordinary instance keeps the 2 s limit a compile-time constant.
-template <bool kTestHook>
+// kFp8: the cache is in the FP8 form (E4M3 latent bytes, bf16 k^R, a scale per row).
+template <bool kTestHook, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
   const uint64_t wait_ns = kTestHook ? p.wait_ns : kDefaultWaitNs;
+  constexpr uint32_t kRopeAt = kFp8 ? kOffRope8 : kOffRope;      // rope ring
+  constexpr int kRopeX = kFp8 ? 256 : kDc;                        // first k^R column in the rope map
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -235,6 +276,16 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     mbar_init(bar(kVGo), 1);
     mbar_init(bar(kRecvFree + 0), 1);
     mbar_init(bar(kRecvFree + 1), 1);
+    if (kFp8) {
+      for (int i = 0; i < kStages8; ++i) {
+        mbar_init(bar(kStageLoaded + i), 1);
+        mbar_init(bar(kStageFree + i), kGroupWarps);
+      }
+      for (int i = 0; i < kSlots8; ++i) {
+        mbar_init(bar(kSlotFull + i), kGroupThreads);
+        mbar_init(bar(kSlotEmpty + i), 1);
+      }
+    }
     fence_mbar_init();
     // The first waits on kRecvFree are for tiles 2 and 3 (the peer has read tiles 0, 1).
     if (ntiles > 2) mbar_arrive_expect_tx(bar(kRecvFree + 0), 4 * kGroupWarps);
@@ -262,7 +313,51 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     // 32 rope columns into rope slot i % 2 (free once QK(i-2) is done).  "QK(j) done" is the commit the score groups wait for (kSFull):
     // the TMA thread waits for each of its phases in order, and the next phase of that
     // barrier needs a tile that is requested only after the wait.
-    if (lane == 0) {
+    if (kFp8 && lane == 0) {
+      // FP8 cache: tile i's E4M3 bytes into staging buffer i % 2, free once tile i-2 has
+      // been read out of it, and its k^R into rope slot i % 2 as for the bf16 cache.
+      prefetch_tmap(&maps.kv_lat);
+      prefetch_tmap(&maps.kv_rope);
+      prefetch_tmap(&maps.q_rope);
+      int issued = 0, rope_issued = 0;
+      bool q_issued = false;
+      auto load_q = [&]() {
+        grid_dep_wait();
+        mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
+        tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+        q_issued = true;
+      };
+      for (int i = 0; i < ntiles; ++i) {
+        const int ss = i % kStages8, rs = i % kRopeStages;
+        const int y = tile_row(p, b, t0 + i * kN, true);
+        if (i >= 1 && !q_issued) load_q();
+        if (i >= kStages8 && !mbar_wait(bar(kStageFree + ss), (uint32_t)(i / kStages8 - 1) & 1u, wait_ns)) {
+          aborted = true;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kStageLoaded + ss), kLat8Bytes);
+        tma_load_2d(s0 + kOffStage8 + (uint32_t)ss * kLat8Bytes, &maps.kv_lat, bar(kStageLoaded + ss),
+                    256 * (int)rank, y);
+        ++issued;
+        if (i >= kRopeStages &&
+            !mbar_wait(bar(kSFull + (i - kRopeStages) % kGroups), (uint32_t)((i - kRopeStages) / kGroups) & 1u, wait_ns)) {
+          aborted = true;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kRopeFull + rs), kRopeBoxBytes);
+        tma_load_2d(s0 + kRopeAt + (uint32_t)rs * kRopeBoxBytes, &maps.kv_rope, bar(kRopeFull + rs),
+                    kRopeX + 32 * (int)rank, y);
+        ++rope_issued;
+      }
+      if (!q_issued && !aborted) load_q();
+      // No copy may still be landing when the CTA exits.
+      for (int i = max(0, issued - kStages8); i < issued; ++i)
+        mbar_wait(bar(kStageLoaded + i % kStages8), (uint32_t)(i / kStages8) & 1u, wait_ns);
+      for (int i = max(0, rope_issued - kRopeStages); i < rope_issued; ++i)
+        mbar_wait(bar(kRopeFull + i % kRopeStages), (uint32_t)(i / kRopeStages) & 1u, wait_ns);
+      if (q_issued && !mbar_wait(bar(kQFull), 0, wait_ns)) aborted = true;
+    }
+    if (!kFp8 && lane == 0) {
       prefetch_tmap(&maps.kv_lat);
       prefetch_tmap(&maps.kv_rope);
       prefetch_tmap(&maps.q_rope);
@@ -334,16 +429,19 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       const uint64_t qrope_desc = smem_desc(s0 + kOffQRope, 16, 512, kSwizzle64B);
       if (!mbar_wait(bar(kQFull), 0, wait_ns) || !mbar_wait(bar(kQReady), 0, wait_ns)) aborted = true;
       for (int i = 0; i < ntiles && !aborted; ++i) {
-        const int qs = i % kQkStages, rs = i % kRopeStages;
+        // The latent tile: slot i % 3 of the score ring, or (FP8) of the widened ring.
+        const int qs = kFp8 ? i % kSlots8 : i % kQkStages, rs = i % kRopeStages;
+        const uint32_t full_bar = kFp8 ? bar(kSlotFull + qs) : bar(kQkFull + qs);
+        const uint32_t full_ph = (uint32_t)(i / (kFp8 ? kSlots8 : kQkStages)) & 1u;
         const uint32_t d = tb + kTmemS + 64u * (uint32_t)(i & 1);
         if ((i >= 2 && !mbar_wait(bar(kSFree + (i - 2) % kGroups), (uint32_t)((i - 2) / kGroups) & 1u, wait_ns)) ||
-            !mbar_wait(bar(kQkFull + qs), (uint32_t)(i / kQkStages) & 1u, wait_ns)) {
+            !mbar_wait(full_bar, full_ph, wait_ns)) {
           aborted = true;
           break;
         }
         tc_fence_after();
         const uint64_t kv = smem_desc(s0 + kOffQk + (uint32_t)qs * kLatBytes, 16, 1024, kSwizzle128B);
-        const uint64_t kr = smem_desc(s0 + kOffRope + (uint32_t)rs * kRopeBoxBytes, 16, 512, kSwizzle64B);
+        const uint64_t kr = smem_desc(s0 + kRopeAt + (uint32_t)rs * kRopeBoxBytes, 16, 512, kSwizzle64B);
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           mma_ts(d, tb + kTmemQ + 8u * k, kv + (((k >> 2) * kBoxBytes + (k & 3) * 32u) >> 4), id_qk, k > 0 ? 1u : 0u);
@@ -367,7 +465,29 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     // V(i+1) is requested as soon as PV(i-1) has released its slot.  PV(i): O half +=
     // P(i) . V(i), A = P (smem, K-major), B = the V tile read MN-major (N = 256 latent
     // columns over four 64-column boxes, K = 16 rows per step).
-    if (lane == 0) {
+    if (kFp8 && lane == 0) {
+      // FP8 cache: PV(i) reads the widened tile in slot i % 4 (still in place: the slot is
+      // refilled only after this PV) and releases the slot.
+      const uint32_t id_pv = idesc_bf16(128, 256, false, true);
+      for (int i = 0; i < ntiles && !aborted; ++i) {
+        const int ss = i % kSlots8;
+        if (!mbar_wait(bar(kPFull), (uint32_t)i & 1u, wait_ns)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t pd = smem_desc(s0 + kOffP, 16, 1024, kSwizzle128B);
+        const uint64_t vd = smem_desc(s0 + kOffQk + (uint32_t)ss * kLatBytes, 8192, 1024, kSwizzle128B);
+#pragma unroll
+        for (int k = 0; k < kN / 16; ++k)
+          mma_ss(tb + kTmemO, pd + 2u * k, vd + 128u * k, id_pv, (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit(bar(kSlotEmpty + ss));
+        mma_commit(bar(kPvDone + i % kGroups));
+      }
+      mma_commit(bar(kDrainPv));
+      mbar_wait(bar(kDrainPv), 0, wait_ns);
+    }
+    if (!kFp8 && lane == 0) {
       const uint32_t id_pv = idesc_bf16(128, 256, false, true);
       auto load_v = [&](int i) {
         const int vs = i % kVStages;
@@ -460,6 +580,76 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_arrive(bar(kQReady));
     }
     if (h == 0 && g < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + g), kRecvBytes);
+
+    // FP8 cache: the group widens its own tiles (i % 3 == g) from staging into their slots,
+    // tile g before its first tile and tile i+3 once it has finished tile i; thread gtid
+    // takes row gtid / 2, E4M3 bytes [128 (gtid % 2), +128) of the CTA's 256 latent columns.  A row's scale is
+    // loaded one conversion ahead; rows past the readable range are written as zeros (so
+    // their zero weights add exactly 0 in PV).
+    const int crow = gtid >> 1, chalf = gtid & 1;
+    auto tile_valid = [&](int j) {
+      const int t = t0 + j * kN;
+      int v = min(kN, t1 - t);
+      if (p.block_table) {
+        const int page = tile_page(p, b, t);
+        if (page < 0 || page >= p.num_pages) v = 0;
+      }
+      return v;
+    };
+    auto row_scale = [&](int j) -> float {
+      if (!kFp8 || j >= ntiles || crow >= tile_valid(j)) return 0.f;
+      return p.kv_scale[tile_row(p, b, t0 + j * kN, false) + crow];
+    };
+    auto convert = [&](int j, float sc) -> bool {
+      const int ss = j % kSlots8, gs = j % kStages8;
+      const uint32_t slot = s0 + kOffQk + (uint32_t)ss * kLatBytes;
+      // Tile j-2 is widened (so staging buffer j % 2 is in the phase of tile j), tile j's
+      // E4M3 bytes have landed, and the slot is free (PV(j-4) is done: the group waited
+      // for it before finishing tile j-3, so that wait returns at once).
+      if ((j >= 2 && !warp_wait(bar(kSlotFull + (j - 2) % kSlots8), (uint32_t)((j - 2) / kSlots8) & 1u, wait_ns)) ||
+          !warp_wait(bar(kStageLoaded + gs), (uint32_t)(j / kStages8) & 1u, wait_ns) ||
+          (j >= kSlots8 && !warp_wait(bar(kSlotEmpty + ss), (uint32_t)(j / kSlots8 - 1) & 1u, wait_ns)))
+        return false;
+      // Chunk order rotated by (2 row + half): the eight threads of a shared-memory
+      // wavefront then read eight different bank groups of their 256-byte rows.
+      uint4 w[8];
+      const uint32_t rot = (uint32_t)(2 * crow + chalf) & 7u;
+      const uint32_t src = s0 + kOffStage8 + (uint32_t)gs * kLat8Bytes + (uint32_t)crow * 256u + (uint32_t)chalf * 128u;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) w[c] = ld_shared_u4(src + 16u * (((uint32_t)c + rot) & 7u));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kStageFree + gs));   // the staging buffer may be refilled
+      const bool live = crow < tile_valid(j);
+      const float mul = sc * 0x1p112f;
+      const uint32_t mul2 = f2_to_bf2(mul, mul);
+      const uint32_t sw = (uint32_t)(crow & 7);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) e4m3x4_to_bf16(ww[u], mul2, o[2 * u], o[2 * u + 1]);
+        const int col = 128 * chalf + 16 * (int)(((uint32_t)c + rot) & 7u);   // the first of these 16 columns
+        const uint32_t rowp = slot + (uint32_t)(col >> 6) * kBoxBytes + (uint32_t)crow * 128u;
+        const uint32_t j0 = (uint32_t)((col & 63) >> 3);      // its 16-byte chunk in the row
+        if (live) {   // 128B swizzle: chunk j of row r sits at chunk j ^ (r & 7)
+          st_shared_u4(rowp + ((j0 ^ sw) << 4), o[0], o[1], o[2], o[3]);
+          st_shared_u4(rowp + (((j0 + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+        } else {
+          st_shared_v4_zero(rowp + ((j0 ^ sw) << 4));
+          st_shared_v4_zero(rowp + (((j0 + 1) ^ sw) << 4));
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kSlotFull + ss));
+      return true;
+    };
+    float sc_next = 0.f;
+    if (kFp8) {
+      sc_next = row_scale(g);
+      if (g < ntiles && !convert(g, sc_next)) aborted = true;
+      sc_next = row_scale(g + kGroups);
+    }
 
     float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
     for (int i = g; i < ntiles && !aborted; i += kGroups) {
@@ -632,8 +822,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         tc_fence_before();
       }
       // Rows past the readable range may hold anything (even NaN): clear them in the
-      // re-read V tile so that 0-weighted rows add exactly 0.
-      if (valid < kN) {
+      // re-read V tile so that 0-weighted rows add exactly 0 (the FP8 widening writes them
+      // as zeros).
+      if (!kFp8 && valid < kN) {
         const int vs = i % kVStages;
         if (!warp_wait(bar(kVFull + vs), (uint32_t)(i / kVStages) & 1u, wait_ns)) {
           aborted = true;
@@ -648,6 +839,13 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kPFull));
+      if (kFp8 && i + kGroups < ntiles) {
+        if (!convert(i + kGroups, sc_next)) {
+          aborted = true;
+          break;
+        }
+        sc_next = row_scale(i + 2 * kGroups);
+      }
     }
 
     // Epilogue.  The groups' row-sum shares, each moved to the final reference maximum,
@@ -725,18 +923,23 @@ bool encode_rows(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box
   return encode_tma_2d(map, true, base, kRow, rows, (uint64_t)kRow * 2, box_cols, box_rows, sw);
 }
 
-}  // namespace
-
-cudaError_t launch_decode(DecodeParams p, cudaStream_t st) {
+// Tensor maps and launch of one instance.  The FP8 cache is read through two maps over
+// its 640-byte rows: the E4M3 bytes (box 256 bytes x 64 rows, no swizzle) and k^R (the
+// rows viewed as 320 bf16, box 32 x 64, 64B swizzle).
+template <bool kFp8>
+cudaError_t launch_decode_impl(DecodeParams p, cudaStream_t st) {
   Maps maps;
   const uint64_t kv_rows = p.block_table ? (uint64_t)p.num_pages * kPage
                                          : (uint64_t)p.B * (uint64_t)p.kv_seq_stride;
   const uint64_t q_rows = (uint64_t)p.B * p.S * p.H;
   if (kv_rows == 0 || kv_rows > 0x7FFFFFFFull) return cudaErrorInvalidValue;
   const uint64_t o_rows = q_rows * (uint64_t)(p.num_splits > 1 ? p.num_splits : 1);
-  if (!encode_rows(&maps.kv_lat, p.kv, kv_rows, 64, kN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  const bool kv_ok =
+      kFp8 ? encode_tma_2d_u8(&maps.kv_lat, p.kv, kRow8, kv_rows, kRow8, 256, kN, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                 encode_tma_2d(&maps.kv_rope, true, p.kv, kRow8 / 2, kv_rows, kRow8, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B)
+           : encode_rows(&maps.kv_lat, p.kv, kv_rows, 64, kN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                 encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (!kv_ok || !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !encode_tma_2d(&maps.o_store, false, p.o_out, kDc, o_rows, (uint64_t)kDc * 4, 32, (uint32_t)p.H,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -744,13 +947,19 @@ cudaError_t launch_decode(DecodeParams p, cudaStream_t st) {
   p.wait_ns = wc.wait_ns;
   p.fault = wc.fault;
   static SmemOptIn opt_in, opt_in_hook;
-  cudaError_t e = wc.fault ? ensure_dynamic_smem((const void*)k_decode_sm103<true>, (int)kSmemBytes, opt_in_hook)
-                           : ensure_dynamic_smem((const void*)k_decode_sm103<false>, (int)kSmemBytes, opt_in);
+  cudaError_t e = wc.fault ? ensure_dynamic_smem((const void*)k_decode_sm103<true, kFp8>, (int)kSmemBytes, opt_in_hook)
+                           : ensure_dynamic_smem((const void*)k_decode_sm103<false, kFp8>, (int)kSmemBytes, opt_in);
   if (e != cudaSuccess) return e;
   const int units = p.B * p.S * p.num_splits;
-  e = wc.fault ? launch_pdl(k_decode_sm103<true>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p)
-               : launch_pdl(k_decode_sm103<false>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p);
+  e = wc.fault ? launch_pdl(k_decode_sm103<true, kFp8>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p)
+               : launch_pdl(k_decode_sm103<false, kFp8>, dim3(2 * units), dim3(kThreads), kSmemBytes, st, maps, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+}  // namespace
+
+cudaError_t launch_decode(DecodeParams p, cudaStream_t st) { return launch_decode_impl<false>(p, st); }
+
+cudaError_t launch_decode_fp8(DecodeParams p, cudaStream_t st) { return launch_decode_impl<true>(p, st); }
 
 }  // namespace mla

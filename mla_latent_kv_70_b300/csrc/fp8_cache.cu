@@ -1,0 +1,90 @@
+// The FP8 form of the latent cache (page "DeepSeek Multi-Head Latent Attention(MLA) 아키텍처
+// 해부", section 5, the checklist item on FP8 mixed precision: E4M3 over the 512-wide
+// latent space with a per-token scale).
+//
+// A cached row of 576 bf16 (c^KV then k^R) becomes 640 bytes: the 512 latent values as
+// E4M3 codes of c / s (round to nearest even, saturating at +-448), then k^R as it was
+// (64 bf16), with the row's scale s in a separate fp32 array.  s is the least power of
+// two with max|c| / s <= 448 (exponent clamped to [-126, 15]; an all-zero row takes 1),
+// so that c / s and s * E4M3(c / s) are exact in fp32 and bf16; e <= 15 keeps 2^112 * s, the
+// multiplier of the decode's widening to bf16, a finite bf16.
+#include <cuda_fp8.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kFp8Row = 640;   // bytes of one FP8 cache row
+
+// Exponent e of the row scale 2^e: the least e with amax <= 448 * 2^e, from the bits of
+// amax (448 = 1.75 * 2^8, so amax = 1.f * 2^E needs e = E - 8 when its fraction exceeds
+// 0.75, else e = E - 9).
+__device__ __forceinline__ int fp8_scale_exponent(float amax) {
+  const uint32_t bits = __float_as_uint(amax);
+  if (amax == 0.f) return 0;
+  const int ef = (int)(bits >> 23);
+  if (ef == 0) return -126;                       // subnormal: 2^-126 already suffices
+  const int e = (ef - 127) - 8 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return min(15, max(-126, e));
+}
+
+__device__ __forceinline__ float exp2i(int e) {   // 2^e for e in [-127, 127], exact
+  return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t fp8x2(float a, float b) {   // a -> low byte
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(256) k_quantize_fp8(const __nv_bfloat16* __restrict__ rows, int64_t row_stride,
+                                                      int64_t n, uint8_t* __restrict__ out,
+                                                      float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
+    const __nv_bfloat16* src = rows + r * row_stride;
+    // Lane l: latent values [16 l, 16 l + 16).
+    const uint4 u0 = reinterpret_cast<const uint4*>(src)[2 * lane];
+    const uint4 u1 = reinterpret_cast<const uint4*>(src)[2 * lane + 1];
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = fp8_scale_exponent(amax);
+    const float inv = exp2i(-e);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c[i] = fp8x2(x[4 * i] * inv, x[4 * i + 1] * inv) | (fp8x2(x[4 * i + 2] * inv, x[4 * i + 3] * inv) << 16);
+    uint8_t* dst = out + r * kFp8Row;
+    reinterpret_cast<uint4*>(dst)[lane] = make_uint4(c[0], c[1], c[2], c[3]);
+    if (lane < 8)   // k^R: 64 bf16 = 128 bytes, as they are
+      reinterpret_cast<uint4*>(dst + kDc)[lane] = reinterpret_cast<const uint4*>(src + kDc)[lane];
+    if (lane == 0) scales[r] = exp2i(e);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t row_stride, int64_t n, uint8_t* out,
+                                float* scales, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+  const int64_t blocks = std::min<int64_t>((n + 7) / 8, (int64_t)sms * 8);
+  k_quantize_fp8<<<(unsigned)blocks, 256, 0, st>>>(rows, row_stride, n, out, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -219,6 +219,46 @@ def queries(case: DecodeCase):
     return qn, qr
 
 
+FP8_ROW = 640   # bytes of a row of the FP8 cache: 512 E4M3 codes, then k^R as 64 bf16
+
+
+def seq_fp8_rows(case: DecodeCase, b: int):
+    """Sequence b's rows in the FP8 form, drawn directly (no quantizer): E4M3 codes
+    uniform over the magnitude fields 0x00..0x77 (values 0 .. 240) with a random sign,
+    k^R N(0,1) in bf16, one power-of-two scale per row from {2^-9, 2^-8, 2^-7}.
+    Returns (uint8 [rows_alloc(b), 640], fp32 [rows_alloc(b)])."""
+    n = case.rows_alloc(b)
+    g = _gen(case.seed, "fp8", b)
+    mag = torch.randint(0, 0x78, (n, D_C), generator=g, dtype=torch.int32)
+    sign = torch.randint(0, 2, (n, D_C), generator=g, dtype=torch.int32) * 0x80
+    row = torch.empty(n, FP8_ROW, dtype=torch.uint8)
+    row[:, :D_C] = (mag + sign).to(torch.uint8)
+    row[:, D_C:] = randn_bf16((n, D_R), case.seed, "fp8kr", b).view(torch.uint8).view(n, 2 * D_R)
+    scales = torch.pow(2.0, torch.randint(-9, -6, (n,), generator=g).to(torch.float32))
+    return row, scales
+
+
+def fp8_cache(case: DecodeCase, device="cpu"):
+    """The whole FP8 cache: (uint8 [B, t_cap, 640] or pool [num_pages, page, 640],
+    fp32 scales [B, t_cap] or [num_pages, page])."""
+    if case.paged:
+        out = torch.zeros(case.num_pages, case.page_size, FP8_ROW, dtype=torch.uint8, device=device)
+        sc = torch.ones(case.num_pages, case.page_size, dtype=torch.float32, device=device)
+        for b in range(case.B):
+            rows, s = seq_fp8_rows(case, b)
+            ids = case.block_table[b, :case.pages_per_seq[b]].long().to(device)
+            out[ids] = rows.view(-1, case.page_size, FP8_ROW).to(device)
+            sc[ids] = s.view(-1, case.page_size).to(device)
+        return out, sc
+    out = torch.empty(case.B, case.t_cap, FP8_ROW, dtype=torch.uint8, device=device)
+    sc = torch.empty(case.B, case.t_cap, dtype=torch.float32, device=device)
+    for b in range(case.B):
+        rows, s = seq_fp8_rows(case, b)
+        out[b].copy_(rows)
+        sc[b].copy_(s)
+    return out, sc
+
+
 def cache(case: DecodeCase, device="cpu", pin=False) -> torch.Tensor:
     """The whole cache: contiguous [B, t_cap, 576] or a page pool [num_pages, page, 576].
 

@@ -16,6 +16,13 @@ st.async stores and MMA commits complete at random later times, the commits of o
 thread in issue order. Many random schedules run per tile count; a violated argument
 shows up as a failed assertion or a deadlock.
 
+With fp8=True it replays the instance for the FP8 cache instead: the TMA thread loads
+each tile's E4M3 bytes into staging buffer i % 2 (refilled once tile i-2 was read out of
+it); the group that owns the tile (i % 3) widens them into bf16 slot i % 4, tile g before
+its first tile and tile i+3 after finishing tile i, after waiting for tile i-2 to be
+widened (so the shared staging barrier is in the phase of tile i) and for PV(i-4) to
+release the slot; both products read that slot (no second read for PV).
+
 It is a design-level check of the protocol, not of the CUDA code: a change to the
 kernel's barriers or buffers must be mirrored here.
 """
@@ -23,7 +30,7 @@ import random
 
 import pytest
 
-LAT, ROPE, VBYTES, QROPE, RECV, SIG = 32768, 4096, 32768, 8192, 16384, 4
+LAT, ROPE, VBYTES, QROPE, RECV, SIG, LAT8 = 32768, 4096, 32768, 8192, 16384, 4, 16384
 
 
 class ProtocolError(AssertionError):
@@ -108,6 +115,13 @@ class CTA:
         self.recv = [{"tile": None, "landed": [False] * 4, "read": [True] * 4} for _ in range(2)]
         self.p_buf = {"tile": None, "written": [False] * 4, "consumed": True}
         self.mref_tile = [None] * 4          # per lane quarter: which tile wrote the reference
+        # FP8 instance: staging buffers (one per group) and widened bf16 slots.
+        self.stageloaded = [B(f"r{rank}.StageLoaded{i}", 1) for i in range(2)]
+        self.stagefree = [B(f"r{rank}.StageFree{i}", 4) for i in range(2)]
+        self.slotfull = [B(f"r{rank}.SlotFull{i}", 128) for i in range(4)]
+        self.slotempty = [B(f"r{rank}.SlotEmpty{i}", 1) for i in range(4)]
+        self.stage = [{"tile": None, "landed": False, "read": [True] * 4} for _ in range(2)]
+        self.slot8 = [{"tile": None, "written": [False] * 4, "done": True} for _ in range(4)]
         # The first waits on the "free" barriers are for tiles 2 and 3 (one thread at set-up).
         if n > 2:
             self.recvfree[0].arrive(1, tx=4 * SIG)
@@ -116,8 +130,9 @@ class CTA:
 
 
 class Sim:
-    def __init__(self, n, seed, partial_last, faults=()):
+    def __init__(self, n, seed, partial_last, faults=(), fp8=False):
         self.n = n
+        self.fp8 = fp8
         self.faults = set(faults)   # rules left out, to show that the checks catch them
         self.rng = random.Random(seed)
         self.partial_last = partial_last
@@ -160,20 +175,36 @@ class Sim:
             if i >= 1 and not q_issued:
                 load_q()
                 q_issued = True
-            if i == 3 and "no_vgo" not in self.faults:
-                yield ("wait", c.vgo, 0)
-            if i >= 3:
-                yield ("wait", c.sfull[(i - 3) % 3], (i - 3) // 3)
-            s = c.qk_slot[i % 3]
-            check(s.done, f"r{c.rank}: latent slot {i % 3} refilled for tile {i} before QK of tile {s.tile} finished")
-            s.tile, s.landed, s.done = i, False, False
-            c.qkfull[i % 3].arrive(1, tx=LAT)
+            if self.fp8:
+                if i >= 2 and "no_stagefree" not in self.faults:
+                    yield ("wait", c.stagefree[i % 2], i // 2 - 1)
+                st = c.stage[i % 2]
+                check(all(st["read"]), f"r{c.rank}: staging {i % 2} refilled for tile {i} before tile {st['tile']} was read")
+                st["tile"], st["landed"], st["read"] = i, False, [False] * 4
+                c.stageloaded[i % 2].arrive(1, tx=LAT8)
 
-            def land_lat(s=s, i=i):
-                s.landed = True
-                c.qkfull[i % 3].complete_tx(LAT)
-            self.later(land_lat)
-            yield None
+                def land8(st=st, i=i):
+                    st["landed"] = True
+                    c.stageloaded[i % 2].complete_tx(LAT8)
+                self.later(land8)
+                yield None
+            if self.fp8:
+                pass
+            elif i == 3 and "no_vgo" not in self.faults:
+                yield ("wait", c.vgo, 0)
+            if not self.fp8:
+                if i >= 3:
+                    yield ("wait", c.sfull[(i - 3) % 3], (i - 3) // 3)
+                s = c.qk_slot[i % 3]
+                check(s.done, f"r{c.rank}: latent slot {i % 3} refilled for tile {i} before QK of tile {s.tile} finished")
+                s.tile, s.landed, s.done = i, False, False
+                c.qkfull[i % 3].arrive(1, tx=LAT)
+
+                def land_lat(s=s, i=i):
+                    s.landed = True
+                    c.qkfull[i % 3].complete_tx(LAT)
+                self.later(land_lat)
+                yield None
             if i >= 2:
                 yield ("wait", c.sfull[(i - 2) % 3], (i - 2) // 3)
             rs = c.rope_slot[i % 2]
@@ -196,9 +227,16 @@ class Sim:
         for i in range(n):
             if i >= 2 and "no_sfree" not in self.faults:
                 yield ("wait", c.sfree[(i - 2) % 3], (i - 2) // 3)
-            yield ("wait", c.qkfull[i % 3], i // 3)
-            s, sb = c.qk_slot[i % 3], c.s_buf[i & 1]
-            check(s.tile == i and s.landed, f"r{c.rank}: QK({i}) reads a latent slot that does not hold tile {i}")
+            sb = c.s_buf[i & 1]
+            if self.fp8:
+                yield ("wait", c.slotfull[i % 4], i // 4)
+                s8 = c.slot8[i % 4]
+                check(s8["tile"] == i and all(s8["written"]), f"r{c.rank}: QK({i}) reads a slot not holding tile {i}")
+                s = Slot()
+            else:
+                yield ("wait", c.qkfull[i % 3], i // 3)
+                s = c.qk_slot[i % 3]
+                check(s.tile == i and s.landed, f"r{c.rank}: QK({i}) reads a latent slot that does not hold tile {i}")
             check(all(sb["read"]), f"r{c.rank}: QK({i}) overwrites S buffer {i & 1} before tile {sb['tile']} was read")
             sb["tile"], sb["read"] = i, [False] * 4
             yield ("wait", c.ropefull[i % 2], i // 2)
@@ -228,6 +266,21 @@ class Sim:
 
         if self.rng.random() < 0.3:     # the issuer may start late
             yield ("wait", Delay(self, self.step_no + self.rng.randint(1, 400)), 0)
+        if self.fp8:
+            for i in range(n):
+                yield ("wait", c.pfull, i)
+                p, s8 = c.p_buf, c.slot8[i % 4]
+                check(p["tile"] == i and all(p["written"]), f"r{c.rank}: PV({i}) reads a P buffer not holding tile {i}")
+                check(s8["tile"] == i and all(s8["written"]), f"r{c.rank}: PV({i}) reads a slot not holding tile {i}")
+
+                def done8(i=i, s8=s8, p=p):
+                    s8["done"] = True
+                    p["consumed"] = True
+                    c.slotempty[i % 4].arrive()
+                    c.pvdone[i % 3].arrive()
+                self.later_in_order(("pv", c.rank), done8)
+                yield None
+            return
         for i in range(min(2, n)):
             # The first V tiles are requested once the same rows have landed in the score
             # ring (phase 0 of its slot), so that they come from L2.
@@ -255,12 +308,32 @@ class Sim:
             self.later_in_order(("pv", c.rank), done)
             yield None
 
+    def convert(self, c, j, q):
+        """FP8: this warp's share of widening tile j (staging j % 2 -> slot j % 4)."""
+        if j >= 2 and "no_prevwiden" not in self.faults:
+            yield ("wait", c.slotfull[(j - 2) % 4], (j - 2) // 4)
+        yield ("wait", c.stageloaded[j % 2], j // 2)
+        if j >= 4 and "no_slotempty" not in self.faults:
+            yield ("wait", c.slotempty[j % 4], j // 4 - 1)
+        st, s8 = c.stage[j % 2], c.slot8[j % 4]
+        check(st["tile"] == j and st["landed"], f"r{c.rank}: widening tile {j} from staging holding {st['tile']}")
+        st["read"][q] = True
+        c.stagefree[j % 2].arrive(1)
+        if s8["tile"] != j:
+            check(s8["done"], f"r{c.rank}: tile {j} overwrites slot {j % 4} before PV of tile {s8['tile']}")
+            s8["tile"], s8["written"], s8["done"] = j, [False] * 4, False
+        s8["written"][q] = True
+        c.slotfull[j % 4].arrive(32)
+        yield None
+
     def group_warp(self, c, peer, g, q):
         n = self.n
         if g < 2:
             c.qready.arrive(32)            # this warp's q~ columns are in TMEM
         if q == 0 and g < n:
             c.recvfull[g].arrive(1, tx=RECV)
+        if self.fp8 and g < n:
+            yield from self.convert(c, g, q)
         for i in range(g, n, 3):
             k = i // 3
             b = i & 1
@@ -314,12 +387,14 @@ class Sim:
                 check(p["consumed"], f"r{c.rank} g{g}: P of tile {i} overwrites tile {p['tile']} before its PV")
                 p["tile"], p["written"], p["consumed"] = i, [False] * 4, False
             p["written"][q] = True
-            if i == n - 1 and self.partial_last:
+            if i == n - 1 and self.partial_last and not self.fp8:
                 yield ("wait", c.vfull[i % 2], i // 2)
                 v = c.v_slot[i % 2]
                 check(v.tile == i and v.landed, f"r{c.rank} g{g}: clears a V slot that does not hold tile {i}")
             c.pfull.arrive(32)
             yield None
+            if self.fp8 and i + 3 < n:
+                yield from self.convert(c, i + 3, q)
         yield ("wait", c.pvdone[(n - 1) % 3], (n - 1) // 3)
 
     # ---- scheduler
@@ -373,6 +448,38 @@ class Sim:
 def test_protocol_holds_under_random_schedules(n, partial_last):
     for seed in range(40):
         assert Sim(n, seed, partial_last).run()
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 13])
+def test_fp8_protocol_holds_under_random_schedules(n):
+    for seed in range(40):
+        assert Sim(n, seed, seed % 2 == 1, fp8=True).run()
+
+
+@pytest.mark.parametrize("fault", ["no_prevwiden", "no_stagefree"])
+def test_the_fp8_model_catches_a_broken_rule(fault):
+    # - no_prevwiden: the group waits for tile i's bytes in the shared staging buffer
+    #   without first waiting for tile i-2 to be widened, so its parity wait can take the
+    #   phase of tile i-2 (the mistake of an earlier version of this instance);
+    # - no_stagefree: tile i is loaded into staging buffer i % 2 before tile i-2 was read.
+    # Some schedule must trip an assertion or deadlock.
+    failures = 0
+    for seed in range(200):
+        for n in (7, 13):
+            try:
+                Sim(n, seed, False, faults=[fault], fp8=True).run()
+            except ProtocolError:
+                failures += 1
+    assert failures > 0, f"no schedule exposed {fault}"
+
+
+@pytest.mark.parametrize("n", [5, 7, 13])
+def test_fp8_slot_empty_wait_is_implied(n):
+    # The group also waits for PV(i-4) before widening tile i into slot i % 4 (kSlotEmpty).
+    # The model shows it is implied: the group widens tile i after finishing tile i-3, for
+    # which it waited for PV(i-4).  Without it every schedule holds.
+    for seed in range(60):
+        assert Sim(n, seed, False, faults=["no_slotempty"], fp8=True).run()
 
 
 @pytest.mark.parametrize("fault", ["no_sfree", "no_freeseen", "no_vgo"])

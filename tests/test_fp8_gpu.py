@@ -1,0 +1,197 @@
+"""FP8 latent cache ("DeepSeek Multi-Head Latent Attention(MLA) 아키텍처 해부", section 5, the
+checklist item on FP8 mixed precision): the quantizer against the oracle byte for byte,
+and the decode over the FP8 form against the oracle's attention over the dequantized
+rows (o_lat rows within 1e-2, LSE within 1e-3), plus the host-side rejects.
+
+The decode's inputs are drawn directly in the FP8 form (inputs.seq_fp8_rows: codes and
+power-of-two scales from a seeded generator), so the oracle's inputs never pass through
+the CUDA quantizer."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from mla_latent_kv_70_b300 import inputs as I
+from tests.mla_cases import LSE_ABS_TOL, ROW_REL_TOL, log_lse, lse_err, row_rel_err
+
+P = 4096  # a fake 16-byte aligned address: a call rejected on the host never dereferences it
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import mla_latent_kv_70_b300 as mla
+    from mla_latent_kv_70_b300 import build
+    build.build()
+    return mla.lib()
+
+
+# ----------------------------------------------------------------------------
+# Host-side rejects (no GPU)
+# ----------------------------------------------------------------------------
+
+def test_quantize_rejects_on_the_host(lib):
+    f = lib.mla_quantize_fp8
+    assert f(None, 576, 4, P, P, None) == 1
+    assert f(P, 576, 4, None, P, None) == 1
+    assert f(P, 576, 4, P, None, None) == 1
+    assert f(P, 570, 4, P, P, None) == 1          # row stride below 576
+    assert f(P, 580, 4, P, P, None) == 1          # row stride not a multiple of 8
+    assert f(P + 8, 576, 4, P, P, None) == 1      # rows not 16-byte aligned
+    assert f(P, 576, 4, P + 4, P, None) == 1      # kv8 not 16-byte aligned
+    assert f(P, 576, 4, P, P + 2, None) == 1      # scales not 4-byte aligned
+    assert f(P, 576, -1, P, P, None) == 1
+    assert f(P, 576, 0, P, P, None) == 0          # nothing to do
+
+
+def fp8_args(**over):
+    a = dict(q_cat=P, kv8=P, kv_scale=P, kv_seq_stride=256, seqlens=P, block_table=None, max_pages=0,
+             page_size=64, num_pages=0, B=4, S=1, H=16, causal=0, scale=0.07, num_splits=1,
+             max_seqlen=256, o_lat=P, lse=P, workspace=None, workspace_bytes=0, status=None, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(kv_scale=None), 1), (dict(kv_scale=P + 2), 1), (dict(kv8=None), 1), (dict(kv8=P + 8), 1),
+    (dict(q_cat=None), 1), (dict(H=24), 2), (dict(S=5), 2), (dict(num_splits=129), 1),
+    (dict(block_table=P, page_size=32, max_pages=4, num_pages=4), 2)])
+def test_decode_fp8_rejects_on_the_host(lib, over, code):
+    assert lib.mla_decode_latent_fp8(*fp8_args(**over)) == code
+
+
+# ----------------------------------------------------------------------------
+# Quantizer: bit for bit
+# ----------------------------------------------------------------------------
+
+@pytest.mark.gpu
+def test_quantize_matches_the_oracle_bytewise(lib):
+    import mla_latent_kv_70_b300 as mla
+    g = torch.Generator().manual_seed(11)
+    n = 1500
+    x = torch.randn(n, I.ROW, generator=g) * torch.pow(10.0, torch.empty(n, 1).uniform_(-3, 3, generator=g))
+    x[0] = 0.0                                               # all-zero row: scale 1
+    x[1, 7] = 3.0e6                                          # one large value
+    x[2, :I.D_C] = 1e9                                       # beyond 448 * 2^15: saturates
+    x[3, :I.D_C] = torch.randn(I.D_C, generator=g) * 1e-38   # bf16 subnormals
+    ties = torch.tensor([448.0, 1.0625, 1.1875, -1.0625, 2.0 ** -10, 1.5 * 2.0 ** -10, -2.0 ** -11, 0.0])
+    x[4, :ties.numel()] = ties                               # scale 1: exact ties and tiny values
+    x[4, ties.numel():I.D_C] = 0.5
+    rows = torch.zeros(n, I.ROW + 8, dtype=torch.bfloat16)   # a row stride of 584
+    rows[:, :I.ROW] = x.to(torch.bfloat16)
+    ref_codes, ref_kr, ref_scales = O.quantize_fp8_rows(rows[:, :I.ROW].double().numpy())
+    d_rows = rows.cuda()
+    kv8 = torch.full((n, I.FP8_ROW), 0xAA, dtype=torch.uint8, device="cuda")
+    sc = torch.full((n,), float("nan"), device="cuda")
+    mla.mla_quantize_fp8(d_rows[:, :I.ROW], kv8, sc)
+    torch.cuda.synchronize()
+    kv8, sc = kv8.cpu().numpy(), sc.cpu().numpy()
+    mism = np.argwhere(kv8[:, :I.D_C] != ref_codes)
+    assert mism.size == 0, (mism[:5], kv8[tuple(mism[0])], ref_codes[tuple(mism[0])])
+    assert np.array_equal(kv8[:, I.D_C:], rows[:, I.D_C:I.ROW].contiguous().view(torch.uint8).numpy())
+    assert np.array_equal(sc.astype(np.float64), ref_scales)
+
+
+# ----------------------------------------------------------------------------
+# Decode over the FP8 form
+# ----------------------------------------------------------------------------
+
+class Fp8Case:
+    def __init__(self, case):
+        self.case = case
+        self.kv8, self.sc = I.fp8_cache(case, device="cuda")
+        if not case.paged:   # rows past each sequence hold NaN codes and NaN scales
+            for b, T in enumerate(case.seqlens):
+                self.kv8[b, T:, :I.D_C] = 0x7F
+                self.sc[b, T:] = float("nan")
+        self.q_cat = I.q_cat(case).cuda()
+        self.seqlens = torch.tensor(case.seqlens, dtype=torch.int32, device="cuda")
+        self.block_table = case.block_table.cuda() if case.paged else None
+
+    def run(self, num_splits):
+        import mla_latent_kv_70_b300 as mla
+        c = self.case
+        T = max(c.seqlens)
+        o_lat = torch.full((c.B, c.S, c.H, I.D_C), float("nan"), device="cuda")
+        lse = torch.full((c.B, c.S, c.H), float("nan"), device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = mla.mla_decode_workspace_bytes(c.B, c.S, c.H, num_splits, T)
+        ws = torch.empty(ws // 4, device="cuda") if ws else None
+        mla.mla_decode_latent_fp8(self.q_cat, self.kv8, self.sc, self.seqlens, o_lat, lse, scale=c.scale,
+                                  max_seqlen=T, block_table=self.block_table, causal=c.causal,
+                                  num_splits=num_splits, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        return o_lat.cpu().numpy(), lse.cpu().numpy()
+
+
+def oracle_fp8_seq(case, b):
+    """The oracle's attention of sequence b over its dequantized FP8 rows."""
+    T = case.seqlens[b]
+    rows, sc = I.seq_fp8_rows(case, b)
+    rows, sc = rows[:T], sc[:T]
+    kr = rows[:, I.D_C:].contiguous().view(torch.bfloat16).double().numpy()
+    cache = O.dequantize_fp8_rows(rows[:, :I.D_C].numpy(), kr, sc.double().numpy())
+    q = I.seq_q_cat(case, b).double().numpy()
+    return O.decode_absorbed_seq(q[..., :I.D_C], q[..., I.D_C:], cache[:, :I.D_C], cache[:, I.D_C:],
+                                 case.scale, case.causal)
+
+
+def check_fp8(case, o_lat, lse, seqs, key):
+    for b in seqs:
+        r_lat, r_lse = oracle_fp8_seq(case, b)
+        assert row_rel_err(o_lat[b], r_lat) <= ROW_REL_TOL, (key, b)
+        err = lse_err(lse[b], r_lse)
+        log_lse(key, err, LSE_ABS_TOL)
+        assert err <= LSE_ABS_TOL, (key, b, err)
+
+
+CASES = {
+    # every tile count 1..11 with ragged tails, T = 1 and an empty sequence
+    "ragged": lambda: I.make_case("fp8_ragged", 5, 1, 16, [1, 0, 200, 700, 64], seed=21, t_cap=720),
+    "heads128": lambda: I.make_case("fp8_h128", 2, 1, 128, [333, 1024], seed=22, t_cap=1040),
+    "causal_s2": lambda: I.make_case("fp8_causal", 3, 2, 64, [2, 130, 511], causal=True, seed=23, t_cap=520),
+    "paged": lambda: I.make_case("fp8_paged", 3, 1, 32, [64, 640, 1000], paged=True, seed=24),
+    "paged_causal_s3": lambda: I.make_case("fp8_paged_c3", 2, 3, 16, [5, 900], paged=True, causal=True, seed=25),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_fp8_matches_the_oracle(lib, name, splits):
+    case = CASES[name]()
+    fc = Fp8Case(case)
+    o_lat, lse = fc.run(splits)
+    check_fp8(case, o_lat, lse, range(case.B), f"{name}/{splits}")
+
+
+@pytest.mark.gpu
+def test_decode_fp8_equals_the_bf16_decode_on_the_widened_cache(lib):
+    # Widening E4M3 * (power-of-two scale) to bf16 is exact, so the bf16 decode over the
+    # widened rows reads the same operands in the same order: the results agree bit for bit.
+    import mla_latent_kv_70_b300 as mla
+    case = I.make_case("fp8_same", 4, 1, 128, [1, 100, 1000, 2048], seed=26, t_cap=2048)
+    fc = Fp8Case(case)
+    codes = fc.kv8[..., :I.D_C].contiguous().view(torch.float8_e4m3fn).float()
+    lat = torch.nan_to_num(codes * fc.sc[..., None], nan=0.0)
+    kv = torch.cat([lat.to(torch.bfloat16), fc.kv8[..., I.D_C:].contiguous().view(torch.bfloat16)], dim=-1)
+    for splits in (1, 2):
+        o8, l8 = fc.run(splits)
+        o = torch.empty(case.B, 1, case.H, I.D_C, device="cuda")
+        l = torch.empty(case.B, 1, case.H, device="cuda")
+        ws = mla.mla_decode_workspace_bytes(case.B, 1, case.H, splits, 2048)
+        ws = torch.empty(ws // 4, device="cuda") if ws else None
+        mla.mla_decode_latent(fc.q_cat, kv.contiguous(), fc.seqlens, o, l, scale=case.scale, max_seqlen=2048,
+                              num_splits=splits, workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(o.cpu().numpy(), o8) and np.array_equal(l.cpu().numpy(), l8), splits
+
+
+@pytest.mark.gpu
+def test_decode_fp8_deepseek_v3_full_size(lib):
+    case = I.make_case("fp8_dsv3", 64, 1, 128, [4096] * 64, seed=27)
+    fc = Fp8Case(case)
+    o_lat, lse = fc.run(1)
+    check_fp8(case, o_lat, lse, [0, 31, 63], "dsv3_fp8")
