@@ -210,7 +210,8 @@ mla_status mla_decode_latent(const mla_bf16* q_cat, const mla_bf16* kv, int64_t 
  * multiple of 8) to that form: s = the least power of two 2^e with max|c| / s <= 448,
  * e clamped to [-126, 15] (an all-zero row takes 1); codes = E4M3 of c / s rounded to
  * nearest even, saturating at +-448.  Latent values must be finite.  Writes kv8
- * [n_rows, 640] and kv_scale [n_rows] (both device, 16- and 4-byte aligned).
+ * [n_rows, 640] and kv_scale [n_rows] (both device; kv8 16-byte aligned, kv_scale 4-byte
+ * aligned here and 16-byte aligned for mla_decode_latent_fp8).
  */
 mla_status mla_quantize_fp8(const mla_bf16* rows, int64_t row_stride, int64_t n_rows, uint8_t* kv8,
                             float* kv_scale, mla_stream stream);
@@ -221,8 +222,9 @@ mla_status mla_quantize_fp8(const mla_bf16* rows, int64_t row_stride, int64_t n_
  * bf16 for the power-of-two scales mla_quantize_fp8 writes; other scales are rounded
  * once to bf16 after the product) and whose k^R is the stored one.  Arguments as for
  * mla_decode_latent, with kv8 (640-byte rows, 16-byte aligned) and kv_scale (fp32, one
- * per row) in place of kv; scales must lie in [2^-126, 2^15].  Same workspace, split
- * planning, status flags and early-start contract.
+ * per row, 16-byte aligned) in place of kv; scales must lie in [2^-126, 2^15].  For a
+ * contiguous cache kv_seq_stride is a multiple of 4 (a tile's 64 scales are read as one
+ * 256-byte block).  Same workspace, split planning, status flags and early-start contract.
  */
 mla_status mla_decode_latent_fp8(const mla_bf16* q_cat, const uint8_t* kv8, const float* kv_scale,
                                  int64_t kv_seq_stride, const int32_t* seqlens, const int32_t* block_table,

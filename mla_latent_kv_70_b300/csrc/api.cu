@@ -195,7 +195,9 @@ mla_status decode_any(const mla_bf16* q_cat, const void* kv, const float* kv_sca
                                                 max_pages, page_size, num_pages, B, S, H, scale,
                                                 num_splits, max_seqlen, o_lat, lse);
   if (bad != MLA_OK) return bad;
-  if (fp8 && (!kv_scale || (reinterpret_cast<uintptr_t>(kv_scale) & 3u))) return MLA_ERR_INVALID;
+  // FP8: a tile's 64 scales are one TMA box, so the scale array is 16-byte aligned and a
+  // contiguous cache keeps sequences a multiple of 4 rows apart.
+  if (fp8 && (!kv_scale || !aligned16(kv_scale) || (!block_table && kv_seq_stride % 4))) return MLA_ERR_INVALID;
   const int splits = num_splits ? num_splits : mla_decode_num_splits(B, S, H, max_seqlen, 0);
   const size_t need = mla_decode_workspace_bytes(B, S, H, splits, max_seqlen);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))

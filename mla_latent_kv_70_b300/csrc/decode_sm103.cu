@@ -82,8 +82,10 @@ constexpr uint32_t kOffMref = kOffP + kPBytes;    // [128] reference maximum per
 constexpr uint32_t kOffBars = kOffMref + 128 * 4;
 constexpr uint32_t kOffSlot = kOffBars + 512;
 constexpr uint32_t kOffSig = kOffSlot + 16;       // [4] landing words of the peer's "buffer free" signals
-constexpr uint32_t kSmemBytes = kOffSig + 16 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kOffScale8 = (kOffSig + 16 + 127) & ~127u;   // FP8: [2 staging buffers][64 rows] fp32 row scales
+constexpr uint32_t kSmemBytes = kOffScale8 + 2 * 64 * 4 + 1024;   // + slack for 1024-B alignment
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kOffScale8 % 128 == 0, "TMA destination alignment");
 static_assert(kOffV % 1024 == 0 && kOffP % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
 static_assert(kOffRope % 512 == 0 && kOffQRope % 512 == 0, "64B-swizzled tiles need 512-byte alignment");
 static_assert(kGroups * kGroupThreads * 4 <= 2 * kRecvBytes, "row sums reuse the receive buffers");
@@ -148,6 +150,7 @@ struct Maps {
   CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle (FP8: rows as 320 bf16)
   CUtensorMap q_rope;    // q_cat rows, box 32 cols x 128 rows, 64B swizzle
   CUtensorMap o_store;   // output rows (o_lat or split partials) fp32, box 32 cols x H rows, 128B swizzle
+  CUtensorMap kv_scale;  // FP8: the row scales as one line of fp32, box 64
 };
 
 // Epilogue staging: chunk c (32 output columns of the 128 head rows, 128 B per row,
@@ -319,6 +322,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       prefetch_tmap(&maps.kv_lat);
       prefetch_tmap(&maps.kv_rope);
       prefetch_tmap(&maps.q_rope);
+      prefetch_tmap(&maps.kv_scale);
       int issued = 0, rope_issued = 0;
       bool q_issued = false;
       auto load_q = [&]() {
@@ -335,9 +339,10 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
           aborted = true;
           break;
         }
-        mbar_arrive_expect_tx(bar(kStageLoaded + ss), kLat8Bytes);
+        mbar_arrive_expect_tx(bar(kStageLoaded + ss), kLat8Bytes + kN * 4);
         tma_load_2d(s0 + kOffStage8 + (uint32_t)ss * kLat8Bytes, &maps.kv_lat, bar(kStageLoaded + ss),
                     256 * (int)rank, y);
+        tma_load_2d(s0 + kOffScale8 + (uint32_t)ss * (kN * 4), &maps.kv_scale, bar(kStageLoaded + ss), y, 0);
         ++issued;
         if (i >= kRopeStages &&
             !mbar_wait(bar(kSFull + (i - kRopeStages) % kGroups), (uint32_t)((i - kRopeStages) / kGroups) & 1u, wait_ns)) {
@@ -582,11 +587,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     if (h == 0 && g < ntiles) mbar_arrive_expect_tx(bar(kRecvFull + g), kRecvBytes);
 
     // FP8 cache: the group widens its own tiles (i % 3 == g) from staging into their slots,
-    // tile g before its first tile and tile i+3 once it has finished tile i; thread gtid
-    // takes row gtid / 2, E4M3 bytes [128 (gtid % 2), +128) of the CTA's 256 latent columns.  A row's scale is
-    // loaded one conversion ahead; rows past the readable range are written as zeros (so
-    // their zero weights add exactly 0 in PV).
-    const int crow = gtid >> 1, chalf = gtid & 1;
+    // tile g before its first tile and tile i+3 once it has finished tile i, each row
+    // times its scale (landed with the bytes); rows past the readable range are written as
+    // zeros (so their zero weights add exactly 0 in PV).
     auto tile_valid = [&](int j) {
       const int t = t0 + j * kN;
       int v = min(kN, t1 - t);
@@ -596,43 +599,52 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       return v;
     };
-    auto row_scale = [&](int j) -> float {
-      if (!kFp8 || j >= ntiles || crow >= tile_valid(j)) return 0.f;
-      return p.kv_scale[tile_row(p, b, t0 + j * kN, false) + crow];
-    };
-    auto convert = [&](int j, float sc) -> bool {
+    auto convert = [&](int j) -> bool {
       const int ss = j % kSlots8, gs = j % kStages8;
       const uint32_t slot = s0 + kOffQk + (uint32_t)ss * kLatBytes;
       // Tile j-2 is widened (so staging buffer j % 2 is in the phase of tile j), tile j's
-      // E4M3 bytes have landed, and the slot is free (PV(j-4) is done: the group waited
-      // for it before finishing tile j-3, so that wait returns at once).
+      // E4M3 bytes and scales have landed, and the slot is free (PV(j-4) is done: the group
+      // waited for it before finishing tile j-3, so that wait returns at once).
       if ((j >= 2 && !warp_wait(bar(kSlotFull + (j - 2) % kSlots8), (uint32_t)((j - 2) / kSlots8) & 1u, wait_ns)) ||
           !warp_wait(bar(kStageLoaded + gs), (uint32_t)(j / kStages8) & 1u, wait_ns) ||
           (j >= kSlots8 && !warp_wait(bar(kSlotEmpty + ss), (uint32_t)(j / kSlots8 - 1) & 1u, wait_ns)))
         return false;
-      // Chunk order rotated by (2 row + half): the eight threads of a shared-memory
-      // wavefront then read eight different bank groups of their 256-byte rows.
+      // Eight passes over the tile's 64 rows x 16 chunks (16 E4M3 bytes each).  In pass
+      // pp, the eight threads of a shared-memory wavefront take four chunks of an even row
+      // and the four chunks of the other parity of quarter of the odd row after it: their
+      // staging reads hit eight different bank groups, and so do their bf16 stores (the
+      // 128B swizzle puts the even row's chunks in even and the odd row's in odd groups).
+      const uint32_t stage = s0 + kOffStage8 + (uint32_t)gs * kLat8Bytes;
+      const float* scl = reinterpret_cast<const float*>(smem + kOffScale8 + gs * (kN * 4));
+      const int valid = tile_valid(j);
+      const int sub = (gtid >> 2) & 1, l4 = gtid & 3;
       uint4 w[8];
-      const uint32_t rot = (uint32_t)(2 * crow + chalf) & 7u;
-      const uint32_t src = s0 + kOffStage8 + (uint32_t)gs * kLat8Bytes + (uint32_t)crow * 256u + (uint32_t)chalf * 128u;
+      int rowv[8], qv[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) w[c] = ld_shared_u4(src + 16u * (((uint32_t)c + rot) & 7u));
+      for (int pp = 0; pp < 8; ++pp) {
+        const int k = pp * 16 + (gtid >> 3);             // task: row pair k / 4, quarter k % 4
+        rowv[pp] = 2 * (k >> 2) + sub;
+        qv[pp] = (k & 3) ^ sub;
+        w[pp] = ld_shared_u4(stage + (uint32_t)rowv[pp] * 256u + (uint32_t)(16 * (4 * qv[pp] + l4)));
+      }
+      float sc[8];
+#pragma unroll
+      for (int pp = 0; pp < 8; ++pp) sc[pp] = scl[rowv[pp]];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kStageFree + gs));   // the staging buffer may be refilled
-      const bool live = crow < tile_valid(j);
-      const float mul = sc * 0x1p112f;
-      const uint32_t mul2 = f2_to_bf2(mul, mul);
-      const uint32_t sw = (uint32_t)(crow & 7);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t ww[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+      for (int pp = 0; pp < 8; ++pp) {
+        const int r = rowv[pp];
+        const float mul = sc[pp] * 0x1p112f;
+        const uint32_t mul2 = f2_to_bf2(mul, mul);
+        const uint32_t ww[4] = {w[pp].x, w[pp].y, w[pp].z, w[pp].w};
         uint32_t o[8];
 #pragma unroll
         for (int u = 0; u < 4; ++u) e4m3x4_to_bf16(ww[u], mul2, o[2 * u], o[2 * u + 1]);
-        const int col = 128 * chalf + 16 * (int)(((uint32_t)c + rot) & 7u);   // the first of these 16 columns
-        const uint32_t rowp = slot + (uint32_t)(col >> 6) * kBoxBytes + (uint32_t)crow * 128u;
-        const uint32_t j0 = (uint32_t)((col & 63) >> 3);      // its 16-byte chunk in the row
-        if (live) {   // 128B swizzle: chunk j of row r sits at chunk j ^ (r & 7)
+        // Columns 16 (4 q + l4) .. +15: box q, 16-byte chunks 2 l4 and 2 l4 + 1 of the row.
+        const uint32_t rowp = slot + (uint32_t)qv[pp] * kBoxBytes + (uint32_t)r * 128u;
+        const uint32_t j0 = (uint32_t)(2 * l4), sw = (uint32_t)(r & 7);
+        if (r < valid) {   // 128B swizzle: chunk c of row r sits at chunk c ^ (r & 7)
           st_shared_u4(rowp + ((j0 ^ sw) << 4), o[0], o[1], o[2], o[3]);
           st_shared_u4(rowp + (((j0 + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
         } else {
@@ -644,12 +656,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       mbar_arrive(bar(kSlotFull + ss));
       return true;
     };
-    float sc_next = 0.f;
-    if (kFp8) {
-      sc_next = row_scale(g);
-      if (g < ntiles && !convert(g, sc_next)) aborted = true;
-      sc_next = row_scale(g + kGroups);
-    }
+    if (kFp8 && g < ntiles && !convert(g)) aborted = true;
 
     float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
     for (int i = g; i < ntiles && !aborted; i += kGroups) {
@@ -839,12 +846,9 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kPFull));
-      if (kFp8 && i + kGroups < ntiles) {
-        if (!convert(i + kGroups, sc_next)) {
-          aborted = true;
-          break;
-        }
-        sc_next = row_scale(i + 2 * kGroups);
+      if (kFp8 && i + kGroups < ntiles && !convert(i + kGroups)) {
+        aborted = true;
+        break;
       }
     }
 
@@ -939,7 +943,10 @@ cudaError_t launch_decode_impl(DecodeParams p, cudaStream_t st) {
                  encode_tma_2d(&maps.kv_rope, true, p.kv, kRow8 / 2, kv_rows, kRow8, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B)
            : encode_rows(&maps.kv_lat, p.kv, kv_rows, 64, kN, CU_TENSOR_MAP_SWIZZLE_128B) &&
                  encode_rows(&maps.kv_rope, p.kv, kv_rows, 32, kN, CU_TENSOR_MAP_SWIZZLE_64B);
-  if (!kv_ok || !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  // FP8: the scales as one line of kv_rows fp32 (x = the tile's first row, a multiple of 4).
+  const bool scale_ok = !kFp8 || encode_tma_2d(&maps.kv_scale, false, p.kv_scale, kv_rows, 1,
+                                               (kv_rows * 4 + 15) & ~uint64_t(15), kN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!kv_ok || !scale_ok || !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !encode_tma_2d(&maps.o_store, false, p.o_out, kDc, o_rows, (uint64_t)kDc * 4, 32, (uint32_t)p.H,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;

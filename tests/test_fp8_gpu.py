@@ -54,7 +54,8 @@ def fp8_args(**over):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(kv_scale=None), 1), (dict(kv_scale=P + 2), 1), (dict(kv8=None), 1), (dict(kv8=P + 8), 1),
+    (dict(kv_scale=None), 1), (dict(kv_scale=P + 4), 1), (dict(kv_seq_stride=258, max_seqlen=256), 1),
+    (dict(kv8=None), 1), (dict(kv8=P + 8), 1),
     (dict(q_cat=None), 1), (dict(H=24), 2), (dict(S=5), 2), (dict(num_splits=129), 1),
     (dict(block_table=P, page_size=32, max_pages=4, num_pages=4), 2)])
 def test_decode_fp8_rejects_on_the_host(lib, over, code):
