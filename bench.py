@@ -392,6 +392,8 @@ EXTRA = {
     "prefill_4k": "prefill of one 4096-token prompt, H=128 (mla_prefill: K_h, V_h built, causal attention)",
     "dsv3_fused": "DeepSeek-V3 decode step on pre-fused weights: c^Q W_UQK -> latent attention -> "
                   "sum_h z_h W_UVO[h] (d_cq=1536, d_model=4096)",
+    "dsv3_fp8": "DeepSeek-V3 decode step over the FP8 latent cache (E4M3 latent + bf16 k^R, 640-byte rows, "
+                "power-of-two scale per row, quantized by mla_quantize_fp8 before timing)",
 }
 
 
@@ -422,6 +424,20 @@ def cpu_baseline_extra(name, case, min_seconds=10.0):
         dt = time.perf_counter() - t0
         value = case.S / (dt * case.H / heads)
         sample = f"{heads} of {case.H} heads of the {T}-token prompt (fp64 expanded attention), {dt:.1f} s, scaled to all heads"
+    elif name == "dsv3_fp8":
+        w_uk, w_uv = (d(w) for w in I.weights(case))
+        seqs = 0
+        while seqs == 0 or (time.perf_counter() - t0 < min_seconds and seqs < case.B):
+            T = case.seqlens[seqs]
+            codes, kr, scales = O.quantize_fp8_rows(d(I.seq_rows(case, seqs)[:T]))
+            rows = O.dequantize_fp8_rows(codes, kr, scales)
+            qn, qr = (d(t) for t in I.seq_queries(case, seqs))
+            o_lat, _ = O.decode_absorbed_seq(O.absorb_q(qn, w_uk), qr, rows[:, :512], rows[:, 512:], case.scale)
+            O.out_proj_uv(o_lat, w_uv)
+            seqs += 1
+        dt = time.perf_counter() - t0
+        value = seqs * case.S / dt
+        sample = f"{seqs} whole sequences (E4M3 quantization, absorbed fp64 attention, W_UV), {dt:.1f} s"
     else:
         w_uk, w_uv = (d(w) for w in I.weights(case))
         w_uq, w_o = d(I.query_side_weights(case)), d(I.output_weights(case))
@@ -487,6 +503,29 @@ def run_extra(args):
         flops = prefill_flops(B, S, T, H)
         alg_bytes = B * T * 1152 + B * S * H * (192 * 2 + 128 * 4 + 4) + 2 * H * 512 * 128 * 2
         kernel = "mla_prefill (K_h, V_h expansion GEMMs + causal attention)"
+    elif name == "dsv3_fp8":
+        kv8 = torch.empty(case.B, case.t_cap, I.FP8_ROW, dtype=torch.uint8, device=dev)
+        kv_sc = torch.empty(case.B, case.t_cap, device=dev)
+        mla.mla_quantize_fp8(kv.view(-1, I.ROW), kv8.view(-1, I.FP8_ROW), kv_sc.view(-1))
+        del kv
+        seqlens = torch.tensor(case.seqlens, dtype=torch.int32, device=dev)
+        dstep = mla.DecodeStep(B, S, H, w_uk, w_uv, max_seqlen=max(case.seqlens), seqlens=case.seqlens)
+        inputs_h, inputs_d, result = [qn_h, qr_h], [q_nope, q_rope], dstep.o
+
+        def step(st, marks=None):
+            mla.mla_absorb_q(q_nope, q_rope, w_uk, None, case.theta, dstep.q_cat, st)
+            if marks:
+                marks(0)
+            mla.mla_decode_latent_fp8(dstep.q_cat, kv8, kv_sc, seqlens, dstep.o_lat, dstep.lse, scale=case.scale,
+                                      max_seqlen=dstep.max_seqlen, num_splits=dstep.num_splits,
+                                      workspace=dstep.workspace, status=dstep.status, stream=st)
+            if marks:
+                marks(1)
+            mla.mla_out_proj_uv(dstep.o_lat, w_uv, dstep.o, st)
+        rows_read = sum(case.seqlens)
+        flops = 2.0 * B * S * H * (576 + 512) * rows_read / B
+        alg_bytes = rows_read * (I.FP8_ROW + 4) + B * S * H * (1152 + 2048 + 4)
+        kernel = "mla_decode_latent_fp8 (E4M3 tiles widened to bf16 in shared memory)"
     else:
         w_uq, w_o = I.query_side_weights(case).to(dev), I.output_weights(case).to(dev)
         d_cq, d_model = w_uq.shape[1], w_o.shape[2]
@@ -595,7 +634,7 @@ def run_extra(args):
             "clocks": clock_info,
             "e2e": {"value": whole_job_rate(world, tokens, e2e_ms / args.steps), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * (3 if name == "prefill_4k" else 6),
+            "gpu_launches": args.steps * (3 if name in ("prefill_4k", "dsv3_fp8") else 6),
             "roofline": roof}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_extra(name, case)
@@ -607,7 +646,9 @@ def run_extra(args):
 
 METRIC_EXTRA = {"prefill_4k": "MLA prefill tokens/s (one attention layer, expanded order)",
                 "dsv3_fused": "MLA decode tokens/s on pre-fused weights (one attention layer: "
-                              "c^Q W_UQK + latent attention + sum_h z_h W_UVO[h])"}
+                              "c^Q W_UQK + latent attention + sum_h z_h W_UVO[h])",
+                "dsv3_fp8": "MLA decode tokens/s over the FP8 latent cache (one attention layer: "
+                            "absorb + latent attention + W_UV)"}
 
 
 def main():

@@ -12,7 +12,8 @@ import math
 import torch
 
 from . import (D_C, D_V, ROW, mla_absorb_q, mla_append_latent, mla_decode_latent,
-               mla_decode_num_splits, mla_decode_plan_splits, mla_decode_workspace_bytes, mla_out_proj_uv)
+               mla_decode_latent_fp8, mla_decode_num_splits, mla_decode_plan_splits,
+               mla_decode_workspace_bytes, mla_out_proj_uv)
 
 
 class DecodeStep:
@@ -52,7 +53,8 @@ class DecodeStep:
         mla_append_latent(new_rows, seqlens, kv, rope_theta=self.rope_theta if self.rope else 0.0,
                           block_table=block_table, status=self.status, stream=stream)
 
-    def capture(self, q_nope, q_rope, kv, seqlens, *, block_table=None, q_pos=None, new_rows=None):
+    def capture(self, q_nope, q_rope, kv, seqlens, *, block_table=None, q_pos=None, new_rows=None,
+                kv_scale=None):
         """Record one step on these buffers as a CUDA graph and return a callable that
         replays it on the current stream.  The library makes no host synchronisation, so
         the step is capturable; a replay reads whatever the given tensors hold then, and
@@ -61,7 +63,7 @@ class DecodeStep:
         new_rows it appends, so seqlens has advanced by S once capture() returns."""
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        kw = dict(block_table=block_table, q_pos=q_pos, new_rows=new_rows)
+        kw = dict(block_table=block_table, q_pos=q_pos, new_rows=new_rows, kv_scale=kv_scale)
         with torch.cuda.stream(side):
             self(q_nope, q_rope, kv, seqlens, **kw)
         torch.cuda.current_stream().wait_stream(side)
@@ -72,15 +74,20 @@ class DecodeStep:
         return graph.replay
 
     def __call__(self, q_nope, q_rope, kv, seqlens, *, block_table=None, q_pos=None,
-                 new_rows=None, stream=None):
+                 new_rows=None, kv_scale=None, stream=None):
         """One step; with new_rows [B,S,576] the step's latent rows are appended first
-        (seqlens advance by S, so max_seqlen must cover the grown sequences)."""
+        (seqlens advance by S, so max_seqlen must cover the grown sequences).  A uint8 kv
+        is the FP8 form of the cache (640-byte rows) with its row scales in kv_scale."""
         if new_rows is not None:
+            if kv.dtype == torch.uint8:
+                raise ValueError("appending to the FP8 cache goes through mla_quantize_fp8")
             self.append(new_rows, kv, seqlens, block_table=block_table, stream=stream)
         mla_absorb_q(q_nope, q_rope, self.w_uk, q_pos, self.rope_theta, self.q_cat, stream)
-        mla_decode_latent(self.q_cat, kv, seqlens, self.o_lat, self.lse, scale=self.scale,
-                          max_seqlen=self.max_seqlen, block_table=block_table,
-                          causal=self.causal, num_splits=self.num_splits,
-                          workspace=self.workspace, status=self.status, stream=stream)
+        kw = dict(scale=self.scale, max_seqlen=self.max_seqlen, block_table=block_table, causal=self.causal,
+                  num_splits=self.num_splits, workspace=self.workspace, status=self.status, stream=stream)
+        if kv.dtype == torch.uint8:
+            mla_decode_latent_fp8(self.q_cat, kv, kv_scale, seqlens, self.o_lat, self.lse, **kw)
+        else:
+            mla_decode_latent(self.q_cat, kv, seqlens, self.o_lat, self.lse, **kw)
         mla_out_proj_uv(self.o_lat, self.w_uv, self.o, stream)
         return self.o
