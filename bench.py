@@ -619,7 +619,8 @@ def run_extra(args):
         roof = {"bound": "tensor", "achieved": flops / part_s / 1e12, "peak": tf_burst, "unit": "TFLOP/s"}
     else:
         roof = {"bound": "hbm", "achieved": alg_bytes / part_s / 1e9, "peak": hbm, "unit": "GB/s"}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": kernel,
+    roof.update({"frac": roof["achieved"] / roof["peak"],
+                 "traffic": recorded_traffic(name, 1) if name == "dsv3_fp8" else None, "kernel": kernel,
                  "peak_source": f"{peak_kind} (MEASURED_PEAKS.json burst)", "kernel_us": part_s * 1e6,
                  "algorithmic_bytes": alg_bytes, "flops": flops, "roofline_us": max(t_hbm, t_tc) * 1e6})
     tokens = B * S

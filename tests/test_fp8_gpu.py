@@ -196,3 +196,30 @@ def test_decode_fp8_deepseek_v3_full_size(lib):
     fc = Fp8Case(case)
     o_lat, lse = fc.run(1)
     check_fp8(case, o_lat, lse, [0, 31, 63], "dsv3_fp8")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("splits", [1, 3])
+def test_decode_fp8_timeout_is_flagged_and_device_recovers(lib, splits):
+    # The test hook withholds the score commit of each unit's first tile and shortens the
+    # wait limit to 1 ms: every unit gives up, records the timeout and writes the empty
+    # result; the next ordinary call on the same device matches the oracle.
+    import mla_latent_kv_70_b300 as mla
+    case = I.make_case("fp8_timeout", 3, 1, 128, [300, 130, 64], seed=62, t_cap=320)
+    fc = Fp8Case(case)
+    o_lat = torch.full((case.B, 1, case.H, I.D_C), float("nan"), device="cuda")
+    lse = torch.full((case.B, 1, case.H), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = mla.mla_decode_workspace_bytes(case.B, 1, case.H, splits, 300)
+    ws = torch.empty(ws // 4, device="cuda") if ws else None
+    mla.mla_debug_inject_timeout(mla.FAULT_DECODE, 1.0)
+    try:
+        mla.mla_decode_latent_fp8(fc.q_cat, fc.kv8, fc.sc, fc.seqlens, o_lat, lse, scale=case.scale,
+                                  max_seqlen=300, num_splits=splits, workspace=ws, status=status)
+        torch.cuda.synchronize()
+    finally:
+        mla.mla_debug_inject_timeout(0)
+    assert int(status.item()) & mla.FLAG_TIMEOUT
+    assert torch.all(o_lat == 0) and torch.all(torch.isneginf(lse))
+    o_lat, lse = fc.run(splits)
+    check_fp8(case, o_lat, lse, range(case.B), f"fp8_recovery/{splits}")
