@@ -217,6 +217,20 @@ mla_status mla_quantize_fp8(const mla_bf16* rows, int64_t row_stride, int64_t n_
                             float* kv_scale, mla_stream stream);
 
 /*
+ * mla_append_latent_fp8 -- mla_append_latent into the FP8 form of the cache: row s of
+ * sequence b (bf16 [B,S,576], S <= 4) goes to position seqlens[b] + s of kv8 / kv_scale
+ * (laid out as for mla_decode_latent_fp8), its latent values quantized exactly as by
+ * mla_quantize_fp8, its k^R rotated at that position as by mla_append_latent (when
+ * rope_theta > 0) and stored as bf16; seqlens[b] += S.  A row with no place is skipped
+ * and 1 << MLA_ERR_BLOCK_TABLE is OR-ed into *status_dev.  No early start for the next
+ * kernel, as for mla_append_latent.
+ */
+mla_status mla_append_latent_fp8(const mla_bf16* rows, int B, int S, float rope_theta, int32_t* seqlens,
+                                 uint8_t* kv8, float* kv_scale, int64_t kv_seq_stride, const int32_t* block_table,
+                                 int max_pages, int page_size, int num_pages, int32_t* status_dev,
+                                 mla_stream stream);
+
+/*
  * mla_decode_latent_fp8 -- mla_decode_latent over the FP8 form of the cache: the same
  * result as mla_decode_latent on rows whose latent part is s * E4M3(code) (exact in
  * bf16 for the power-of-two scales mla_quantize_fp8 writes; other scales are rounded

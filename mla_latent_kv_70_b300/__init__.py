@@ -38,6 +38,7 @@ SIGNATURES = {
     "mla_decode_latent_fp8": (_I, [_P, _P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                                    _P, _P, _P, _SZ, _P, _P]),
     "mla_quantize_fp8": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "mla_append_latent_fp8": (_I, [_P, _I, _I, _F, _P, _P, _P, _I64, _P, _I, _I, _I, _P, _P]),
     "mla_decode_latent_noalloc": (_I, [_P, _P, _I64, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                        _I, _P, _P, _P, _P]),
     "mla_combine_partials": (_I, [_P, _P, _I, _I64, _P, _P, _P]),
@@ -175,6 +176,21 @@ def mla_quantize_fp8(rows, kv8, kv_scale, *, stream=None):
         raise ValueError("output too small")
     _check("mla_quantize_fp8", lib().mla_quantize_fp8(rows.data_ptr(), int(rows.stride(0)), n, _ptr(kv8, _U8),
                                                       _ptr(kv_scale, _F32), _stream(stream)))
+
+
+def mla_append_latent_fp8(rows, seqlens, kv8, kv_scale, *, rope_theta=0.0, block_table=None, kv_seq_stride=0,
+                          page_size=64, status=None, stream=None):
+    """mla_append_latent into the FP8 form of the cache (kv8 uint8 [..., 640], kv_scale fp32)."""
+    B, S, _ = rows.shape
+    if block_table is not None:
+        num_pages, max_pages = kv8.shape[0], block_table.shape[1]
+    else:
+        num_pages, max_pages = 0, 0
+        kv_seq_stride = kv_seq_stride or kv8.shape[1]
+    _check("mla_append_latent_fp8", lib().mla_append_latent_fp8(
+        _ptr(rows, _BF16), B, S, float(rope_theta), _ptr(seqlens, _I32), _ptr(kv8, _U8), _ptr(kv_scale, _F32),
+        int(kv_seq_stride), _ptr(block_table, _I32), max_pages, page_size, num_pages,
+        _ptr(status, _I32), _stream(stream)))
 
 
 def mla_decode_latent_fp8(q_cat, kv8, kv_scale, seqlens, o_lat, lse, *, scale, max_seqlen,

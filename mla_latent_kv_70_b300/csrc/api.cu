@@ -303,6 +303,25 @@ mla_status mla_append_latent(const mla_bf16* rows, int B, int S, float rope_thet
       static_cast<cudaStream_t>(stream)));
 }
 
+mla_status mla_append_latent_fp8(const mla_bf16* rows, int B, int S, float rope_theta, int32_t* seqlens,
+                                 uint8_t* kv8, float* kv_scale, int64_t kv_seq_stride, const int32_t* block_table,
+                                 int max_pages, int page_size, int num_pages, int32_t* status_dev,
+                                 mla_stream stream) {
+  if (!rows || !seqlens || !kv8 || !kv_scale) return MLA_ERR_INVALID;
+  if (B < 1 || S < 1 || S > 4 || rope_theta < 0.f || !std::isfinite(rope_theta)) return MLA_ERR_INVALID;
+  if (!aligned16(rows) || !aligned16(kv8) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)) return MLA_ERR_INVALID;
+  if (block_table) {
+    if (page_size != kPage) return MLA_ERR_UNSUPPORTED;
+    if (max_pages < 1 || num_pages < 1) return MLA_ERR_INVALID;
+  } else if (kv_seq_stride < 1) {
+    return MLA_ERR_INVALID;
+  }
+  const mla::RopeFreqs f = mla::make_rope_freqs(rope_theta > 0.f ? rope_theta : 10000.f);
+  return launch_status(mla::launch_append_latent_fp8(
+      reinterpret_cast<const __nv_bfloat16*>(rows), B, S, seqlens, kv8, kv_scale, kv_seq_stride, block_table,
+      max_pages, num_pages, rope_theta > 0.f ? 1 : 0, f, status_dev, static_cast<cudaStream_t>(stream)));
+}
+
 static inline int round16(int x) { return (x + 15) & ~15; }
 
 mla_status mla_fuse_weights(const mla_bf16* w_uq, const mla_bf16* w_uk, const mla_bf16* w_uv,

@@ -189,6 +189,10 @@ cudaError_t launch_decode(DecodeParams p, cudaStream_t st);
 cudaError_t launch_decode_fp8(DecodeParams p, cudaStream_t st);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t row_stride, int64_t n, uint8_t* out,
                                 float* scales, cudaStream_t st);
+cudaError_t launch_append_latent_fp8(const __nv_bfloat16* rows, int B, int S, int32_t* seqlens, uint8_t* kv8,
+                                     float* kv_scale, int64_t kv_seq_stride, const int32_t* block_table,
+                                     int max_pages, int num_pages, int rotate, const RopeFreqs& f,
+                                     int32_t* status, cudaStream_t st);
 cudaError_t launch_append_latent(const __nv_bfloat16* rows, int B, int S, int32_t* seqlens,
                                  __nv_bfloat16* kv, int64_t kv_seq_stride, const int32_t* block_table,
                                  int max_pages, int num_pages, int rotate, const RopeFreqs& f,

@@ -76,7 +76,87 @@ __global__ void __launch_bounds__(256) k_quantize_fp8(const __nv_bfloat16* __res
   }
 }
 
+// The step's new rows straight into the FP8 cache: one CTA per sequence, one warp per new
+// row (S <= 4).  Row s goes to position seqlens[b] + s: its latent values quantized as by
+// k_quantize_fp8, its k^R rotated at that position (as the bf16 append does) and stored
+// as bf16, its scale beside it; seqlens[b] advances by S.  A row with no place is skipped
+// and flagged.  No early trigger: the decode after it sees the rows and the new seqlens.
+__global__ void __launch_bounds__(128) k_append_latent_fp8(const __nv_bfloat16* __restrict__ rows, int S,
+                                                           int32_t* __restrict__ seqlens, uint8_t* __restrict__ kv8,
+                                                           float* __restrict__ kv_scale, int64_t kv_seq_stride,
+                                                           const int32_t* __restrict__ block_table, int max_pages,
+                                                           int num_pages, int rotate, RopeFreqs f,
+                                                           int32_t* __restrict__ status) {
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = seqlens[b];
+  __syncthreads();   // every warp has read seqlens[b] before it is advanced
+  for (int s = warp; s < S; s += 4) {
+    const int t = T + s;
+    int64_t dst = -1;
+    if (block_table) {
+      const int page = (t >= 0 && t / kPage < max_pages) ? block_table[(int64_t)b * max_pages + t / kPage] : -1;
+      if (page >= 0 && page < num_pages) dst = (int64_t)page * kPage + t % kPage;
+    } else if (t >= 0 && t < kv_seq_stride) {
+      dst = (int64_t)b * kv_seq_stride + t;
+    }
+    if (dst < 0) {
+      if (lane == 0) raise_flag(status, kFlagBlockTable);
+      continue;
+    }
+    const __nv_bfloat16* src = rows + ((int64_t)b * S + s) * kRow;
+    const uint4 u0 = reinterpret_cast<const uint4*>(src)[2 * lane];
+    const uint4 u1 = reinterpret_cast<const uint4*>(src)[2 * lane + 1];
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const int e = fp8_scale_exponent(amax);
+    const float inv = exp2i(-e);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      c[i] = fp8x2(x[4 * i] * inv, x[4 * i + 1] * inv) | (fp8x2(x[4 * i + 2] * inv, x[4 * i + 3] * inv) << 16);
+    uint8_t* row8 = kv8 + dst * kFp8Row;
+    reinterpret_cast<uint4*>(row8)[lane] = make_uint4(c[0], c[1], c[2], c[3]);
+    if (lane < 8) {   // k^R: 8 pieces of 4 pairs
+      uint4 v = reinterpret_cast<const uint4*>(src + kDc)[lane];
+      if (rotate) {
+        uint32_t r[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int pair = 4 * lane + j;
+          const float2 p = bf2_to_f2(r[j]);
+          const float2 q = rope_pair(p.x, p.y, t, f.hi[pair], f.lo[pair]);
+          r[j] = f2_to_bf2(q.x, q.y);
+        }
+        v = make_uint4(r[0], r[1], r[2], r[3]);
+      }
+      reinterpret_cast<uint4*>(row8 + kDc)[lane] = v;
+    }
+    if (lane == 0) kv_scale[dst] = exp2i(e);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) seqlens[b] = T + S;
+}
+
 }  // namespace
+
+cudaError_t launch_append_latent_fp8(const __nv_bfloat16* rows, int B, int S, int32_t* seqlens, uint8_t* kv8,
+                                     float* kv_scale, int64_t kv_seq_stride, const int32_t* block_table,
+                                     int max_pages, int num_pages, int rotate, const RopeFreqs& f,
+                                     int32_t* status, cudaStream_t st) {
+  k_append_latent_fp8<<<B, 128, 0, st>>>(rows, S, seqlens, kv8, kv_scale, kv_seq_stride, block_table, max_pages,
+                                         num_pages, rotate, f, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* rows, int64_t row_stride, int64_t n, uint8_t* out,
                                 float* scales, cudaStream_t st) {

@@ -11,7 +11,7 @@ import math
 
 import torch
 
-from . import (D_C, D_V, ROW, mla_absorb_q, mla_append_latent, mla_decode_latent,
+from . import (D_C, D_V, ROW, mla_absorb_q, mla_append_latent, mla_append_latent_fp8, mla_decode_latent,
                mla_decode_latent_fp8, mla_decode_num_splits, mla_decode_plan_splits,
                mla_decode_workspace_bytes, mla_out_proj_uv)
 
@@ -46,12 +46,18 @@ class DecodeStep:
     def kernels_per_step(self) -> int:
         return 3 + (1 if self.num_splits > 1 else 0)
 
-    def append(self, new_rows, kv, seqlens, *, block_table=None, stream=None):
+    def append(self, new_rows, kv, seqlens, *, block_table=None, kv_scale=None, stream=None):
         """Add the step's latent rows [B,S,576] (k^R not yet rotated) at positions
         seqlens[b] + s and advance seqlens; rotated with this step's RoPE base when it
-        applies RoPE (rope_theta > 0)."""
-        mla_append_latent(new_rows, seqlens, kv, rope_theta=self.rope_theta if self.rope else 0.0,
-                          block_table=block_table, status=self.status, stream=stream)
+        applies RoPE (rope_theta > 0).  A uint8 kv is the FP8 cache: the rows are
+        quantized as they are written."""
+        theta = self.rope_theta if self.rope else 0.0
+        if kv.dtype == torch.uint8:
+            mla_append_latent_fp8(new_rows, seqlens, kv, kv_scale, rope_theta=theta, block_table=block_table,
+                                  status=self.status, stream=stream)
+        else:
+            mla_append_latent(new_rows, seqlens, kv, rope_theta=theta, block_table=block_table,
+                              status=self.status, stream=stream)
 
     def capture(self, q_nope, q_rope, kv, seqlens, *, block_table=None, q_pos=None, new_rows=None,
                 kv_scale=None):
@@ -79,9 +85,7 @@ class DecodeStep:
         (seqlens advance by S, so max_seqlen must cover the grown sequences).  A uint8 kv
         is the FP8 form of the cache (640-byte rows) with its row scales in kv_scale."""
         if new_rows is not None:
-            if kv.dtype == torch.uint8:
-                raise ValueError("appending to the FP8 cache goes through mla_quantize_fp8")
-            self.append(new_rows, kv, seqlens, block_table=block_table, stream=stream)
+            self.append(new_rows, kv, seqlens, block_table=block_table, kv_scale=kv_scale, stream=stream)
         mla_absorb_q(q_nope, q_rope, self.w_uk, q_pos, self.rope_theta, self.q_cat, stream)
         kw = dict(scale=self.scale, max_seqlen=self.max_seqlen, block_table=block_table, causal=self.causal,
                   num_splits=self.num_splits, workspace=self.workspace, status=self.status, stream=stream)

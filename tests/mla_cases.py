@@ -200,24 +200,32 @@ def lse_tolerance(case: I.DecodeCase, b: int, w_uk=None) -> np.ndarray:
         KR = O.rope_interleaved(KR, np.arange(T), case.theta)
         pos = np.array([T - S + s for s in range(S)], dtype=np.float64)
         qr = O.rope_interleaved(qr, pos[:, None], case.theta)
-    u, k, sc = U_BF16, K_HOEFFDING, case.scale
     for s in short:
         n = n_vis[s]
-        x = (q_lat[s] @ C[:n].T + qr[s] @ KR[:n].T) * sc          # [H, n]
-        a = np.exp(x - x.max(axis=1, keepdims=True))
-        a /= a.sum(axis=1, keepdims=True)
-        z = a @ C[:n]                                                # [H, 512]
-        var = ((u * q_lat[s] * z) ** 2).sum(axis=1)                  # q~ roundings
-        per_score = ((u * q_lat[s]) ** 2) @ (C[:n] ** 2).T           # [H, n]
-        if case.rope:
-            zr = a @ KR[:n]
-            var += ((u * qr[s] * zr) ** 2).sum(axis=1)               # q^R roundings
-            var += (((a ** 2) @ (KR[:n] ** 2)) * (u * qr[s]) ** 2).sum(axis=1)   # k^R roundings
-            per_score += 2.0 * ((u * qr[s]) ** 2) @ (KR[:n] ** 2).T
-        first = k * sc * np.sqrt(var)
-        second = 0.5 * (k * sc) ** 2 * per_score.max(axis=1)
-        tol[s] = LSE_ABS_TOL + first + second
+        tol[s] = rounding_lse_tol(q_lat[s], qr[s], C[:n], KR[:n], case.scale, case.rope)
     return tol
+
+
+def rounding_lse_tol(q_lat, q_rope, C, KR, scale, rope=False) -> np.ndarray:
+    """LSE_ABS_TOL plus the bound of lse_tolerance for one query token (q_lat [H,512],
+    q_rope [H,64]) over the rows C [n,512], KR [n,64] it reads: the q~ roundings (and,
+    with RoPE, those of q^R and k^R) of the CUDA path, by Hoeffding's inequality, plus the
+    second-order remainder.  Returns [H]."""
+    u, k, sc = U_BF16, K_HOEFFDING, scale
+    x = (q_lat @ C.T + q_rope @ KR.T) * sc                       # [H, n]
+    a = np.exp(x - x.max(axis=1, keepdims=True))
+    a /= a.sum(axis=1, keepdims=True)
+    z = a @ C                                                    # [H, 512]
+    var = ((u * q_lat * z) ** 2).sum(axis=1)                     # q~ roundings
+    per_score = ((u * q_lat) ** 2) @ (C ** 2).T                  # [H, n]
+    if rope:
+        zr = a @ KR
+        var += ((u * q_rope * zr) ** 2).sum(axis=1)              # q^R roundings
+        var += (((a ** 2) @ (KR ** 2)) * (u * q_rope) ** 2).sum(axis=1)   # k^R roundings
+        per_score += 2.0 * ((u * q_rope) ** 2) @ (KR ** 2).T
+    first = k * sc * np.sqrt(var)
+    second = 0.5 * (k * sc) ** 2 * per_score.max(axis=1)
+    return LSE_ABS_TOL + first + second
 
 
 def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:

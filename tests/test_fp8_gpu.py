@@ -14,7 +14,7 @@ import torch
 
 import oracle as O
 from mla_latent_kv_70_b300 import inputs as I
-from tests.mla_cases import LSE_ABS_TOL, ROW_REL_TOL, log_lse, lse_err, row_rel_err
+from tests.mla_cases import LSE_ABS_TOL, ROW_REL_TOL, check_lse, log_lse, lse_err, rounding_lse_tol, row_rel_err
 
 P = 4096  # a fake 16-byte aligned address: a call rejected on the host never dereferences it
 
@@ -223,3 +223,92 @@ def test_decode_fp8_timeout_is_flagged_and_device_recovers(lib, splits):
     assert torch.all(o_lat == 0) and torch.all(torch.isneginf(lse))
     o_lat, lse = fc.run(splits)
     check_fp8(case, o_lat, lse, range(case.B), f"fp8_recovery/{splits}")
+
+
+# ----------------------------------------------------------------------------
+# Append into the FP8 cache
+# ----------------------------------------------------------------------------
+
+def test_append_fp8_rejects_on_the_host(lib):
+    f = lib.mla_append_latent_fp8
+    ok = dict(rows=P, B=2, S=1, theta=1e4, seqlens=P, kv8=P, sc=P, stride=64, bt=None, max_pages=0,
+              page_size=64, num_pages=0, status=None, stream=None)
+    call = lambda **o: f(*{**ok, **o}.values())
+    assert call(rows=None) == 1 and call(kv8=None) == 1 and call(sc=None) == 1
+    assert call(S=5) == 1 and call(theta=-1.0) == 1 and call(kv8=P + 8) == 1 and call(sc=P + 2) == 1
+    assert call(bt=P, max_pages=2, num_pages=4, page_size=32) == 2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("paged", [False, True])
+@pytest.mark.parametrize("S,theta", [(1, 10000.0), (3, 0.0)])
+def test_append_fp8_places_quantized_rows(lib, paged, S, theta):
+    import mla_latent_kv_70_b300 as mla
+    lens = [5, 0, 100, 63]
+    case = I.make_case("append8", len(lens), S, 16, [T + S for T in lens], paged=paged, seed=81, t_cap=128)
+    kv8, sc = I.fp8_cache(case, device="cuda")
+    before8, before_sc = kv8.cpu(), sc.cpu()
+    new = torch.stack([I.randn_bf16((S, I.ROW), case.seed, "new8", b) for b in range(case.B)])
+    new[0, 0, :I.D_C] = 0.0                         # an all-zero latent row: scale 1
+    seqlens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt = case.block_table.cuda() if paged else None
+    mla.mla_append_latent_fp8(new.cuda(), seqlens, kv8, sc, rope_theta=theta, block_table=bt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert seqlens.cpu().tolist() == [T + S for T in lens]
+    after8, after_sc = kv8.cpu(), sc.cpu()
+    written = torch.zeros(after8.shape[:-1], dtype=torch.bool)
+    for b, T in enumerate(lens):
+        rows = new[b].double().numpy()
+        codes, _, scales = O.quantize_fp8_rows(rows)
+        ref, pos = O.append_latent_rows(rows, T, theta or None)
+        for s, t in enumerate(pos):
+            t = int(t)
+            if paged:
+                page = int(case.block_table[b, t // 64])
+                got8, got_sc = after8[page, t % 64], after_sc[page, t % 64]
+                written[page, t % 64] = True
+            else:
+                got8, got_sc = after8[b, t], after_sc[b, t]
+                written[b, t] = True
+            np.testing.assert_array_equal(got8[:I.D_C].numpy(), codes[s])          # codes: byte for byte
+            assert float(got_sc) == scales[s]
+            kr = got8[I.D_C:].contiguous().view(torch.bfloat16).double().numpy()
+            np.testing.assert_allclose(kr, ref[s, I.D_C:], rtol=2 ** -7, atol=2 ** -7)   # k^R rotated, bf16
+    assert torch.equal(after8[~written], before8[~written])
+    assert torch.equal(after_sc[~written], before_sc[~written])
+
+
+@pytest.mark.gpu
+def test_fp8_step_that_appends_matches_the_oracle(lib):
+    # A DecodeStep over the FP8 cache that appends its token's row first: the decode then
+    # reads the quantized new row at its position.
+    import mla_latent_kv_70_b300 as mla
+    lens = [63, 200, 1]
+    case = I.make_case("fp8_step", 3, 1, 32, [T + 1 for T in lens], seed=83, t_cap=256)
+    kv8, sc = I.fp8_cache(case, device="cuda")
+    new = torch.stack([I.randn_bf16((1, I.ROW), case.seed, "new8s", b) for b in range(case.B)])
+    qn, qr = I.queries(case)
+    w_uk, w_uv = I.weights(case)
+    seqlens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    step = mla.DecodeStep(case.B, 1, case.H, w_uk.cuda(), w_uv.cuda(), max_seqlen=max(lens) + 1, num_splits=2)
+    step(qn.cuda(), qr.cuda(), kv8, seqlens, new_rows=new.cuda(), kv_scale=sc)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    o_lat, lse = step.o_lat.cpu().numpy(), step.lse.cpu().numpy()
+    wk = w_uk.double().numpy()
+    for b, T in enumerate(lens):
+        rows, s_ = I.seq_fp8_rows(case, b)
+        kr = rows[:T, I.D_C:].contiguous().view(torch.bfloat16).double().numpy()
+        cache = O.dequantize_fp8_rows(rows[:T, :I.D_C].numpy(), kr, s_[:T].double().numpy())
+        codes, nkr, nsc = O.quantize_fp8_rows(new[b].double().numpy())
+        cache = np.concatenate([cache, O.dequantize_fp8_rows(codes, nkr, nsc)])
+        q_lat = O.absorb_q(qn[b].double().numpy(), wk)
+        r_lat, r_lse = O.decode_absorbed_seq(q_lat, qr[b].double().numpy(), cache[:, :I.D_C], cache[:, I.D_C:],
+                                             case.scale)
+        assert row_rel_err(o_lat[b], r_lat) <= ROW_REL_TOL, b
+        # q~ is stored in bf16 on the GPU and exact in the oracle: the derived bound of the
+        # absorb -> decode path (every sequence here reads fewer than 256 rows)
+        tol = rounding_lse_tol(q_lat[0], qr[b].double().numpy()[0], cache[:, :I.D_C], cache[:, I.D_C:], case.scale)
+        check_lse(lse[b][0], r_lse[0], tol, key="fp8_step", where=b)
