@@ -19,6 +19,13 @@
  *                      the projections multiplied together ahead of time, and the two
  *                      decode-time products that use them
  *   mla_prefill        prefill / chunked prefill in the expanded order (per-head K, V built)
+ *   mla_quantize_fp8, mla_append_latent_fp8, mla_decode_latent_fp8
+ *                      the FP8 (E4M3, a power-of-two scale per row) form of the latent
+ *                      cache: quantize rows, append a step's rows, decode over it
+ *   mla_decode_num_splits, mla_decode_plan_splits
+ *                      split counts for the decode (from max_seqlen, or from the
+ *                      batch's host-side lengths)
+ *   mla_copy_from_host the host-to-device leg of a serving loop, by SM loads
  *
  * Conventions shared by every call
  *   - Dimensions are fixed: d_c = 512 (latent), d_r = 64 (decoupled RoPE key),
