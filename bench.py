@@ -502,7 +502,7 @@ def run_extra(args):
                 marks(1)
         flops = prefill_flops(B, S, T, H)
         alg_bytes = B * T * 1152 + B * S * H * (192 * 2 + 128 * 4 + 4) + 2 * H * 512 * 128 * 2
-        kernel = "mla_prefill (K_h, V_h expansion GEMMs + causal attention)"
+        kernel = "mla_prefill (K_h, V_h expansion + causal attention)"
     elif name == "dsv3_fp8":
         kv8 = torch.empty(case.B, case.t_cap, I.FP8_ROW, dtype=torch.uint8, device=dev)
         kv_sc = torch.empty(case.B, case.t_cap, device=dev)
@@ -635,7 +635,7 @@ def run_extra(args):
             "clocks": clock_info,
             "e2e": {"value": whole_job_rate(world, tokens, e2e_ms / args.steps), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * (3 if name in ("prefill_4k", "dsv3_fp8") else 6),
+            "gpu_launches": args.steps * {"prefill_4k": 2, "dsv3_fp8": 3}.get(name, 6),
             "roofline": roof}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_extra(name, case)

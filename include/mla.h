@@ -405,7 +405,8 @@ mla_status mla_out_proj_fused(const float* o_lat, const mla_bf16* w_uvo, int B, 
  *   first T_kv rows per sequence are read (k^R already rotated); w_uk, w_uv [H,512,128];
  *   o fp32 [B,T_q,H,128]; lse fp32 [B,T_q,H]; 1 <= T_q <= T_kv <= kv_seq_stride.
  *   workspace: mla_prefill_workspace_bytes(B, kv_seq_stride, H) bytes, which hold K_h and
- *   V_h of every cache row of the B sequences.
+ *   V_h of every cache row of the B sequences (bf16 [B * kv_seq_stride][H][128], K_h first;
+ *   rows past T_kv hold whatever their cache rows give and are never read).
  */
 size_t mla_prefill_workspace_bytes(int B, int64_t kv_seq_stride, int H);
 mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla_bf16* kv, int64_t kv_seq_stride,

@@ -438,20 +438,13 @@ mla_status mla_prefill(const mla_bf16* q_nope, const mla_bf16* q_rope, const mla
   const uint64_t rows = (uint64_t)B * (uint64_t)kv_seq_stride;
   __nv_bfloat16* k_exp = static_cast<__nv_bfloat16*>(workspace);
   __nv_bfloat16* v_exp = k_exp + rows * (uint64_t)H * mla::kDn;
-  // K_h[t] = c_t W_UK[h], V_h[t] = c_t W_UV[h]: m = output column (128), n = cache row t,
-  // k = latent column (512); the weights are read MN-major, the cache rows K-major.
-  for (int which = 0; which < 2; ++which) {
-    const mla::GemmOperand a{which ? w_uv : w_uk, (uint64_t)H * kDc, (uint64_t)mla::kDn, (uint64_t)mla::kDn, 1};
-    const mla::GemmOperand b{kv, rows, (uint64_t)kRow, (uint64_t)kRow, 0};
-    mla::GemmShape g{};
-    // Eight k blocks per tile: two stages are enough, and let two CTAs share an SM.
-    g.M = mla::kDn, g.N = (int)rows, g.K = kDc, g.batches = H, g.n_tile = 256, g.k_splits = 1, g.stages = 2;
-    g.a_batch_rows = kDc, g.b_batch_rows = 0;
-    g.c = which ? v_exp : k_exp, g.out_bf16 = 1, g.ldc_m = 1, g.ldc_n = (int64_t)H * mla::kDn, g.ldc_batch = mla::kDn;
-    g.status = status_dev;
-    const mla_status r = launch_status(mla::launch_gemm(a, b, g, st));
-    if (r != MLA_OK) return r;
-  }
+  // K_h[t] = c_t W_UK[h], V_h[t] = c_t W_UV[h] for every row of the cache (rows past T_kv
+  // included; the attention never reads them).
+  const mla_status r = launch_status(mla::launch_expand_kv(reinterpret_cast<const __nv_bfloat16*>(kv), rows,
+                                                           reinterpret_cast<const __nv_bfloat16*>(w_uk),
+                                                           reinterpret_cast<const __nv_bfloat16*>(w_uv), H,
+                                                           k_exp, v_exp, status_dev, st));
+  if (r != MLA_OK) return r;
   return launch_status(mla::launch_prefill_attn(
       reinterpret_cast<const __nv_bfloat16*>(q_nope), reinterpret_cast<const __nv_bfloat16*>(q_rope),
       reinterpret_cast<const __nv_bfloat16*>(kv), kv_seq_stride, k_exp, v_exp, B, T_q, T_kv, H, scale, o, lse,

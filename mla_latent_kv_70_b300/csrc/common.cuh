@@ -126,6 +126,11 @@ __device__ __forceinline__ void split_range(const DecodeParams& p, int T, int s,
 bool encode_tma_2d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t inner,
                    uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                    uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// A 3D map over [outer][rows][inner] (bf16 or fp32): strides in bytes of a row and of an
+// outer slice, boxes of box_inner x box_rows x 1.  Boxes clip at the end of each slice.
+bool encode_tma_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t outer, uint64_t row_stride_bytes, uint64_t outer_stride_bytes,
+                   uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 // The same over bytes (uint8 elements).
 bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -25,6 +25,11 @@ struct GemmShape {
   int32_t* status;                  // device flag word or null
 };
 cudaError_t launch_gemm(const GemmOperand& a, const GemmOperand& b, GemmShape g, cudaStream_t st);
+// K_h = C W_UK[h] and V_h = C W_UV[h] for every cache row and head, bf16 [rows][H][128]
+// (expand_sm103.cu).
+cudaError_t launch_expand_kv(const __nv_bfloat16* kv, uint64_t rows, const __nv_bfloat16* w_uk,
+                             const __nv_bfloat16* w_uv, int H, __nv_bfloat16* k_exp, __nv_bfloat16* v_exp,
+                             int32_t* status, cudaStream_t st);
 cudaError_t launch_f32_to_bf16(const float* x, int64_t n, __nv_bfloat16* y, cudaStream_t st);
 cudaError_t launch_copy_from_host(const void* src_dev_alias, void* dst, int64_t bytes, cudaStream_t st);
 cudaError_t launch_rope_slice(const __nv_bfloat16* q_rope, const int32_t* q_pos, const RopeFreqs& f, int M,

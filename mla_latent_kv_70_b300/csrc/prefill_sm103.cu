@@ -54,7 +54,12 @@ constexpr uint32_t kPOffRed = kPOffQR + kPBox;   // [2 halves][128 rows] fp32
 constexpr uint32_t kPOffBars = kPOffRed + 2 * 128 * 4;
 constexpr uint32_t kPSmem = kPOffBars + 192 + 1024;
 static_assert(kPSmem <= 232448, "shared memory per CTA");
+constexpr uint32_t kPOffQn = kPOffV + kPVBytes;   // q_nope staged in value stage 1
+constexpr uint32_t kPOffOst = kPOffK;             // O staged (4 boxes of 32 fp32 x 128) in the key ring
+constexpr uint32_t kPOBox = 128 * 128;            // 128 rows x 32 fp32 (128B swizzle)
+constexpr uint32_t kPEpiBar = 5;                  // named barrier of the 256 softmax threads
 static_assert(kPOffV % 1024 == 0 && kPOffQR % 1024 == 0, "128B-swizzled tiles");
+static_assert(4 * kPOBox <= kPKStages * kPKBytes, "O staging fits the key ring");
 
 // TMEM columns.
 constexpr uint32_t kPTmemO = 0;      // [0,128)   O, fp32
@@ -64,8 +69,8 @@ constexpr uint32_t kPTmemP = 448;    // [448,512) P, bf16 pairs
 constexpr float kPRescale = 8.0f;
 
 enum PBar {
-  kPQFullB = 0,                         // q^R landed
-  kPQReadyB,                            // q_nope in TMEM (256 threads)
+  kPQFullB = 0,                         // q^R and q_nope landed
+  kPQReadyB,                            // q_nope in TMEM (256 threads), its staging read
   kPKFullB,                             // [3] key tile landed
   kPKEmptyB = kPKFullB + kPKStages,     // [3] score products of the stage done
   kPVFullB = kPKEmptyB + kPKStages,     // [2] value tile landed
@@ -81,6 +86,8 @@ static_assert(kPNumBars * 8 + 16 <= 192, "barrier area");
 
 struct PrefillMaps {
   CUtensorMap q_rope;   // [B*T_q, H*64], box 64 x 128
+  CUtensorMap q_nope;   // [B*T_q, H*128], box 64 x 128
+  CUtensorMap o;        // fp32 [B][T_q][H*128], box 32 x 128 x 1 (rows past T_q clipped)
   CUtensorMap k_exp;    // [rows, H*128], box 64 x 128
   CUtensorMap k_rope;   // cache rows [rows, 576], box 64 x 128 (columns 512..575)
   CUtensorMap v_exp;    // [rows, H*128], box 64 x 128
@@ -90,7 +97,6 @@ struct PrefillParams {
   int B, T_q, T_kv, H;
   int64_t kv_seq_stride;
   float scale_log2;
-  const __nv_bfloat16* q_nope;   // [B, T_q, H, 128]
   float* o;      // [B, T_q, H, 128]
   float* lse;    // [B, T_q, H]
   int32_t* status;
@@ -158,11 +164,17 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     // waiting for an aggregation.
     if (lane == 0) {
       prefetch_tmap(&maps.q_rope);
+      prefetch_tmap(&maps.q_nope);
       prefetch_tmap(&maps.k_exp);
       prefetch_tmap(&maps.k_rope);
       prefetch_tmap(&maps.v_exp);
-      mbar_arrive_expect_tx(bar(kPQFullB), kPBox);
+      prefetch_tmap(&maps.o);
+      // q_nope is staged in value stage 1 (two boxes) until the softmax warps move it
+      // into TMEM.
+      mbar_arrive_expect_tx(bar(kPQFullB), 3 * kPBox);
       tma_load_2d(s0 + kPOffQR, &maps.q_rope, bar(kPQFullB), h * 64, b * p.T_q + q0);
+      tma_load_2d(s0 + kPOffQn, &maps.q_nope, bar(kPQFullB), h * 128, b * p.T_q + q0);
+      tma_load_2d(s0 + kPOffQn + kPBox, &maps.q_nope, bar(kPQFullB), h * 128 + 64, b * p.T_q + q0);
       int k_issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int ks = j % kPKStages;
@@ -191,8 +203,9 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       int v_issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int vs = j % kPVStages;
-        if (j >= kPVStages &&
-            !mbar_wait(bar(kPVEmptyB + vs), (uint32_t)(j / kPVStages - 1) & 1u, kDefaultWaitNs)) {
+        if ((j >= kPVStages &&
+             !mbar_wait(bar(kPVEmptyB + vs), (uint32_t)(j / kPVStages - 1) & 1u, kDefaultWaitNs)) ||
+            (j == 1 && !mbar_wait(bar(kPQReadyB), 0, kDefaultWaitNs))) {   // stage 1 holds q_nope
           aborted = true;
           break;
         }
@@ -268,13 +281,18 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     const bool row_ok = qi < p.T_q;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const uint32_t pair_bar = 1u + (uint32_t)quarter;   // the two warps of this lane quarter
-    // This thread's half of q_nope (64 dims) into TMEM: the A operand of the score MMAs.
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_nope + (((int64_t)b * p.T_q + qi) * p.H + h) * kDn + 64 * hf);
+    // The two threads of a row meet at named barriers, so they leave the loop together:
+    // a failed wait is carried to the next meeting, where the pair agrees to give up.
+    float m_ref = -INFINITY, l = 0.f;
+    bool failed = false;   // a wait of this thread gave up since the last meeting
+    // This thread's half of q_nope (64 dims, box hf of the staged tile: row r, 16-byte
+    // chunk c at c ^ (r & 7)) into TMEM: the A operand of the score MMAs.
+    if (pwarp_wait(bar(kPQFullB), 0)) {
+      const uint32_t src = s0 + kPOffQn + (uint32_t)hf * kPBox + (uint32_t)r * 128u;
       uint32_t v[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 w = row_ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 w = ld_shared_u4(src + (uint32_t)((c ^ (r & 7)) * 16));
         v[4 * c] = w.x;
         v[4 * c + 1] = w.y;
         v[4 * c + 2] = w.z;
@@ -282,13 +300,11 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       }
       tmem_st32(tb + lane_off + kPTmemQ + 32u * (uint32_t)hf, v);
       tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kPQReadyB));
+    } else {
+      failed = true;
     }
-    // The two threads of a row meet at named barriers, so they leave the loop together:
-    // a failed wait is carried to the next meeting, where the pair agrees to give up.
-    float m_ref = -INFINITY, l = 0.f;
-    bool failed = false;   // a wait of this thread gave up since the last meeting
+    tc_fence_before();
+    mbar_arrive(bar(kPQReadyB));
     for (int j = 0; j < nt; ++j) {
       float x[64];
       if (pwarp_wait(bar(kPSFullB + (j & 1)), (uint32_t)(j >> 1) & 1u)) {
@@ -391,21 +407,49 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     const float l_row = l + red[(hf ^ 1) * 128 + r];
     const bool have = !aborted && l_row > 0.f;
     const float inv = have ? 1.f / l_row : 0.f;
-    float* out = p.o + (((int64_t)b * p.T_q + qi) * p.H + h) * 128 + 64 * hf;
+    // With every row done, the key ring is idle (each key tile landed and its score
+    // products finished before PV(nt-1) did): O is staged there, this thread's half of
+    // row r in boxes 2 hf and 2 hf + 1 (16-byte chunk c of the row at c ^ (r & 7)), and
+    // stored by TMA.  If any row gave up, O is written directly (zeros for those rows).
+    if (named_bar_and(kPEpiBar, 32 * kPSoftWarps, !aborted)) {
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      uint32_t o[32];
-      if (!aborted && nt > 0) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
         tmem_ld32(tb + lane_off + kPTmemO + 64u * (uint32_t)hf + 32u * c, o);
         tmem_ld_wait();
-      }
-      if (row_ok) {
+        const uint32_t dst = s0 + kPOffOst + (uint32_t)(2 * hf + c) * kPOBox + (uint32_t)r * 128u;
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-          reinterpret_cast<float4*>(out + 32 * c)[v] =
-              have ? make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          st_shared_u4(dst + (uint32_t)((v ^ (r & 7)) * 16), __float_as_uint(__uint_as_float(o[4 * v]) * inv),
+                       __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
+                       __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
+                       __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kPEpiBar, 32 * kPSoftWarps);
+      if (tid == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_store_3d(&maps.o, h * 128 + 32 * c, q0, b, s0 + kPOffOst + (uint32_t)c * kPOBox);
+        bulk_commit_group();
+        bulk_wait_group_read0();   // the staging must outlive its reads
+      }
+    } else {
+      float* out = p.o + (((int64_t)b * p.T_q + qi) * p.H + h) * 128 + 64 * hf;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        if (!aborted) {
+          tmem_ld32(tb + lane_off + kPTmemO + 64u * (uint32_t)hf + 32u * c, o);
+          tmem_ld_wait();
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(out + 32 * c)[v] =
+                have ? make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     if (row_ok && hf == 0)
@@ -431,6 +475,10 @@ cudaError_t launch_prefill_attn(const __nv_bfloat16* q_nope, const __nv_bfloat16
   const uint64_t qrows = (uint64_t)B * T_q, krows = (uint64_t)B * kv_seq_stride;
   if (!encode_tma_2d(&maps.q_rope, true, q_rope, (uint64_t)H * kDr, qrows, (uint64_t)H * kDr * 2, 64, kPQ,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tma_2d(&maps.q_nope, true, q_nope, (uint64_t)H * kDn, qrows, (uint64_t)H * kDn * 2, 64, kPQ,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tma_3d(&maps.o, false, o, (uint64_t)H * kDv, (uint64_t)T_q, (uint64_t)B, (uint64_t)H * kDv * 4,
+                     (uint64_t)T_q * H * kDv * 4, 32, kPQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tma_2d(&maps.k_exp, true, k_exp, (uint64_t)H * kDn, krows, (uint64_t)H * kDn * 2, 64, kPKeys,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tma_2d(&maps.k_rope, true, kv, kRow, krows, (uint64_t)kRow * 2, 64, kPKeys,
@@ -438,7 +486,7 @@ cudaError_t launch_prefill_attn(const __nv_bfloat16* q_nope, const __nv_bfloat16
       !encode_tma_2d(&maps.v_exp, true, v_exp, (uint64_t)H * kDv, krows, (uint64_t)H * kDv * 2, 64, kPKeys,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  PrefillParams p{B, T_q, T_kv, H, kv_seq_stride, scale * kLog2e, q_nope, o, lse, status};
+  PrefillParams p{B, T_q, T_kv, H, kv_seq_stride, scale * kLog2e, o, lse, status};
   static SmemOptIn opt_in;
   cudaError_t e = ensure_dynamic_smem((const void*)k_prefill_attn, (int)kPSmem, opt_in);
   if (e != cudaSuccess) return e;

@@ -48,6 +48,21 @@ bool encode_tma_2d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t in
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tma_3d(CUtensorMap* map, bool is_bf16, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t outer, uint64_t row_stride_bytes, uint64_t outer_stride_bytes,
+                   uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_stride_bytes, (cuuint64_t)outer_stride_bytes};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                       CUtensorMapSwizzle swizzle) {

@@ -59,14 +59,18 @@ def test_prefill_matches_oracle(B, T_q, T_kv, H):
     kv[:, T_kv:] = float("nan")                 # rows past the sequence must never be used
     qn, qr = I.queries(case)
     w_uk, w_uv = I.weights(case)
-    o = torch.empty(B, T_q, H, 128, device="cuda")
-    lse = torch.empty(B, T_q, H, device="cuda")
+    # One batch more than asked for, holding a sentinel: the tiles of the last query block
+    # must not be written past row T_q of the last sequence.
+    o_all = torch.full((B + 1, T_q, H, 128), 7.0, device="cuda")
+    lse_all = torch.full((B + 1, T_q, H), 7.0, device="cuda")
+    o, lse = o_all[:B], lse_all[:B]
     ws = torch.empty(mla.mla_prefill_workspace_bytes(B, case.t_cap, H), dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mla.mla_prefill(qn.cuda(), qr.cuda(), kv, T_kv, w_uk.cuda(), w_uv.cuda(), o, lse, scale=case.scale,
                     workspace=ws, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    assert bool((o_all[B] == 7.0).all()) and bool((lse_all[B] == 7.0).all())
     heads = list(range(H)) if H <= 32 else [0, 61, 127]
     wk, wv = w_uk.double().numpy(), w_uv.double().numpy()
     for b in range(B):
@@ -78,3 +82,37 @@ def test_prefill_matches_oracle(B, T_q, T_kv, H):
         assert row_rel_err(o[b][:, heads].cpu().numpy(), r_o) <= ROW_REL_TOL, b
         tol = prefill_lse_tolerance(q_n, q_r, C, KR, wk, case.scale, heads)
         check_lse(lse[b][:, heads].cpu().numpy(), r_lse, tol, where=b)
+
+
+@pytest.mark.parametrize("B,T,H", [(2, 300, 16), (1, 1000, 128), (3, 129, 32)])
+def test_prefill_expansion_matches_definition(B, T, H):
+    """The K_h and V_h that mla_prefill leaves in its workspace (bf16 [B * kv_seq_stride][H][128],
+    K_h then V_h) against K_h[t] = c_t W_UK[h], V_h[t] = c_t W_UV[h] in fp64: the result of an
+    fp32 sum rounded once to bf16 (unit roundoff u = 2^-8), so |gpu - exact| <= u |exact| +
+    (fp32 sum error), the latter bounded by 2^-14 sum_k |c_k w_k| (twice the worst case of 512
+    fp32 roundings)."""
+    import mla_latent_kv_70_b300 as mla
+    case = I.make_case("prefill", B, T, H, [T] * B, causal=True, seed=93, t_cap=T + 40)
+    kv = I.cache(case, device="cuda")
+    kv[:, T:] = float("nan")
+    qn, qr = I.queries(case)
+    w_uk, w_uv = I.weights(case)
+    o = torch.empty(B, T, H, 128, device="cuda")
+    lse = torch.empty(B, T, H, device="cuda")
+    ws = torch.empty(mla.mla_prefill_workspace_bytes(B, case.t_cap, H), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_prefill(qn.cuda(), qr.cuda(), kv, T, w_uk.cuda(), w_uv.cuda(), o, lse, scale=case.scale,
+                    workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    exp = ws.view(torch.bfloat16).view(2, B, case.t_cap, H, 128).float().cpu().numpy()
+    heads = list(range(H)) if H <= 32 else [0, 1, 63, 64, 126, 127]
+    for which, w in enumerate((w_uk, w_uv)):
+        wd = w.double().numpy()
+        for b in range(B):
+            C = I.seq_rows(case, b)[:T, :512].double().numpy()
+            for h in heads:
+                e = C @ wd[h]
+                bound = U_BF16 * np.abs(e) + 2.0 ** -14 * (np.abs(C) @ np.abs(wd[h]))
+                err = np.abs(exp[which, b, :T, h] - e)
+                assert (err <= bound).all(), (which, b, h, float(err.max()), float((err / bound).max()))
