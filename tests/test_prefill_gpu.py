@@ -46,12 +46,15 @@ def prefill_lse_tolerance(qn, qr, C, KR, w_uk, scale, heads):
     return tol
 
 
-# Query tiles of 128 rows go two to a CTA: 300 leaves a second CTA whose upper tile holds no
-# query; 200/200 ends the sequence inside a key tile that only the upper tile reads (it
-# clears the rows past the end); 512/600 fills both tiles of two CTAs with the key tiles
-# offset from the query tiles (chunked prefill).
+# Query blocks of 128 rows: 300 leaves a last block of 44 queries (its other rows are never
+# written); 200/200 ends the sequence inside a key tile (the rows past the end are cleared
+# in the value tile); 512/600 and 600/900 are chunked prefill (the queries are the last T_q
+# positions).  Blocks i and n-1-i of a head form one unit of the persistent schedule:
+# 1024 with 128 heads and 600/900 with two sequences of 64 heads give each CTA several
+# units, and the five blocks of 600 leave the middle one without a partner.
 @pytest.mark.parametrize("B,T_q,T_kv,H", [(2, 300, 300, 16), (1, 130, 700, 16), (1, 64, 64, 32),
-                                          (1, 200, 1000, 128), (1, 200, 200, 16), (1, 512, 600, 16)])
+                                          (1, 200, 1000, 128), (1, 200, 200, 16), (1, 512, 600, 16),
+                                          (1, 1024, 1024, 128), (2, 600, 900, 64)])
 def test_prefill_matches_oracle(B, T_q, T_kv, H):
     import mla_latent_kv_70_b300 as mla
     case = I.make_case("prefill", B, T_q, H, [T_kv] * B, causal=True, seed=91, t_cap=T_kv + 40)
@@ -71,7 +74,7 @@ def test_prefill_matches_oracle(B, T_q, T_kv, H):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert bool((o_all[B] == 7.0).all()) and bool((lse_all[B] == 7.0).all())
-    heads = list(range(H)) if H <= 32 else [0, 61, 127]
+    heads = list(range(H)) if H <= 32 else [0, H // 2 - 3, H - 1]
     wk, wv = w_uk.double().numpy(), w_uv.double().numpy()
     for b in range(B):
         rows = I.seq_rows(case, b)[:T_kv].double().numpy()
