@@ -82,6 +82,8 @@ enum PBar {
   kPQReadyB,                            // q_nope of item n in TMEM (256 threads)
   kPQrFreeB,                            // score products of item n done: q^R and q_nope free
   kPQnFullB,                            // q_nope of item n landed in the O slots
+  kPOStagedB,                           // O of item n staged (256 threads)
+  kPOReadB,                             // O of item n stored: its slots and value stage read
   kPKFullB,                             // [2] key tile landed
   kPKEmptyB = kPKFullB + kPKStages,     // [2] score products of the stage done
   kPVFullB = kPKEmptyB + kPKStages,     // [2] value tile landed
@@ -168,6 +170,8 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     mbar_init(bar(kPQReadyB), 32 * kPSoftWarps);
     mbar_init(bar(kPQrFreeB), 1);
     mbar_init(bar(kPQnFullB), 1);
+    mbar_init(bar(kPOStagedB), 32 * kPSoftWarps);
+    mbar_init(bar(kPOReadB), 1);
     for (int i = 0; i < kPKStages; ++i) {
       mbar_init(bar(kPKFullB + i), 1);
       mbar_init(bar(kPKEmptyB + i), 1);
@@ -257,13 +261,36 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       if (n > 0) mbar_wait(bar(kPQFullB), (uint32_t)(n - 1) & 1u, kDefaultWaitNs);
     }
   } else if (warp == kPVWarp) {
-    // ---------------- TMA producer: the value tiles ----------------
-    // Value tile g into V stage g % 2, free once PV(g-2) is done.
+    // ---------------- TMA producer: the value tiles, and O out ----------------
+    // Value tile g into V stage g % 2, free once PV(g-2) is done.  The softmax warps stage
+    // an item's O in four 32-column boxes: columns 64 hf + [0, 32) in slot hf, columns
+    // 64 hf + [32, 64) in half hf of the value stage of the item's last tile.  This thread
+    // stores them by TMA before that stage is loaded again (or at the end), waits until
+    // the boxes are read, and says so (the slots then take the next q_nope).
     if (lane == 0) {
       int u = blockIdx.x;
       int k = 0;
       uint32_t g = 0;
       PItem it;
+      PItem pend_it[4];          // items whose O is staged or about to be, in order
+      uint32_t pend_last[4];     // the last tile of each
+      int pend_head = 0, pend_n = 0, stored = 0;
+      auto store_o = [&]() {
+        const PItem t = pend_it[pend_head];
+        const uint32_t vst = s0 + kPOffV + (pend_last[pend_head] % kPVStages) * kPVBytes;
+        pend_head = (pend_head + 1) & 3;
+        --pend_n;
+        if (!mbar_wait(bar(kPOStagedB), (uint32_t)stored & 1u, kDefaultWaitNs)) return false;
+        tma_store_3d(&maps.o, t.h * 128, t.q0, t.b, s0 + kPOffOst);
+        tma_store_3d(&maps.o, t.h * 128 + 32, t.q0, t.b, vst);
+        tma_store_3d(&maps.o, t.h * 128 + 64, t.q0, t.b, s0 + kPOffOst + kPOBox);
+        tma_store_3d(&maps.o, t.h * 128 + 96, t.q0, t.b, vst + kPOBox);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar(kPOReadB));
+        ++stored;
+        return true;
+      };
       while (!aborted && pnext(p, u, k, it)) {
         const int64_t krow0 = (int64_t)it.b * p.kv_seq_stride;
         for (int j = 0; j < it.nt; ++j, ++g) {
@@ -273,13 +300,24 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
             aborted = true;
             break;
           }
+          if (pend_n > 0 && pend_last[pend_head] + kPVStages == g && !store_o()) {   // the stage holds O
+            aborted = true;
+            break;
+          }
           const int y = (int)(krow0 + (int64_t)j * kPKeys);
           const uint32_t vst = s0 + kPOffV + vs * kPVBytes;
           mbar_arrive_expect_tx(bar(kPVFullB + vs), kPVBytes);
           tma_load_2d(vst, &maps.v_exp, bar(kPVFullB + vs), it.h * 128, y);
           tma_load_2d(vst + kPBox, &maps.v_exp, bar(kPVFullB + vs), it.h * 128 + 64, y);
         }
+        if (aborted) break;
+        pend_it[(pend_head + pend_n) & 3] = it;
+        pend_last[(pend_head + pend_n) & 3] = g - 1;
+        ++pend_n;
       }
+      while (!aborted && pend_n > 0)
+        if (!store_o()) aborted = true;
+      bulk_wait_group0();   // every store complete before exit
       for (uint32_t i = g > (uint32_t)kPVStages ? g - kPVStages : 0u; i < g; ++i)   // no copy may land after exit
         mbar_wait(bar(kPVFullB + i % kPVStages), (i / kPVStages) & 1u, kDefaultWaitNs);
     }
@@ -289,8 +327,8 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     // from TMEM against the two K_h boxes, 4 with q^R from shared memory against k^R),
     // then PV(g-1) once P(g-1) is in TMEM (8 MMAs, A = P from TMEM, B = the value tile
     // read MN-major).  The first PV of an item overwrites O: the softmax warps write its P
-    // only after reading the previous item's O out of TMEM.  The last PV of an item is
-    // issued before the next item's score products, which wait for its q_nope.
+    // only after reading the previous item's O out of TMEM.  The last PV of an item goes
+    // out before the wait for the next item's q^R and q_nope.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, kPKeys, false, false);
       const uint32_t id_o = idesc_bf16(128, 128, false, true);
@@ -315,8 +353,7 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       bool pend = false, pend_first = false;   // PV of tile g-1 still to issue
       PItem it;
       while (!aborted && pnext(p, u, k, it)) {
-        // The last aggregation of the previous item goes first: the softmax warps move
-        // this item's q_nope into TMEM only once it is done.
+        // The last aggregation of the previous item goes first.
         if (pend && !pv(g - 1, pend_first)) {
           aborted = true;
           break;
@@ -423,10 +460,12 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       for (int j = 0; j < it.nt; ++j, ++g) {
         float x[64];
         // A tile before the last (or at the only one), the next item's q_nope is loaded
-        // into the slots, which the previous item's O has left by then.
+        // into the slots, once the previous item's O has left them.
         if (tid == 0 && have_nx && j == max(0, it.nt - 2)) {
-          bulk_wait_group_read0();
-          q_issue(nx);
+          if (n == 0 || mbar_wait(bar(kPOReadB), (uint32_t)(n - 1) & 1u, kDefaultWaitNs))
+            q_issue(nx);
+          else
+            failed = true;
         }
         if (pwarp_wait(bar(kPSFullB + (g & 1)), (g >> 1) & 1u)) {
           tc_fence_after();
@@ -532,34 +571,32 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       const float l_row = l + red[(hf ^ 1) * 128 + r];
       const bool have_l = !aborted && l_row > 0.f;
       const float inv = have_l ? 1.f / l_row : 0.f;
-      // O leaves through the two staging slots by TMA, in two rounds: slot hf takes this
-      // thread's 32 columns 64 hf + 32 c at round c (row r, 16-byte chunk v at v ^ (r & 7)).
-      // The next item's first P (and with it the PV that overwrites O) follows.
+      // O is staged for the value producer to store: this thread's columns 64 hf + 32 c go
+      // to slot hf (c = 0) or to half hf of the value stage of the last tile (c = 1), row r,
+      // 16-byte chunk v at v ^ (r & 7).  The slots were emptied before this item's last
+      // q_nope came in, except after the last item: then the previous item's O must have
+      // left them.  The next item's first P (and with it the PV that overwrites O) follows.
       // If any row gave up, O is written directly (zeros for those rows) and the CTA stops.
+      if (tid == 0 && !have_nx && n > 0 && !mbar_wait(bar(kPOReadB), (uint32_t)(n - 1) & 1u, kDefaultWaitNs))
+        aborted = true;
       const bool all_ok = named_bar_and(kPEpiBar, 32 * kPSoftWarps, !aborted);
       if (all_ok) {
+        const uint32_t vst = s0 + kPOffV + ((g - 1) % kPVStages) * kPVBytes;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
           tmem_ld32(tb + lane_off + kPTmemO + 64u * (uint32_t)hf + 32u * c, o);
           tmem_ld_wait();
-          if (tid == 0) bulk_wait_group_read0();   // the slots' previous contents have left
-          named_bar_sync(kPEpiBar, 32 * kPSoftWarps);
-          const uint32_t dst = s0 + kPOffOst + (uint32_t)hf * kPOBox + (uint32_t)r * 128u;
+          const uint32_t dst = (c == 0 ? s0 + kPOffOst : vst) + (uint32_t)hf * kPOBox + (uint32_t)r * 128u;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             st_shared_u4(dst + (uint32_t)((v ^ (r & 7)) * 16), __float_as_uint(__uint_as_float(o[4 * v]) * inv),
                          __float_as_uint(__uint_as_float(o[4 * v + 1]) * inv),
                          __float_as_uint(__uint_as_float(o[4 * v + 2]) * inv),
                          __float_as_uint(__uint_as_float(o[4 * v + 3]) * inv));
-          fence_proxy_async_smem();
-          named_bar_sync(kPEpiBar, 32 * kPSoftWarps);
-          if (tid == 0) {
-            tma_store_3d(&maps.o, it.h * 128 + 32 * c, it.q0, it.b, s0 + kPOffOst);
-            tma_store_3d(&maps.o, it.h * 128 + 64 + 32 * c, it.q0, it.b, s0 + kPOffOst + kPOBox);
-            bulk_commit_group();
-          }
         }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kPOStagedB));
       } else {
         float* out = p.o + (((int64_t)it.b * p.T_q + qi) * p.H + it.h) * 128 + 64 * hf;
 #pragma unroll 1
@@ -588,7 +625,6 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       have = pnext(p, u, k, it);
       ++n;
     }
-    if (tid == 0) bulk_wait_group0();   // every store complete before exit
   }
 
   if (aborted) raise_flag(p.status, kFlagTimeout);

@@ -2,19 +2,29 @@
 random schedules.
 
 Each CTA of the prefill kernel walks a list of work items (sequence, head, 128 queries)
-and keeps its rings running from one item to the next. Five agents share these buffers
+and keeps its rings running from one item to the next. Four agents share these buffers
 through mbarriers: a key-tile TMA thread (which also loads each item's q^R), a value-tile
-TMA thread, the MMA thread, and the softmax warps. The softmax warps are modelled as one
-agent, since they meet at named barriers for every tile. The buffers are:
+TMA thread (which also stores each item's O), the MMA thread, and the softmax warps. The
+softmax warps are modelled as one agent, since they meet at named barriers for every tile.
+The buffers are:
 - the key ring (2 stages) and the value ring (2 stages);
-- q^R in shared memory, and q_nope, the two score buffers, P and O in TMEM.
+- q^R and two 16 KB slots in shared memory;
+- q_nope, the two score buffers, P and O in TMEM.
 
-Each is reused only after its last reader is done. The checks are:
+The slots carry the next item's q_nope in (loaded by the softmax leader a tile before an
+item's last) and half of an item's O out. The other half goes out through the value stage
+of the item's last tile. The value thread stores O before it loads that stage again.
+
+Each buffer is reused only after its last reader is done. The checks are:
 - the key stage of tile g is reloaded only after the score products of g-2;
 - q^R and q_nope of item n+1 are written only after the last score products of item n;
 - the first aggregation of item n+1 (which overwrites O) starts only after the softmax
   warps have read out O of item n (implied: they write its P after that);
 - P(g) is written only after PV(g-1);
+- the slots take q_nope only after the previous O has been read out of them, and O only
+  after that q_nope has been moved to TMEM;
+- a value stage takes O only after its PV, and the next tile only after O has been read
+  out of it;
 - and so on for the score buffers and the value ring.
 
 Copies complete at random later times. MMA commits complete in issue order, also later.
@@ -99,9 +109,11 @@ class Sim:
         self.sfull = [B(f"SFull{i}", 1) for i in range(2)]
         self.sfree = [B(f"SFree{i}", 8) for i in range(2)]
         self.pfull, self.pvdone = B("PFull", 256), B("PvDone", 1)
+        self.qnfull, self.ostaged, self.oread = B("QnFull", 1), B("OStaged", 256), B("ORead", 1)
         # Buffer state: occupant and whether its readers are done.
         self.kslot = [{"tile": None, "landed": False, "done": True} for _ in range(2)]
-        self.vslot = [{"tile": None, "landed": False, "done": True} for _ in range(2)]
+        self.vslot = [{"tile": None, "landed": False, "done": True, "o": None} for _ in range(2)]
+        self.slots = {"what": None, "landed": True, "read": True}   # ("q", n) or ("o", n)
         self.qrope = {"item": None, "landed": False, "done": True}
         self.qnope = {"item": None, "done": True}
         self.sbuf = [{"tile": None, "ready": False, "read": True} for _ in range(2)]
@@ -159,22 +171,48 @@ class Sim:
                 g += 1
                 yield None
 
-    # ---- the value-tile producer
-    def vprod(self):
-        for g in range(len(self.item_of)):
-            vs = g % 2
-            if g >= 2:
-                yield ("wait", self.vempty[vs], g // 2 - 1)
-            s = self.vslot[vs]
-            check(s["done"], f"value stage {vs} reloaded for tile {g} before PV({s['tile']}) was done")
-            s.update(tile=g, landed=False, done=False)
-            self.vfull[vs].arrive(1, tx=VT)
+    # ---- the value-tile producer, which also stores O
+    def store_o(self, n, last):
+        if "no_ostaged" not in self.faults:
+            yield ("wait", self.ostaged, n)
+        vs = self.vslot[last % 2]
+        check(self.slots["what"] == ("o", n) and vs["o"] == n, f"O of item {n} stored from slots holding "
+                                                               f"{self.slots['what']} and a stage holding {vs['o']}")
+        done = Bar("StoreRead", 1)
 
-            def land(s=s, vs=vs):
-                s["landed"] = True
-                self.vfull[vs].complete_tx(VT)
-            self.later(land)
-            yield None
+        def read():
+            self.slots["read"] = True
+            vs["o"] = None
+            done.arrive()
+        self.later(read)
+        yield ("wait", done, 0)
+        self.oread.arrive()
+
+    def vprod(self):
+        g = 0
+        pend = []
+        for n, nt in enumerate(self.nts):
+            for j in range(nt):
+                vs = g % 2
+                if g >= 2:
+                    yield ("wait", self.vempty[vs], g // 2 - 1)
+                if pend and pend[0][1] + 2 == g:
+                    yield from self.store_o(*pend.pop(0))
+                s = self.vslot[vs]
+                check(s["done"] and s["o"] is None, f"value stage {vs} reloaded for tile {g} before PV({s['tile']}) "
+                                                    f"was done or while it holds O of item {s['o']}")
+                s.update(tile=g, landed=False, done=False)
+                self.vfull[vs].arrive(1, tx=VT)
+
+                def land(s=s, vs=vs):
+                    s["landed"] = True
+                    self.vfull[vs].complete_tx(VT)
+                self.later(land)
+                g += 1
+                yield None
+            pend.append((n, g - 1))
+        while pend:
+            yield from self.store_o(*pend.pop(0))
 
     # ---- the MMA issuer
     def pv(self, gi):
@@ -202,7 +240,7 @@ class Sim:
         pend = None
         g = 0
         for n, nt in enumerate(self.nts):
-            if pend is not None and "pv_after_qready" not in self.faults:
+            if pend is not None:
                 yield from self.pv(pend)
                 pend = None
             yield ("wait", self.qfull, n)
@@ -239,15 +277,38 @@ class Sim:
 
     # ---- the softmax warps
     def softmax(self):
-        def q_store(n):
+        def q_issue(n):   # the leader loads q_nope of item n into the slots
+            check(self.slots["read"], f"q_nope of item {n} loaded into slots holding unread {self.slots['what']}")
+            self.slots.update(what=("q", n), landed=False, read=False)
+            self.qnfull.arrive(1, tx=2 * QR)
+
+            def land():
+                self.slots["landed"] = True
+                self.qnfull.complete_tx(2 * QR)
+            self.later(land)
+
+        def q_move(n):    # every thread moves its half row into TMEM
+            yield ("wait", self.qnfull, n)
+            check(self.slots["what"] == ("q", n) and self.slots["landed"], f"q_nope of item {n} read from slots "
+                                                                           f"holding {self.slots['what']}")
             check(self.qnope["done"], f"q_nope of item {n} written while item {self.qnope['item']} still reads it")
+            self.slots["read"] = True
             self.qnope.update(item=n, done=False)
             self.qready.arrive(256)
+
         g = 0
         nitems = len(self.nts)
-        q_store(0)
+        q_issue(0)
+        yield from q_move(0)
         for n, nt in enumerate(self.nts):
+            j_q = max(0, nt - 2)
             for j in range(nt):
+                if n + 1 < nitems and j == j_q:
+                    if n > 0 and "no_oread" not in self.faults:
+                        yield ("wait", self.oread, n - 1)
+                    q_issue(n + 1)
+                if j == nt - 1 and n + 1 < nitems and "early_qmove" in self.faults:
+                    yield from q_move(n + 1)
                 yield ("wait", self.sfull[g & 1], g // 2)
                 sb = self.sbuf[g & 1]
                 check(sb["tile"] == g and sb["ready"], f"softmax of tile {g} read S({sb['tile']})")
@@ -261,13 +322,22 @@ class Sim:
                     yield ("wait", self.vfull[g % 2], g // 2)
                     check(self.vslot[g % 2]["tile"] == g, f"cleared the value stage of tile {self.vslot[g % 2]['tile']}")
                 self.pfull.arrive(256)
+                if j == nt - 1 and n + 1 < nitems and "early_qmove" not in self.faults:
+                    yield from q_move(n + 1)
                 g += 1
                 yield None
             yield ("wait", self.pvdone, g - 1)
-            if n + 1 < nitems:
-                q_store(n + 1)
             check(self.o["item"] == n and self.o["pvs"] == nt, f"O of item {n} read out with {self.o['pvs']} of {nt} PVs")
             self.o["read"] = True
+            if n + 1 == nitems and n > 0:
+                yield ("wait", self.oread, n - 1)
+            check(self.slots["read"], f"O of item {n} staged into slots holding unread {self.slots['what']}")
+            vs = self.vslot[(g - 1) % 2]
+            check(vs["tile"] == g - 1 and vs["done"] and vs["o"] is None,
+                  f"O of item {n} staged into the value stage of tile {vs['tile']} (PV done: {vs['done']})")
+            self.slots.update(what=("o", n), landed=True, read=False)
+            vs["o"] = n
+            self.ostaged.arrive(256)
             yield None
 
     def run(self):
@@ -330,15 +400,19 @@ def test_protocol_holds_under_random_schedules(shape):
             assert Sim(nts, seed).run()
 
 
-@pytest.mark.parametrize("fault", ["no_qrfree", "no_kempty", "no_pvdone", "pv_after_qready"])
+@pytest.mark.parametrize("fault", ["no_qrfree", "no_kempty", "no_pvdone", "early_qmove", "no_ostaged",
+                                   "no_oread"])
 def test_the_model_catches_a_broken_rule(fault):
     # - no_qrfree: q^R of the next item is loaded without waiting for the last score
     #   products of the current one;
     # - no_kempty: a key stage is reloaded without waiting for the score products of the
     #   tile two back;
     # - no_pvdone: P(g) is written without waiting for PV(g-1);
-    # - pv_after_qready: the last aggregation of an item is issued after the wait for the
-    #   next item's q_nope, which the softmax warps store only once it is done (deadlock).
+    # - early_qmove: the next item's q_nope is moved into TMEM before the softmax has seen
+    #   the item's last scores (whose products may still read the current q_nope);
+    # - no_ostaged: O is stored without waiting for the softmax warps to stage it;
+    # - no_oread: the next q_nope is loaded into the slots without waiting for the previous
+    #   O to be read out of them.
     caught = 0
     for seed in range(40):
         try:
