@@ -45,7 +45,7 @@ DECODE_SOURCES = ["mla_latent_kv_70_b300/csrc/decode_sm103.cu",
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3_decode", choices=sorted(I.WORKLOADS) + sorted(EXTRA))
