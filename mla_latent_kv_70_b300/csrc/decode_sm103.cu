@@ -149,6 +149,7 @@ struct Maps {
   CUtensorMap kv_lat;    // cache rows, box 64 cols x 64 rows, 128B swizzle; FP8: bytes, box 256 x 64
   CUtensorMap kv_rope;   // cache rows, box 32 cols x 64 rows, 64B swizzle (FP8: rows as 320 bf16)
   CUtensorMap q_rope;    // q_cat rows, box 32 cols x 128 rows, 64B swizzle
+  CUtensorMap q_lat;     // q_cat rows, box 64 cols x 128 rows, 128B swizzle (bf16 cache: q~ staged)
   CUtensorMap o_store;   // output rows (o_lat or split partials) fp32, box 32 cols x H rows, 128B swizzle
   CUtensorMap kv_scale;  // FP8: the row scales as one line of fp32, box 64
 };
@@ -158,6 +159,12 @@ struct Maps {
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kStageChunk = 128 * 128;
 static_assert(kOffStage + 8 * kStageChunk <= kOffQRope, "staging stays clear of q^R and the exchange buffers");
+
+// bf16 cache: this CTA's 256 q~ columns of the 128 head rows land by TMA in the V ring
+// (four 64-column boxes, 128B-swizzled), which takes its first tile only after groups 0
+// and 1 have moved them into TMEM.
+constexpr uint32_t kQLatBox = 128 * 128;
+static_assert(4 * kQLatBox == kVStages * kLatBytes, "q~ fills the V ring");
 
 __device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int t) {
   return p.block_table[(int64_t)b * p.max_pages + t / kPage];
@@ -366,14 +373,19 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
       prefetch_tmap(&maps.kv_lat);
       prefetch_tmap(&maps.kv_rope);
       prefetch_tmap(&maps.q_rope);
+      prefetch_tmap(&maps.q_lat);
       int issued = 0, rope_issued = 0;
       bool q_issued = false;
-      // q^R comes from q_cat, which the previous kernel writes: it is requested after the
-      // first tiles (which no kernel writes), and before the first wait that needs QK(0).
+      // q^R and q~ come from q_cat, which the previous kernel writes: they are requested
+      // after the first tiles (which no kernel writes), and before the first wait that
+      // needs QK(0).  q~ goes to the V ring (groups 0 and 1 move it into TMEM).
       auto load_q = [&]() {
         grid_dep_wait();
-        mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes);
+        mbar_arrive_expect_tx(bar(kQFull), kQRopeBytes + 4 * kQLatBox);
         tma_load_2d(s0 + kOffQRope, &maps.q_rope, bar(kQFull), kDc + 32 * (int)rank, m * p.H);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(s0 + kOffV + (uint32_t)j * kQLatBox, &maps.q_lat, bar(kQFull), 256 * (int)rank + 64 * j,
+                      m * p.H);
         q_issued = true;
       };
       auto qk_done = [&](int j) {
@@ -503,10 +515,11 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
                       256 * (int)rank + 64 * j, y);
       };
       int v_issued = 0;
-      // The first V tiles re-read latent rows that the score ring requested first: asked
-      // for once those have landed, they are L2 hits rather than part of the start-up
-      // burst from HBM.
-      for (; v_issued < min(kVStages, ntiles); ++v_issued) {
+      // The V ring holds q~ until groups 0 and 1 have moved it into TMEM.  The first V tiles
+      // re-read latent rows that the score ring requested first: asked for once those have
+      // landed, they are L2 hits rather than part of the start-up burst from HBM.
+      if (!mbar_wait(bar(kQReady), 0, wait_ns)) aborted = true;
+      for (; !aborted && v_issued < min(kVStages, ntiles); ++v_issued) {
         if (!mbar_wait(bar(kQkFull + v_issued), 0u, wait_ns)) break;
         load_v(v_issued);
       }
@@ -565,22 +578,31 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
     float* mref_sh = reinterpret_cast<float*>(smem + kOffMref);
     if (g < 2) {
       // Half g of this head's 256 q~ columns into TMEM (A operand of the score MMA,
-      // bf16 pairs packed in 32-bit columns).
-      const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * g);
+      // bf16 pairs packed in 32-bit columns): from the boxes 2g and 2g+1 staged in the V
+      // ring (row h, 16-byte chunk v at v ^ (h & 7)), or (FP8 cache) from q_cat itself.
+      bool got = true;
+      if (!kFp8) got = warp_wait(bar(kQFull), 0, wait_ns);
+      if (got) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + qrow * kRow + 256 * rank + 128 * g);
 #pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          const uint32_t box = s0 + kOffV + (uint32_t)(2 * g + c) * kQLatBox + (uint32_t)h * 128u;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 w = head_ok ? src[c * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * v] = w.x;
-          r[4 * v + 1] = w.y;
-          r[4 * v + 2] = w.z;
-          r[4 * v + 3] = w.w;
+          for (int v = 0; v < 8; ++v) {
+            const uint4 w = !kFp8 ? ld_shared_u4(box + (uint32_t)((v ^ (h & 7)) << 4))
+                                  : head_ok ? src[c * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+            r[4 * v] = w.x;
+            r[4 * v + 1] = w.y;
+            r[4 * v + 2] = w.z;
+            r[4 * v + 3] = w.w;
+          }
+          tmem_st32(tb + lane_off + kTmemQ + 64u * g + 32u * c, r);
         }
-        tmem_st32(tb + lane_off + kTmemQ + 64u * g + 32u * c, r);
+        tmem_st_wait();
+      } else {
+        aborted = true;
       }
-      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kQReady));
     }
@@ -905,7 +927,7 @@ k_decode_sm103(const __grid_constant__ Maps maps, const DecodeParams p) {
         for (int c = g; c < 8; c += kGroups)
           tma_store_2d(&maps.o_store, 256 * (int)rank + 32 * c, y, s0 + kOffStage + (uint32_t)c * kStageChunk);
         bulk_commit_group();
-        bulk_wait_group0();
+        bulk_wait_group_read0();   // the staging outlives its reads; the writes finish with the grid
       }
     }
     if (g == 0 && head_ok && rank == 0)
@@ -947,6 +969,7 @@ cudaError_t launch_decode_impl(DecodeParams p, cudaStream_t st) {
   const bool scale_ok = !kFp8 || encode_tma_2d(&maps.kv_scale, false, p.kv_scale, kv_rows, 1,
                                                (kv_rows * 4 + 15) & ~uint64_t(15), kN, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (!kv_ok || !scale_ok || !encode_rows(&maps.q_rope, p.q_cat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_rows(&maps.q_lat, p.q_cat, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tma_2d(&maps.o_store, false, p.o_out, kDc, o_rows, (uint64_t)kDc * 4, 32, (uint32_t)p.H,
                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;

@@ -255,7 +255,7 @@ k_expand_kv(const __grid_constant__ ExpandMaps maps, const ExpandParams p) {
         }
       }
     }
-    if (leader) bulk_wait_group0();   // every store complete before exit
+    if (leader) bulk_wait_group_read0();   // the staging outlives its reads; the writes finish with the grid
   }
 
   if (!ok) raise_flag(p.status, kFlagTimeout);

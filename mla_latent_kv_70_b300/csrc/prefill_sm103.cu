@@ -317,7 +317,7 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       }
       while (!aborted && pend_n > 0)
         if (!store_o()) aborted = true;
-      bulk_wait_group0();   // every store complete before exit
+      bulk_wait_group_read0();   // the staging outlives its reads; the writes finish with the grid
       for (uint32_t i = g > (uint32_t)kPVStages ? g - kPVStages : 0u; i < g; ++i)   // no copy may land after exit
         mbar_wait(bar(kPVFullB + i % kPVStages), (i / kPVStages) & 1u, kDefaultWaitNs);
     }

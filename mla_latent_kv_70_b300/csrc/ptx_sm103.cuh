@@ -269,7 +269,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // 2D tile store from this CTA's shared memory to global memory, tracked by the issuing
-// thread's bulk async-group (bulk_commit_group / bulk_wait_group0).
+// thread's bulk async-group (bulk_commit_group / bulk_wait_group_read0).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
                "r"(y), "r"(src)
@@ -285,9 +285,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int32_t x, 
 }
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Wait until every committed bulk group of this thread has completed (its writes done).
-__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Wait until every committed bulk group of this thread has read its shared-memory source.
 __device__ __forceinline__ void bulk_wait_group_read0() {

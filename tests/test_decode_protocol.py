@@ -30,7 +30,7 @@ import random
 
 import pytest
 
-LAT, ROPE, VBYTES, QROPE, RECV, SIG, LAT8 = 32768, 4096, 32768, 8192, 16384, 4, 16384
+LAT, ROPE, VBYTES, QROPE, RECV, SIG, LAT8, QLAT = 32768, 4096, 32768, 8192, 16384, 4, 16384, 65536
 
 
 class ProtocolError(AssertionError):
@@ -111,6 +111,8 @@ class CTA:
         self.qk_slot = [Slot() for _ in range(3)]
         self.rope_slot = [Slot() for _ in range(2)]
         self.v_slot = [Slot() for _ in range(2)]
+        # bf16 cache: q~ is staged in the V ring; groups 0 and 1 (eight warps) read it.
+        self.q_lat = {"landed": False, "read": [False] * 8}
         self.s_buf = [{"tile": None, "read": [True] * 4} for _ in range(2)]
         self.recv = [{"tile": None, "landed": [False] * 4, "read": [True] * 4} for _ in range(2)]
         self.p_buf = {"tile": None, "written": [False] * 4, "consumed": True}
@@ -168,8 +170,16 @@ class Sim:
         q_issued = False
 
         def load_q():
-            c.qfull.arrive(1, tx=QROPE)
-            self.later(lambda: c.qfull.complete_tx(QROPE))
+            if self.fp8:
+                c.qfull.arrive(1, tx=QROPE)
+                self.later(lambda: c.qfull.complete_tx(QROPE))
+                return
+            c.qfull.arrive(1, tx=QROPE + QLAT)
+
+            def land():
+                c.q_lat["landed"] = True
+                c.qfull.complete_tx(QROPE + QLAT)
+            self.later(land)
 
         for i in range(n):
             if i >= 1 and not q_issued:
@@ -256,6 +266,7 @@ class Sim:
         def load_v(i):
             v = c.v_slot[i % 2]
             check(v.done, f"r{c.rank}: V slot {i % 2} refilled for tile {i} before PV of tile {v.tile} finished")
+            check(all(c.q_lat["read"]), f"r{c.rank}: V slot {i % 2} refilled for tile {i} while q~ is still unread")
             v.tile, v.landed, v.done = i, False, False
             c.vfull[i % 2].arrive(1, tx=VBYTES)
 
@@ -281,6 +292,8 @@ class Sim:
                 self.later_in_order(("pv", c.rank), done8)
                 yield None
             return
+        if "no_qready_v" not in self.faults:
+            yield ("wait", c.qready, 0)      # the V ring holds q~ until it is in TMEM
         for i in range(min(2, n)):
             # The first V tiles are requested once the same rows have landed in the score
             # ring (phase 0 of its slot), so that they come from L2.
@@ -329,7 +342,13 @@ class Sim:
     def group_warp(self, c, peer, g, q):
         n = self.n
         if g < 2:
-            c.qready.arrive(32)            # this warp's q~ columns are in TMEM
+            if self.fp8:
+                c.qready.arrive(32)        # this warp's q~ columns are in TMEM (read from q_cat)
+            else:
+                yield ("wait", c.qfull, 0)
+                check(c.q_lat["landed"], f"r{c.rank} g{g}: q~ read from the V ring before it landed")
+                c.q_lat["read"][4 * g + q] = True
+                c.qready.arrive(32)        # this warp's q~ columns are in TMEM
         if q == 0 and g < n:
             c.recvfull[g].arrive(1, tx=RECV)
         if self.fp8 and g < n:
@@ -482,9 +501,11 @@ def test_fp8_slot_empty_wait_is_implied(n):
         assert Sim(n, seed, False, faults=["no_slotempty"], fp8=True).run()
 
 
-@pytest.mark.parametrize("fault", ["no_sfree", "no_freeseen", "no_vgo"])
+@pytest.mark.parametrize("fault", ["no_sfree", "no_freeseen", "no_vgo", "no_qready_v"])
 def test_the_model_catches_a_broken_rule(fault):
     # Each planted mistake leaves out one rule of the protocol:
+    # - no_qready_v: the aggregation issuer requests the first V tiles before groups 0 and
+    #   1 have moved q~ out of the V ring;
     # - no_sfree: the score issuer overwrites S buffer i & 1 before the group of tile i-2
     #   read it;
     # - no_freeseen: the groups wait for the peer's "free" signals out of tile order, so a
