@@ -5,7 +5,7 @@
 // the per-head keys and values; page "MLA의 계산: KV를 펼치지 않고 Attention하기", section
 // "계산 재배치의 효과와 한계": the absorbed order pays d_c-wide dot products per key, which
 // pays off only when reading the cache dominates (decode).  Here:
-//   K_h = C W_UK[h], V_h = C W_UV[h]  (the batched GEMM of gemm_sm103.cu), then for each
+//   K_h = C W_UK[h], V_h = C W_UV[h]  (k_expand_kv, expand_sm103.cu), then for each
 //   head, causal attention of the T_q query tokens (the last T_q of T_kv positions) over
 //   [K_h | k^R] with [q_nope | q^R], one scale, and V_h mixed by the weights.
 //
@@ -17,8 +17,9 @@
 // in L2).  TMEM holds O (128 columns), two score buffers (128 each), q_nope as the A
 // operand of the score products (64 columns of bf16 pairs) and P as the A operand of the
 // aggregation (64 columns); shared memory holds the key tiles [K_h | k^R] (48 KB, a ring
-// of two), the value tiles V_h (32 KB, a ring of two), q^R and two 16 KB slots through
-// which q_nope arrives and O leaves by TMA.  Per key tile j:
+// of two), the value tiles V_h (32 KB, a ring of two), q^R and two 16 KB slots.  q_nope
+// comes in by TMA through the slots; O goes out by TMA through the slots and the value
+// stage of the item's last tile, stored by the value producer.  Per key tile j:
 //   S(j) [128 x 128] = q_nope . K_h(j)^T (8 MMAs, A from TMEM) + q^R . k^R(j)^T (4 MMAs)
 //   O [128 x 128]   += P(j-1) [128 x 128] . V(j-1)  (8 MMAs, A from TMEM)
 // The rings, the score buffers and P run on from one item to the next: the score products
@@ -28,9 +29,9 @@
 // their operand reads).  Warps 0-7 run the online softmax, two threads per query row
 // (TMEM lane = row; warp w takes key columns [64 (w / 4), 64 (w / 4) + 64)), the pair
 // agreeing on the row maximum through shared memory; they also move the next item's
-// q_nope from the slots into TMEM during the current item's last tile.  Warps 8 and 10 stream the key
-// and value tiles by TMA; warp 9 issues the MMAs, S(j+1) running while the softmax of tile
-// j does.  The running maximum is raised lazily (O is rescaled only when a row's maximum
+// q_nope from the slots into TMEM during the current item's last tile.  Warps 8 and 10
+// stream the key and value tiles by TMA; warp 9 issues the MMAs, S(j+1) running while the
+// softmax of tile j does.  The running maximum is raised lazily (O is rescaled only when a row's maximum
 // grows by more than 2^8), as in the latent decode.  Key tiles past the last query's
 // position are not loaded.  Every wait is bounded; on expiry the CTA records
 // MLA_ERR_TIMEOUT, drains and exits.
