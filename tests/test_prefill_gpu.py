@@ -51,10 +51,12 @@ def prefill_lse_tolerance(qn, qr, C, KR, w_uk, scale, heads):
 # in the value tile); 512/600 and 600/900 are chunked prefill (the queries are the last T_q
 # positions).  Blocks i and n-1-i of a head form one unit of the persistent schedule:
 # 1024 with 128 heads and 600/900 with two sequences of 64 heads give each CTA several
-# units, and the five blocks of 600 leave the middle one without a partner.
+# units, and the five blocks of 600 leave the middle one without a partner.  One query
+# over 5 rows, and one over one row, are the smallest chunks.
 @pytest.mark.parametrize("B,T_q,T_kv,H", [(2, 300, 300, 16), (1, 130, 700, 16), (1, 64, 64, 32),
                                           (1, 200, 1000, 128), (1, 200, 200, 16), (1, 512, 600, 16),
-                                          (1, 1024, 1024, 128), (2, 600, 900, 64)])
+                                          (1, 1024, 1024, 128), (2, 600, 900, 64), (3, 1, 5, 16),
+                                          (1, 1, 1, 16)])
 def test_prefill_matches_oracle(B, T_q, T_kv, H):
     import mla_latent_kv_70_b300 as mla
     case = I.make_case("prefill", B, T_q, H, [T_kv] * B, causal=True, seed=91, t_cap=T_kv + 40)
