@@ -122,9 +122,13 @@ k_expand_kv(const __grid_constant__ ExpandMaps maps, const ExpandParams p) {
       int64_t blk = -1;
       int a_loads = 0;
       uint32_t g = 0;   // slices issued
-      for (int64_t u = u0; u < u1 && ok; ++u) {
-        const int64_t rb = u / p.H;
-        const int h = (int)(u % p.H);
+      int64_t rb = u0 / p.H;   // unit u = (row block rb, head h), counted without divisions
+      int h = (int)(u0 % p.H);
+      for (int64_t u = u0; u < u1 && ok; ++u, ++h) {
+        if (h == p.H) {
+          h = 0;
+          ++rb;
+        }
         if (rb != blk) {   // a new row block, once the MMAs of the previous one are done
           if (a_loads > 0 && !mbar_wait(bar(kXAFree), (uint32_t)(a_loads - 1) & 1u, kDefaultWaitNs)) {
             ok = false;
@@ -166,8 +170,13 @@ k_expand_kv(const __grid_constant__ ExpandMaps maps, const ExpandParams p) {
       int a_loads = 0;
       uint32_t g = 0;
       int i = 0;   // units of this CTA so far
-      for (int64_t u = u0; u < u1 && ok; ++u, ++i) {
-        const int64_t rb = u / p.H;
+      int64_t rb = u0 / p.H;
+      int h = (int)(u0 % p.H);
+      for (int64_t u = u0; u < u1 && ok; ++u, ++i, ++h) {
+        if (h == p.H) {
+          h = 0;
+          ++rb;
+        }
         if (rb != blk) {
           if (!mbar_wait(bar(kXAFull), (uint32_t)a_loads & 1u, kDefaultWaitNs)) {
             ok = false;
@@ -202,7 +211,7 @@ k_expand_kv(const __grid_constant__ ExpandMaps maps, const ExpandParams p) {
         }
         if (!ok) break;
         mma_commit(bar(kXAccFull + ab));
-        if (u + 1 < u1 && (u + 1) / p.H != rb) mma_commit(bar(kXAFree));
+        if (u + 1 < u1 && h + 1 == p.H) mma_commit(bar(kXAFree));   // the next unit starts a row block
       }
       mma_commit(bar(kXDrain));   // tracks every MMA issued
       mbar_wait(bar(kXDrain), 0, kDefaultWaitNs);
@@ -215,9 +224,13 @@ k_expand_kv(const __grid_constant__ ExpandMaps maps, const ExpandParams p) {
     const bool leader = warp == kXEpiWarp0 && lane == 0;
     const uint32_t stg = s0 + kXOffStg + (uint32_t)r * 128u;
     int i = 0;
-    for (int64_t u = u0; u < u1; ++u, ++i) {
-      const int64_t rb = u / p.H;
-      const int h = (int)(u % p.H);
+    int64_t rb = u0 / p.H;
+    int h = (int)(u0 % p.H);
+    for (int64_t u = u0; u < u1; ++u, ++i, ++h) {
+      if (h == p.H) {
+        h = 0;
+        ++rb;
+      }
       const int ab = i & 1;
       const bool got = !__any_sync(0xffffffffu, !mbar_wait(bar(kXAccFull + ab), (uint32_t)(i >> 1) & 1u,
                                                             kDefaultWaitNs));
