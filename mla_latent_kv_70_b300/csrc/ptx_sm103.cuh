@@ -45,18 +45,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
                : "memory");
 }
 
-// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
-// completes or about kSuspendNs pass, so waiting warps do not take issue slots from the
-// warps that share their sub-partition.
-constexpr uint32_t kSuspendNs = 20000;
-
+// try_wait without a suspend-time hint: the thread may be suspended for a system-dependent
+// time until the phase completes (with a 20 us hint the prefill ran 1.3% and the decode
+// 0.3% slower).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
 }
@@ -77,10 +75,10 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
 }
