@@ -14,9 +14,10 @@
 // head go in pairs (query block i with block n-1-i: for a whole prompt their key tile
 // counts add up to a constant), the pairs dealt round-robin, so that every CTA carries the
 // same work and the CTAs running at one time share heads (their key and value tiles meet
-// in L2).  TMEM holds O (128 columns), two score buffers (128 each), q_nope as the A
-// operand of the score products (64 columns of bf16 pairs) and P as the A operand of the
-// aggregation (64 columns); shared memory holds the key tiles [K_h | k^R] (48 KB, a ring
+// in L2).  TMEM holds O (128 columns), two score buffers (128 each) and q_nope as the A
+// operand of the score products (64 columns of bf16 pairs).  P(j), the A operand of the
+// aggregation, is written into the score buffer of S(j) over the columns its thread has
+// read, so P is double-buffered with S; shared memory holds the key tiles [K_h | k^R] (48 KB, a ring
 // of two), the value tiles V_h (32 KB, a ring of two), q^R and two 16 KB slots.  q_nope
 // comes in by TMA through the slots; O goes out by TMA through the slots and the value
 // stage of the item's last tile, stored by the value producer.  Per key tile j:
@@ -72,9 +73,10 @@ static_assert(kPOffV % 1024 == 0 && kPOffQR % 1024 == 0 && kPOffOst % 1024 == 0,
 
 // TMEM columns.
 constexpr uint32_t kPTmemO = 0;      // [0,128)   O, fp32
-constexpr uint32_t kPTmemS = 128;    // [128,384) two score buffers of 128 fp32
-constexpr uint32_t kPTmemQ = 384;    // [384,448) q_nope, bf16 pairs
-constexpr uint32_t kPTmemP = 448;    // [448,512) P, bf16 pairs
+constexpr uint32_t kPTmemS = 128;    // [128,384) two score buffers of 128 fp32; P(j) in
+                                     // buffer j & 1, keys 0-63 in columns [0,32) and keys
+                                     // 64-127 in [64,96), bf16 pairs
+constexpr uint32_t kPTmemQ = 384;    // [384,448) q_nope, bf16 pairs; [448,512) unused
 constexpr float kPRescale = 8.0f;
 
 // Tiles count up across the items of a CTA (g); items count up too (n).
@@ -91,9 +93,9 @@ enum PBar {
   kPVEmptyB = kPVFullB + kPVStages,     // [2] aggregation of the stage done
   kPSFullB = kPVEmptyB + kPVStages,     // [2] S buffer ready
   kPSFreeB = kPSFullB + 2,              // [2] S buffer read (8 warps)
-  kPPFullB = kPSFreeB + 2,              // P in TMEM (256 threads)
-  kPPvDoneB,                            // PV(g) done: P free, O stable
-  kPDrainB,
+  kPPFullB = kPSFreeB + 2,              // [2] P(g) in TMEM, by g & 1 (256 threads)
+  kPPvDoneB = kPPFullB + 2,             // [2] PV(g) done, by g & 1: O stable
+  kPDrainB = kPPvDoneB + 2,
   kPNumBars
 };
 static_assert(kPNumBars * 8 + 16 <= 256, "barrier area");
@@ -186,7 +188,9 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
       mbar_init(bar(kPSFreeB + i), kPSoftWarps);
     }
     mbar_init(bar(kPPFullB), 32 * kPSoftWarps);
+    mbar_init(bar(kPPFullB + 1), 32 * kPSoftWarps);
     mbar_init(bar(kPPvDoneB), 1);
+    mbar_init(bar(kPPvDoneB + 1), 1);
     mbar_init(bar(kPDrainB), 1);
     fence_mbar_init();
   }
@@ -326,26 +330,30 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
     // ---------------- MMA issuer ----------------
     // Tile g: S(g) once the softmax has read buffer g & 1 at tile g-2 (8 MMAs with q_nope
     // from TMEM against the two K_h boxes, 4 with q^R from shared memory against k^R),
-    // then PV(g-1) once P(g-1) is in TMEM (8 MMAs, A = P from TMEM, B = the value tile
-    // read MN-major).  The first PV of an item overwrites O: the softmax warps write its P
-    // only after reading the previous item's O out of TMEM.  The last PV of an item goes
-    // out before the wait for the next item's q^R and q_nope.
+    // then PV(g-1) once P(g-1) is in TMEM (8 MMAs, A = P from score buffer (g-1) & 1, B =
+    // the value tile read MN-major).  PV(g-1) is thus always issued before S(g+1), which
+    // overwrites its P: the MMAs of one thread run in issue order.  The softmax warps may
+    // write P(g) before this thread has waited for P(g-1), but not P(g+1) (it needs S(g+1)),
+    // so the P barriers go by parity and none runs two phases ahead of its waiter.  The first PV of an item
+    // overwrites O: the softmax warps write its P only after reading the previous item's O
+    // out of TMEM.  The last PV of an item goes out before the wait for the next item's q^R
+    // and q_nope.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16(128, kPKeys, false, false);
       const uint32_t id_o = idesc_bf16(128, 128, false, true);
       const uint64_t qr_desc = smem_desc(s0 + kPOffQR, 16, 1024, kSwizzle128B);
       auto pv = [&](uint32_t gi, bool first) {   // O (+)= P(gi) V(gi)
         const uint32_t vs = gi % kPVStages;
-        if (!mbar_wait(bar(kPPFullB), gi & 1u, kDefaultWaitNs) ||
+        if (!mbar_wait(bar(kPPFullB + (gi & 1u)), (gi >> 1) & 1u, kDefaultWaitNs) ||
             !mbar_wait(bar(kPVFullB + vs), (gi / kPVStages) & 1u, kDefaultWaitNs))
           return false;
         tc_fence_after();
         const uint64_t vd = smem_desc(s0 + kPOffV + vs * kPVBytes, kPBox, 1024, kSwizzle128B);
 #pragma unroll
         for (int k = 0; k < kPKeys / 16; ++k)
-          mma_ts(tb + kPTmemO, tb + kPTmemP + 8u * k, vd + 128u * k, id_o, (!first || k > 0) ? 1u : 0u);
+          mma_ts(tb + kPTmemO, tb + kPTmemS + 128u * (gi & 1u) + 8u * k + (k >= 4 ? 32u : 0u), vd + 128u * k, id_o, (!first || k > 0) ? 1u : 0u);
         mma_commit(bar(kPVEmptyB + vs));
-        mma_commit(bar(kPPvDoneB));
+        mma_commit(bar(kPPvDoneB + (gi & 1u)));
         return true;
       };
       int u = blockIdx.x;
@@ -523,14 +531,18 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
           pw[c] = f2_to_bf2(a, e);
         }
         l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        // The P columns are free, and O stable, once PV(g-1) is done.
-        if (g >= 1 && !pwarp_wait(bar(kPPvDoneB), (g - 1) & 1u)) {
+        // P(g) goes over the S(g) columns this thread has read, so it waits for nothing.  O
+        // is stable once PV(g-1) is done: a rescale waits for that.  (At tile g the barrier of
+        // PV(g-1) is in its phase or one past it: PV(g-3) preceded S(g-1), and PV(g+1) needs
+        // P(g+1).)
+        const bool resc = __any_sync(0xffffffffu, grow && j > 0);
+        if (resc && !pwarp_wait(bar(kPPvDoneB + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) {
           failed = true;
           continue;
         }
         tc_fence_after();
-        tmem_st32(tb + lane_off + kPTmemP + 32u * (uint32_t)hf, pw);
-        if (__any_sync(0xffffffffu, grow && j > 0)) {   // rescale this thread's half of its O row
+        tmem_st32(tb + lane_off + kPTmemS + 128u * (g & 1) + 64u * (uint32_t)hf, pw);
+        if (resc) {   // rescale this thread's half of its O row
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
@@ -559,13 +571,13 @@ k_prefill_attn(const __grid_constant__ PrefillMaps maps, const PrefillParams p) 
           fence_proxy_async_smem();
         }
         tc_fence_before();
-        mbar_arrive(bar(kPPFullB));
+        mbar_arrive(bar(kPPFullB + (g & 1)));
         // The item's score products are done (S of its last tile was read): the next
         // item's q_nope goes into TMEM.
         if (j == it.nt - 1 && have_nx && !q_move(n + 1)) failed = true;
       }
       // Epilogue: the row sum of both halves, then this thread's half of O / l, and the LSE.
-      if (!aborted && !failed && !pwarp_wait(bar(kPPvDoneB), (g - 1) & 1u)) failed = true;
+      if (!aborted && !failed && !pwarp_wait(bar(kPPvDoneB + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) failed = true;
       tc_fence_after();
       red[hf * 128 + r] = l;
       if (!named_bar_and(pair_bar, 64, !aborted && !failed)) aborted = true;

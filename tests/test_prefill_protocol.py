@@ -9,7 +9,8 @@ softmax warps are modelled as one agent, since they meet at named barriers for e
 The buffers are:
 - the key ring (2 stages) and the value ring (2 stages);
 - q^R and two 16 KB slots in shared memory;
-- q_nope, the two score buffers, P and O in TMEM.
+- q_nope, the two score buffers and O in TMEM. P(g) is written into the score buffer of
+  S(g), so P is double-buffered with S.
 
 The slots carry the next item's q_nope in (loaded by the softmax leader a tile before an
 item's last) and half of an item's O out. The other half goes out through the value stage
@@ -20,7 +21,10 @@ Each buffer is reused only after its last reader is done. The checks are:
 - q^R and q_nope of item n+1 are written only after the last score products of item n;
 - the first aggregation of item n+1 (which overwrites O) starts only after the softmax
   warps have read out O of item n (implied: they write its P after that);
-- P(g) is written only after PV(g-1);
+- S(g) overwrites P(g-2) only after PV(g-2) has been issued (the MMAs of one thread run
+  in issue order, so PV(g-2) has read P(g-2) by then);
+- O is rescaled (at a tile where a row's maximum grows) only after PV(g-1), and read out
+  only after the item's last PV;
 - the slots take q_nope only after the previous O has been read out of them, and O only
   after that q_nope has been moved to TMEM;
 - a value stage takes O only after its PV, and the next tile only after O has been read
@@ -28,7 +32,9 @@ Each buffer is reused only after its last reader is done. The checks are:
 - and so on for the score buffers and the value ring.
 
 Copies complete at random later times. MMA commits complete in issue order, also later.
-A wait returns only on the phase it means (parity semantics, with the phase checked).
+A wait returns only on the phase it means (parity semantics, with the phase checked):
+the softmax waits for the PV barriers only now and then, so this also checks that such a
+barrier is never two phases past the one waited for.
 A rule left out shows up as a failed check or a deadlock.
 
 The item list restates the kernel's schedule: unit u (dealt round-robin over the CTAs) is
@@ -108,7 +114,12 @@ class Sim:
         self.vempty = [B(f"VEmpty{i}", 1) for i in range(2)]
         self.sfull = [B(f"SFull{i}", 1) for i in range(2)]
         self.sfree = [B(f"SFree{i}", 8) for i in range(2)]
-        self.pfull, self.pvdone = B("PFull", 256), B("PvDone", 1)
+        self.pfull = [B(f"PFull{i}", 256) for i in range(2)]
+        if "one_pfull" in self.faults:      # one P barrier for all tiles: phase g, not g // 2
+            self.pfull = [self.pfull[0]] * 2
+        self.pf = (lambda t: (self.pfull[0], t)) if "one_pfull" in self.faults else \
+            (lambda t: (self.pfull[t & 1], t // 2))
+        self.pvdone = [B(f"PvDone{i}", 1) for i in range(2)]
         self.qnfull, self.ostaged, self.oread = B("QnFull", 1), B("OStaged", 256), B("ORead", 1)
         # Buffer state: occupant and whether its readers are done.
         self.kslot = [{"tile": None, "landed": False, "done": True} for _ in range(2)]
@@ -116,8 +127,8 @@ class Sim:
         self.slots = {"what": None, "landed": True, "read": True}   # ("q", n) or ("o", n)
         self.qrope = {"item": None, "landed": False, "done": True}
         self.qnope = {"item": None, "done": True}
-        self.sbuf = [{"tile": None, "ready": False, "read": True} for _ in range(2)]
-        self.p = {"tile": None, "consumed": True}
+        self.sbuf = [{"tile": None, "ready": False, "read": True, "p": None, "p_issued": True}
+                     for _ in range(2)]
         self.o = {"item": None, "pvs": 0, "read": True}
         self.qk_done = {}                       # tile -> score products complete
         self.item_of = []                       # tile -> item
@@ -217,9 +228,11 @@ class Sim:
     # ---- the MMA issuer
     def pv(self, gi):
         n = self.item_of[gi]
-        yield ("wait", self.pfull, gi)
+        yield ("wait", *self.pf(gi))
         yield ("wait", self.vfull[gi % 2], gi // 2)
-        check(self.p["tile"] == gi and not self.p["consumed"], f"PV({gi}) read P of tile {self.p['tile']}")
+        sb = self.sbuf[gi & 1]
+        check(sb["p"] == gi and not sb["p_issued"], f"PV({gi}) read P of tile {sb['p']}")
+        sb["p_issued"] = True        # read before any later MMA of this thread writes the buffer
         vs = self.vslot[gi % 2]
         check(vs["tile"] == gi and vs["landed"], f"PV({gi}) read value stage holding {vs['tile']}")
         if self.first[gi]:
@@ -231,9 +244,8 @@ class Sim:
         def done():
             vs["done"] = True
             self.vempty[gi % 2].arrive()
-            self.p["consumed"] = True
             self.o["pvs"] += 1
-            self.pvdone.arrive()
+            self.pvdone[gi & 1].arrive()
         self.commit(done)
 
     def mma(self):
@@ -255,7 +267,8 @@ class Sim:
                 check(self.qnope["item"] == n, f"S({g}) read q_nope of item {self.qnope['item']}")
                 sb = self.sbuf[g & 1]
                 check(sb["read"], f"S({g}) overwrote S({sb['tile']}) before the softmax read it")
-                sb.update(tile=g, ready=False, read=False)
+                check(sb["p"] is None or sb["p_issued"], f"S({g}) overwrote P({sb['p']}) before its PV was issued")
+                sb.update(tile=g, ready=False, read=False, p=None, p_issued=True)
 
                 def sdone(g=g, sb=sb, ks=ks, last=(j == nt - 1), n=n):
                     sb["ready"] = True
@@ -314,19 +327,23 @@ class Sim:
                 check(sb["tile"] == g and sb["ready"], f"softmax of tile {g} read S({sb['tile']})")
                 sb["read"] = True
                 self.sfree[g & 1].arrive(8)
-                if g >= 1 and "no_pvdone" not in self.faults:
-                    yield ("wait", self.pvdone, g - 1)
-                check(self.p["consumed"], f"P({g}) written before PV({self.p['tile']}) was done")
-                self.p.update(tile=g, consumed=False)
+                if j > 0 and self.rng.random() < 0.3:   # a row's maximum grew: O is rescaled
+                    if "no_pvdone" not in self.faults:
+                        yield ("wait", self.pvdone[(g - 1) & 1], (g - 1) // 2)
+                    check(self.o["item"] == n and self.o["pvs"] == j,
+                          f"O rescaled at tile {g} with {self.o['pvs']} of its item's {j} earlier PVs done")
+                check(sb["p"] is None, f"P({g}) written over P({sb['p']})")
+                sb.update(p=g, p_issued=False)
                 if self.rng.random() < 0.3:      # a partial tile: rows past the end cleared
                     yield ("wait", self.vfull[g % 2], g // 2)
                     check(self.vslot[g % 2]["tile"] == g, f"cleared the value stage of tile {self.vslot[g % 2]['tile']}")
-                self.pfull.arrive(256)
+                self.pf(g)[0].arrive(256)
                 if j == nt - 1 and n + 1 < nitems and "early_qmove" not in self.faults:
                     yield from q_move(n + 1)
                 g += 1
                 yield None
-            yield ("wait", self.pvdone, g - 1)
+            if "no_pvdone_epi" not in self.faults:
+                yield ("wait", self.pvdone[(g - 1) & 1], (g - 1) // 2)
             check(self.o["item"] == n and self.o["pvs"] == nt, f"O of item {n} read out with {self.o['pvs']} of {nt} PVs")
             self.o["read"] = True
             if n + 1 == nitems and n > 0:
@@ -400,14 +417,17 @@ def test_protocol_holds_under_random_schedules(shape):
             assert Sim(nts, seed).run()
 
 
-@pytest.mark.parametrize("fault", ["no_qrfree", "no_kempty", "no_pvdone", "early_qmove", "no_ostaged",
-                                   "no_oread"])
+@pytest.mark.parametrize("fault", ["no_qrfree", "no_kempty", "no_pvdone", "no_pvdone_epi", "one_pfull",
+                                   "early_qmove", "no_ostaged", "no_oread"])
 def test_the_model_catches_a_broken_rule(fault):
     # - no_qrfree: q^R of the next item is loaded without waiting for the last score
     #   products of the current one;
     # - no_kempty: a key stage is reloaded without waiting for the score products of the
     #   tile two back;
-    # - no_pvdone: P(g) is written without waiting for PV(g-1);
+    # - no_pvdone: O is rescaled without waiting for PV(g-1);
+    # - no_pvdone_epi: O is read out without waiting for the item's last PV;
+    # - one_pfull: one P barrier for every tile, which the softmax can move two phases past
+    #   the MMA thread's wait;
     # - early_qmove: the next item's q_nope is moved into TMEM before the softmax has seen
     #   the item's last scores (whose products may still read the current q_nope);
     # - no_ostaged: O is stored without waiting for the softmax warps to stage it;
